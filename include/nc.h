@@ -1,0 +1,208 @@
+/*
+ * nc.h -- C ABI of the B300 (sm_103a) forward pass of a nanochat-style GPT.
+ *
+ * The model is the decoder-only transformer the pages describe: token
+ * embedding; per block RMSNorm (no gain), separate Q/K/V projections, rotary
+ * embedding on precomputed cos/sin tables, QK RMS-norm, causal multi-/grouped-
+ * query attention, output projection + residual, RMSNorm, ReLU^2 MLP +
+ * residual; final RMSNorm and an untied LM head. Sources, by page and section:
+ *   - 復刻 ChatGPT 有多難？ (jxzklqfsx.com), section 為什么可以訓練如此之快:
+ *     own RoPE that splits a vector into two halves and rotates them; Q, K, V as
+ *     separate linear layers; ReLU2 activation; cos/sin precomputed and kept in
+ *     GPU memory; KV cache with a branch on whether the cache exists; dense MLP.
+ *   - 8000行手写代码！nanochat (hongdingcd.com): dense Transformer, rotary
+ *     embedding, QK normalisation; MQA and the KV cache for single-GPU inference.
+ *   - CSDN nanochat article (wap.jaobe.com), inference paragraph: an Engine with
+ *     a KV cache and the two phases prefill and decode.
+ *   - Microgpt summary (telegra.ph), sections 模型参数 and 核心架构: RMSNorm
+ *     instead of LayerNorm, no biases, matrices only (embedding, attention, MLP,
+ *     final output projection), softmax, attention over the current and earlier
+ *     positions, two-layer MLP, residual connections, KV cache; section 推理:
+ *     generation feeds the sampled token back, one position at a time.
+ *
+ * Conventions shared by every entry point:
+ *   - Every matrix is row-major [out, in]: y = x W^T. Head h of the Q projection
+ *     owns output rows [h*hd, (h+1)*hd); KV head g likewise.
+ *   - "dev" pointers are CUDA device pointers on the current device; "host"
+ *     pointers are host memory (pinned memory lets copies overlap).
+ *   - Device pointers handed to the library must be 16-byte aligned.
+ *   - `stream` is a cudaStream_t passed as void* (NULL = legacy default stream).
+ *     Work is enqueued asynchronously on it; results are ready once the stream
+ *     is synchronised. A model and its caches are used from one stream at a time.
+ *   - Every call returns an nc_status and never throws. Errors found on the host
+ *     (bad sizes, null or misaligned pointers, positions out of range) return
+ *     at once and enqueue nothing. Errors found on the device (a token id out of
+ *     [0, vocab), an internal wait that timed out) latch in a per-model status
+ *     word that nc_model_check() reads. nc_last_error() gives a thread-local
+ *     text for the last failure.
+ */
+#ifndef NC_H_
+#define NC_H_
+
+#include <stddef.h>
+#include <stdint.h>
+
+#ifdef __cplusplus
+extern "C" {
+#endif
+
+#define NC_API __attribute__((visibility("default")))
+
+typedef enum {
+    NC_OK = 0,
+    NC_ERR_INVALID_ARG = 1,     /* null/misaligned pointer, size or position out of range */
+    NC_ERR_UNSUPPORTED = 2,     /* shape this build has no kernel for */
+    NC_ERR_OOM = 3,             /* device allocation failed */
+    NC_ERR_CUDA = 4,            /* a CUDA runtime/driver call failed */
+    NC_ERR_DEVICE_TIMEOUT = 5,  /* a kernel's bounded wait ran out (device status word) */
+    NC_ERR_BOUNDS = 6           /* a token id outside [0, vocab) was seen (device status word);
+                                   the kernel used row 0 in its place */
+} nc_status;
+
+typedef enum { NC_F32 = 0, NC_BF16 = 1 } nc_dtype;
+
+/* Model shape. dtype is the storage type of weights, activations and the KV
+ * cache: NC_BF16 runs the tensor-core path and needs head_dim == 128,
+ * d_model % 64 == 0 and d_mlp % 64 == 0; NC_F32 runs an fp32 CUDA-core path for
+ * small shapes (head_dim <= 128, even). Residual stream and logits are fp32 for
+ * both. max_batch * max_seq bounds the tokens of one prefill call and max_seq
+ * bounds every position (cos/sin tables are built for max_seq positions). */
+typedef struct {
+    int32_t vocab, d_model, n_layer, n_head, n_kv_head, head_dim, d_mlp;
+    float rope_base;   /* theta(t, i) = t * rope_base^(-2 i / head_dim) */
+    float rms_eps;     /* x / sqrt(mean(x^2) + rms_eps) */
+    int32_t max_seq, max_batch;
+    nc_dtype dtype;
+} nc_config;
+
+/* Weights: device pointers in cfg.dtype, row-major [out, in]. Borrowed: the
+ * caller keeps them alive and unchanged for the model's lifetime. The per-layer
+ * members are HOST arrays of n_layer device pointers (read during create only).
+ *   wte [vocab, d]      lm_head [vocab, d]       (untied)
+ *   wq [H*hd, d]  wk [Hkv*hd, d]  wv [Hkv*hd, d]  wo [d, H*hd]
+ *   w_fc [d_mlp, d]  w_proj [d, d_mlp]                                        */
+typedef struct {
+    const void* wte;
+    const void* lm_head;
+    const void* const* wq;
+    const void* const* wk;
+    const void* const* wv;
+    const void* const* wo;
+    const void* const* w_fc;
+    const void* const* w_proj;
+} nc_weights;
+
+typedef struct nc_model nc_model;
+typedef struct nc_kv_cache nc_kv_cache;
+
+NC_API const char* nc_version(void);
+NC_API const char* nc_status_string(nc_status s);
+/* Thread-local description of the last failing call ("" if none). */
+NC_API const char* nc_last_error(void);
+
+/* Number of weight values of a shape: 2*vocab*d + n_layer*(per-layer matrices). */
+NC_API int64_t nc_param_count(const nc_config* cfg);
+
+/* Validates cfg, builds the cos/sin tables (computed in fp64 on the host, stored
+ * fp32 on the device), allocates the workspace for max_batch*max_seq tokens and
+ * the device status word, and builds the TMA descriptors of the weights. Uses the
+ * current CUDA device. On failure *out is NULL and nothing is leaked. */
+NC_API nc_status nc_model_create(const nc_config* cfg, const nc_weights* w, nc_model** out);
+NC_API void nc_model_destroy(nc_model* m);
+
+/* Bytes of a KV cache: 2 (K and V) * n_layer * batch * n_kv_head * t_max * head_dim
+ * * sizeof(dtype), plus 256 bytes of header. Layout of K (and V):
+ * [n_layer][batch][n_kv_head][t_max][head_dim]; K is stored after RoPE and QK
+ * norm, V as projected. */
+NC_API size_t nc_kv_cache_bytes(const nc_config* cfg, int32_t batch, int32_t t_max);
+
+/* Creates a cache for `batch` sequences of up to t_max positions (t_max <= cfg
+ * max_seq). mem == NULL: the library allocates and owns the memory. Otherwise
+ * mem is a caller-owned device buffer of nc_kv_cache_bytes() bytes (256-byte
+ * aligned) that must outlive the cache. Starts with length 0. */
+NC_API nc_status nc_kv_cache_alloc(const nc_model* m, int32_t batch, int32_t t_max, void* mem,
+                                   nc_kv_cache** out);
+/* Device pointers to the K and V arrays and the number of filled positions. */
+NC_API nc_status nc_kv_cache_view(const nc_kv_cache* c, void** k, void** v, int32_t* len,
+                                  int32_t* batch, int32_t* t_max);
+NC_API void nc_kv_cache_free(nc_kv_cache* c);
+
+/* Prefill: runs tokens (dev int32 [B, T]) from position 0 through the model,
+ * writes K/V of positions 0..T-1 of sequences 0..B-1 into the cache and sets its
+ * length to T. logits (dev fp32 [B, T, vocab]) receives every position's
+ * logits. Requires 1 <= B <= cache batch, B <= max_batch, 1 <= T <= cache t_max.
+ * (CSDN nanochat article, Engine paragraph: the prefill phase.) */
+NC_API nc_status nc_prefill(nc_model* m, const int32_t* tokens, int32_t B, int32_t T,
+                            float* logits, nc_kv_cache* c, void* stream);
+
+/* As nc_prefill, but the LM head runs only on position T-1 of each sequence:
+ * logits_last (dev fp32 [B, vocab], may be NULL) and argmax_out (dev int32 [B],
+ * may be NULL; the greedy next token, lowest index on ties). */
+NC_API nc_status nc_prefill_last(nc_model* m, const int32_t* tokens, int32_t B, int32_t T,
+                                 float* logits_last, int32_t* argmax_out, nc_kv_cache* c,
+                                 void* stream);
+
+/* One decode step: token (dev int32 [B]) of each sequence at position pos, which
+ * must equal the cache length; K/V are appended at pos, attention runs over
+ * positions 0..pos, the cache length becomes pos+1. logits (dev fp32 [B, vocab],
+ * may be NULL if argmax_out is given) and argmax_out (dev int32 [B] or NULL;
+ * may alias tokens). (jxzklqfsx.com, KV cache paragraph; Microgpt summary 推理.) */
+NC_API nc_status nc_decode_step(nc_model* m, const int32_t* tokens, int32_t B, int32_t pos,
+                                float* logits, int32_t* argmax_out, nc_kv_cache* c, void* stream);
+
+/* Greedy generation with HOST buffers: copies prompt (host int32 [B, T]) to the
+ * device, prefills (token 0 = argmax of the last prompt position), then runs
+ * `steps` decode steps, step j feeding token j back at position T + j and
+ * producing token j + 1. Copies the steps + 1 generated tokens to out_tokens
+ * (host int32 [steps + 1, B], step-major). The cache must hold T + steps
+ * positions; it is overwritten from position 0. Synchronises `stream` before
+ * returning. Host buffers may be pageable; pinned memory lets the copies run
+ * asynchronously. */
+NC_API nc_status nc_generate_host(nc_model* m, const int32_t* prompt, int32_t B, int32_t T,
+                                  int32_t steps, int32_t* out_tokens, nc_kv_cache* c, void* stream);
+
+/* Synchronises `stream`, reads and clears the device status word. Returns NC_OK,
+ * NC_ERR_BOUNDS or NC_ERR_DEVICE_TIMEOUT (or NC_ERR_CUDA). */
+NC_API nc_status nc_model_check(nc_model* m, void* stream);
+
+/* ------------------------------------------------------------------------
+ * Single-step entry points (the kernels of the path, one call each). Same
+ * conventions; they allocate nothing unless stated.
+ * ---------------------------------------------------------------------- */
+
+/* y[m, :] = x[m, :] / sqrt(mean_j x[m, j]^2 + eps); x dev fp32 [M, d]; y dev
+ * [M, d] in y_dtype. d % 4 == 0. */
+NC_API nc_status nc_op_rmsnorm(const float* x, void* y, nc_dtype y_dtype, int64_t M, int32_t d,
+                               float eps, void* stream);
+
+/* C = A B^T: A dev [M, K], B dev [N, K] in `dtype`, C dev fp32 [M, N]. bf16 runs
+ * the tcgen05 tensor-core GEMM (K % 64 == 0); f32 runs the CUDA-core GEMM. */
+NC_API nc_status nc_op_gemm(const void* A, const void* B, float* C, int32_t M, int32_t N,
+                            int32_t K, nc_dtype dtype, void* stream);
+
+/* Causal attention over positions 0..T-1 of B sequences.
+ * q dev [B, H, T, hd]; k, v dev [B, Hkv, t_max, hd] (positions 0..T-1 used);
+ * o dev [B, T, H*hd]. Query head h reads KV head h / (H / Hkv). Scale 1/sqrt(hd). */
+NC_API nc_status nc_op_attention_prefill(const void* q, const void* k, const void* v, void* o,
+                                         int32_t B, int32_t H, int32_t Hkv, int32_t T,
+                                         int32_t t_max, int32_t hd, nc_dtype dtype, void* stream);
+
+/* Attention of one query per sequence (decode) over cache positions 0..len-1.
+ * q dev [B, H, hd]; k, v dev [B, Hkv, t_max, hd]; o dev [B, H*hd]. Splits the
+ * positions into chunks whose partial softmax states go to `scratch` (dev,
+ * >= nc_op_attention_decode_scratch_bytes() bytes, caller-owned) and are merged
+ * by log-sum-exp. */
+NC_API size_t nc_op_attention_decode_scratch_bytes(int32_t B, int32_t H, int32_t t_max, int32_t hd);
+NC_API nc_status nc_op_attention_decode(const void* q, const void* k, const void* v, void* o,
+                                        int32_t B, int32_t H, int32_t Hkv, int32_t len,
+                                        int32_t t_max, int32_t hd, nc_dtype dtype, void* scratch,
+                                        size_t scratch_bytes, void* stream);
+
+/* out[r] = index of the largest x[r, :] (lowest index on ties); x dev fp32
+ * [rows, n], out dev int32 [rows]. */
+NC_API nc_status nc_op_argmax(const float* x, int32_t rows, int32_t n, int32_t* out, void* stream);
+
+#ifdef __cplusplus
+}
+#endif
+#endif /* NC_H_ */

@@ -1,0 +1,611 @@
+// C ABI of the library: argument checks, model / cache objects, workspace and
+// the launch sequence of prefill and decode.
+#include <math.h>
+#include <stdarg.h>
+#include <stdio.h>
+#include <string.h>
+
+#include <algorithm>
+#include <vector>
+
+#include "common.cuh"
+#include "nc_internal.h"
+#include "tc.h"
+
+namespace {
+
+thread_local char g_err[512] = "";
+
+void set_err(const char* fmt, ...) {
+  va_list ap;
+  va_start(ap, fmt);
+  vsnprintf(g_err, sizeof(g_err), fmt, ap);
+  va_end(ap);
+}
+
+#define NC_CUDA(call)                                                              \
+  do {                                                                             \
+    cudaError_t e_ = (call);                                                       \
+    if (e_ != cudaSuccess) {                                                       \
+      set_err("%s failed: %s (%s:%d)", #call, cudaGetErrorString(e_), __FILE__, __LINE__); \
+      return NC_ERR_CUDA;                                                          \
+    }                                                                              \
+  } while (0)
+
+#define NC_CHECK(cond, code, ...) \
+  do {                            \
+    if (!(cond)) {                \
+      set_err(__VA_ARGS__);       \
+      return code;                \
+    }                             \
+  } while (0)
+
+bool aligned16(const void* p) { return (reinterpret_cast<uintptr_t>(p) & 15u) == 0; }
+size_t dtype_size(nc_dtype d) { return d == NC_BF16 ? 2 : 4; }
+size_t round_up(size_t x, size_t a) { return (x + a - 1) / a * a; }
+
+nc_status check_launch() {
+  cudaError_t e = cudaGetLastError();
+  if (e != cudaSuccess) {
+    set_err("kernel launch failed: %s", cudaGetErrorString(e));
+    return NC_ERR_CUDA;
+  }
+  return NC_OK;
+}
+
+}  // namespace
+
+struct nc_model {
+  nc_config cfg;
+  int device;
+  const void* wte;
+  const void* lm_head;
+  std::vector<const void*> wq, wk, wv, wo, w_fc, w_proj;
+  float* cos_tab = nullptr;  // [max_seq, hd/2]
+  float* sin_tab = nullptr;
+  uint32_t* status = nullptr;
+  // workspace
+  void* ws = nullptr;
+  size_t ws_bytes = 0;
+  float* x = nullptr;        // [Mmax, d] fp32 residual stream
+  void* xn = nullptr;        // [Mmax, d] normalised activations
+  void* q = nullptr;         // [Mmax, H*hd]
+  void* att = nullptr;       // [Mmax, H*hd]
+  void* h = nullptr;         // [Mmax, F]
+  float* part = nullptr;     // split-K / fp32 projection outputs
+  size_t part_elems = 0;
+  float* xl = nullptr;       // [max_batch, d] last-position residual rows
+  void* xnl = nullptr;       // [max_batch, d]
+  float* logits_tmp = nullptr;  // [max_batch, V]
+  int32_t* tok_dev = nullptr;   // [Mmax]
+  int32_t* gen_dev = nullptr;   // [max_seq + 1, max_batch] generated tokens
+  float* attn_scratch = nullptr;
+  size_t attn_scratch_bytes = 0;
+  nc::TcModel* tc = nullptr;    // tensor-core state (bf16 models)
+};
+
+struct nc_kv_cache {
+  const nc_model* model;
+  void* k = nullptr;
+  void* v = nullptr;
+  void* mem = nullptr;
+  bool owns = false;
+  int32_t batch = 0, t_max = 0, len = 0;
+  size_t layer_elems = 0;  // batch * Hkv * t_max * hd
+};
+
+extern "C" {
+
+const char* nc_version(void) { return "nc-b300 0.1 (sm_103a)"; }
+
+const char* nc_status_string(nc_status s) {
+  switch (s) {
+    case NC_OK: return "ok";
+    case NC_ERR_INVALID_ARG: return "invalid argument";
+    case NC_ERR_UNSUPPORTED: return "unsupported shape";
+    case NC_ERR_OOM: return "out of device memory";
+    case NC_ERR_CUDA: return "CUDA error";
+    case NC_ERR_DEVICE_TIMEOUT: return "device wait timed out";
+    case NC_ERR_BOUNDS: return "token id out of range";
+  }
+  return "unknown status";
+}
+
+const char* nc_last_error(void) { return g_err; }
+
+int64_t nc_param_count(const nc_config* c) {
+  if (!c) return -1;
+  const int64_t d = c->d_model, qd = (int64_t)c->n_head * c->head_dim,
+                kvd = (int64_t)c->n_kv_head * c->head_dim, F = c->d_mlp;
+  const int64_t per_layer = qd * d + 2 * kvd * d + d * qd + F * d + d * F;
+  return 2 * (int64_t)c->vocab * d + (int64_t)c->n_layer * per_layer;
+}
+
+static nc_status validate_config(const nc_config* c) {
+  NC_CHECK(c, NC_ERR_INVALID_ARG, "config is NULL");
+  NC_CHECK(c->vocab > 0 && c->d_model > 0 && c->n_layer > 0 && c->n_head > 0 &&
+               c->n_kv_head > 0 && c->head_dim > 0 && c->d_mlp > 0 && c->max_seq > 0 &&
+               c->max_batch > 0,
+           NC_ERR_INVALID_ARG, "config sizes must be positive");
+  NC_CHECK(c->n_head % c->n_kv_head == 0, NC_ERR_INVALID_ARG,
+           "n_head (%d) must be a multiple of n_kv_head (%d)", c->n_head, c->n_kv_head);
+  NC_CHECK(c->head_dim % 2 == 0 && c->head_dim <= 128, NC_ERR_UNSUPPORTED,
+           "head_dim must be even and <= 128");
+  NC_CHECK(c->d_model % 4 == 0 && c->d_mlp % 4 == 0, NC_ERR_UNSUPPORTED,
+           "d_model and d_mlp must be multiples of 4");
+  NC_CHECK(c->rms_eps >= 0.f && c->rope_base > 0.f, NC_ERR_INVALID_ARG, "bad eps / rope base");
+  NC_CHECK(c->dtype == NC_F32 || c->dtype == NC_BF16, NC_ERR_INVALID_ARG, "bad dtype");
+  if (c->dtype == NC_BF16) {
+    NC_CHECK(c->head_dim == 128 && c->d_model % 64 == 0 && c->d_mlp % 64 == 0, NC_ERR_UNSUPPORTED,
+             "bf16 path needs head_dim 128 and d_model, d_mlp multiples of 64");
+  }
+  return NC_OK;
+}
+
+void nc_model_destroy(nc_model* m) {
+  if (!m) return;
+  int prev = 0;
+  cudaGetDevice(&prev);
+  cudaSetDevice(m->device);
+  if (m->tc) nc::tc_destroy(m->tc);
+  cudaFree(m->ws);
+  cudaFree(m->cos_tab);
+  cudaFree(m->sin_tab);
+  cudaFree(m->status);
+  cudaSetDevice(prev);
+  delete m;
+}
+
+nc_status nc_model_create(const nc_config* cfg, const nc_weights* w, nc_model** out) {
+  NC_CHECK(out, NC_ERR_INVALID_ARG, "out is NULL");
+  *out = nullptr;
+  nc_status st = validate_config(cfg);
+  if (st != NC_OK) return st;
+  NC_CHECK(w && w->wte && w->lm_head && w->wq && w->wk && w->wv && w->wo && w->w_fc && w->w_proj,
+           NC_ERR_INVALID_ARG, "weights struct has NULL members");
+  const int L = cfg->n_layer;
+  NC_CHECK(aligned16(w->wte) && aligned16(w->lm_head), NC_ERR_INVALID_ARG,
+           "wte / lm_head must be 16-byte aligned");
+  for (int l = 0; l < L; ++l) {
+    const void* ps[6] = {w->wq[l], w->wk[l], w->wv[l], w->wo[l], w->w_fc[l], w->w_proj[l]};
+    for (const void* p : ps)
+      NC_CHECK(p && aligned16(p), NC_ERR_INVALID_ARG, "layer %d weight NULL or misaligned", l);
+  }
+  nc_model* m = new nc_model();
+  m->cfg = *cfg;
+  cudaGetDevice(&m->device);
+  m->wte = w->wte;
+  m->lm_head = w->lm_head;
+  m->wq.assign(w->wq, w->wq + L);
+  m->wk.assign(w->wk, w->wk + L);
+  m->wv.assign(w->wv, w->wv + L);
+  m->wo.assign(w->wo, w->wo + L);
+  m->w_fc.assign(w->w_fc, w->w_fc + L);
+  m->w_proj.assign(w->w_proj, w->w_proj + L);
+
+  auto fail = [&](nc_status s) {
+    nc_model_destroy(m);
+    return s;
+  };
+  // cos/sin tables: fp64 on the host, stored fp32 ("precomputed and kept in GPU memory")
+  const int half = cfg->head_dim / 2, S = cfg->max_seq;
+  std::vector<float> c(size_t(S) * half), s(size_t(S) * half);
+  for (int t = 0; t < S; ++t)
+    for (int i = 0; i < half; ++i) {
+      const double theta = (double)t * pow((double)cfg->rope_base, -2.0 * i / cfg->head_dim);
+      c[size_t(t) * half + i] = (float)cos(theta);
+      s[size_t(t) * half + i] = (float)sin(theta);
+    }
+  if (cudaMalloc(&m->cos_tab, c.size() * 4) != cudaSuccess ||
+      cudaMalloc(&m->sin_tab, s.size() * 4) != cudaSuccess ||
+      cudaMalloc(&m->status, 256) != cudaSuccess) {
+    set_err("allocation of tables failed");
+    return fail(NC_ERR_OOM);
+  }
+  if (cudaMemcpy(m->cos_tab, c.data(), c.size() * 4, cudaMemcpyHostToDevice) != cudaSuccess ||
+      cudaMemcpy(m->sin_tab, s.data(), s.size() * 4, cudaMemcpyHostToDevice) != cudaSuccess ||
+      cudaMemset(m->status, 0, 256) != cudaSuccess) {
+    set_err("upload of tables failed");
+    return fail(NC_ERR_CUDA);
+  }
+
+  // workspace
+  const size_t es = dtype_size(cfg->dtype);
+  const size_t Mmax = (size_t)cfg->max_batch * cfg->max_seq;
+  const size_t d = cfg->d_model, qd = (size_t)cfg->n_head * cfg->head_dim, F = cfg->d_mlp;
+  const size_t nqkv = (size_t)(cfg->n_head + 2 * cfg->n_kv_head) * cfg->head_dim;
+  const size_t widest = std::max(std::max(nqkv, F), d);
+  // fp32 path keeps every projection output in `part`; the bf16 path uses it
+  // for split-K partials of the batch rows only.
+  size_t part_elems = cfg->dtype == NC_F32 ? Mmax * widest
+                                           : (size_t)nc::kMaxSplits * nc::kSwapMaxRows * widest;
+  m->part_elems = part_elems;
+  m->attn_scratch_bytes =
+      nc_op_attention_decode_scratch_bytes(cfg->max_batch, cfg->n_head, cfg->max_seq,
+                                           cfg->head_dim);
+  size_t off = 0;
+  auto carve = [&](size_t bytes) {
+    size_t o = off;
+    off = round_up(off + bytes, 1024);
+    return o;
+  };
+  const size_t o_x = carve(Mmax * d * 4), o_xn = carve(Mmax * d * es),
+               o_q = carve(Mmax * qd * es), o_att = carve(Mmax * qd * es),
+               o_h = carve(Mmax * F * es), o_part = carve(part_elems * 4),
+               o_xl = carve((size_t)cfg->max_batch * d * 4),
+               o_xnl = carve((size_t)cfg->max_batch * d * es),
+               o_lt = carve((size_t)cfg->max_batch * cfg->vocab * 4), o_tok = carve(Mmax * 4),
+               o_gen = carve(((size_t)cfg->max_seq + 1) * cfg->max_batch * 4),
+               o_as = carve(m->attn_scratch_bytes);
+  m->ws_bytes = off;
+  if (cudaMalloc(&m->ws, m->ws_bytes) != cudaSuccess) {
+    cudaGetLastError();
+    set_err("workspace allocation of %zu bytes failed", m->ws_bytes);
+    return fail(NC_ERR_OOM);
+  }
+  char* base = static_cast<char*>(m->ws);
+  m->x = reinterpret_cast<float*>(base + o_x);
+  m->xn = base + o_xn;
+  m->q = base + o_q;
+  m->att = base + o_att;
+  m->h = base + o_h;
+  m->part = reinterpret_cast<float*>(base + o_part);
+  m->xl = reinterpret_cast<float*>(base + o_xl);
+  m->xnl = base + o_xnl;
+  m->logits_tmp = reinterpret_cast<float*>(base + o_lt);
+  m->tok_dev = reinterpret_cast<int32_t*>(base + o_tok);
+  m->gen_dev = reinterpret_cast<int32_t*>(base + o_gen);
+  m->attn_scratch = reinterpret_cast<float*>(base + o_as);
+
+  if (cfg->dtype == NC_BF16) {
+    st = nc::tc_create(m->cfg, m->wte, m->lm_head, m->wq.data(), m->wk.data(), m->wv.data(),
+                       m->wo.data(), m->w_fc.data(), m->w_proj.data(), m->xn, m->att, m->h,
+                       m->xnl, Mmax, m->status, &m->tc);
+    if (st != NC_OK) return fail(st);
+  }
+  *out = m;
+  return NC_OK;
+}
+
+size_t nc_kv_cache_bytes(const nc_config* cfg, int32_t batch, int32_t t_max) {
+  if (!cfg || batch <= 0 || t_max <= 0) return 0;
+  const size_t per = (size_t)cfg->n_layer * batch * cfg->n_kv_head * t_max * cfg->head_dim *
+                     dtype_size(cfg->dtype);
+  return 256 + 2 * round_up(per, 256);
+}
+
+nc_status nc_kv_cache_alloc(const nc_model* m, int32_t batch, int32_t t_max, void* mem,
+                            nc_kv_cache** out) {
+  NC_CHECK(m && out, NC_ERR_INVALID_ARG, "NULL model or out");
+  *out = nullptr;
+  NC_CHECK(batch > 0 && t_max > 0, NC_ERR_INVALID_ARG, "batch and t_max must be positive");
+  NC_CHECK(t_max <= m->cfg.max_seq, NC_ERR_INVALID_ARG, "t_max %d exceeds max_seq %d", t_max,
+           m->cfg.max_seq);
+  NC_CHECK(!mem || (reinterpret_cast<uintptr_t>(mem) & 255u) == 0, NC_ERR_INVALID_ARG,
+           "cache memory must be 256-byte aligned");
+  const size_t bytes = nc_kv_cache_bytes(&m->cfg, batch, t_max);
+  nc_kv_cache* c = new nc_kv_cache();
+  c->model = m;
+  c->batch = batch;
+  c->t_max = t_max;
+  c->layer_elems = (size_t)batch * m->cfg.n_kv_head * t_max * m->cfg.head_dim;
+  if (!mem) {
+    if (cudaMalloc(&c->mem, bytes) != cudaSuccess) {
+      cudaGetLastError();
+      delete c;
+      set_err("KV cache allocation of %zu bytes failed", bytes);
+      return NC_ERR_OOM;
+    }
+    c->owns = true;
+  } else {
+    c->mem = mem;
+  }
+  const size_t per = round_up((size_t)m->cfg.n_layer * c->layer_elems * dtype_size(m->cfg.dtype),
+                              256);
+  c->k = static_cast<char*>(c->mem) + 256;
+  c->v = static_cast<char*>(c->mem) + 256 + per;
+  *out = c;
+  return NC_OK;
+}
+
+nc_status nc_kv_cache_view(const nc_kv_cache* c, void** k, void** v, int32_t* len, int32_t* batch,
+                           int32_t* t_max) {
+  NC_CHECK(c, NC_ERR_INVALID_ARG, "cache is NULL");
+  if (k) *k = c->k;
+  if (v) *v = c->v;
+  if (len) *len = c->len;
+  if (batch) *batch = c->batch;
+  if (t_max) *t_max = c->t_max;
+  return NC_OK;
+}
+
+void nc_kv_cache_free(nc_kv_cache* c) {
+  if (!c) return;
+  if (c->owns) cudaFree(c->mem);
+  delete c;
+}
+
+}  // extern "C"
+
+// --------------------------------------------------------------- launch plan
+namespace {
+
+using nc::RowMap;
+using nc::QkvDst;
+
+void* layer_ptr(void* base, size_t layer_elems, int l, nc_dtype dt) {
+  return static_cast<char*>(base) + (size_t)l * layer_elems * dtype_size(dt);
+}
+
+// Runs the transformer blocks over rows [M] (B sequences of `rows_per_seq`
+// rows each, starting at position pos0). On entry m->x holds the embeddings and
+// m->xn their RMSNorm; on exit m->x holds the final residual and m->xn its final
+// RMSNorm.
+nc_status run_blocks(nc_model* m, nc_kv_cache* c, int B, int rows_per_seq, int pos0,
+                     cudaStream_t s) {
+  const nc_config& cfg = m->cfg;
+  const nc_dtype dt = cfg.dtype;
+  const int64_t M = (int64_t)B * rows_per_seq;
+  const int H = cfg.n_head, Hkv = cfg.n_kv_head, hd = cfg.head_dim, d = cfg.d_model,
+            F = cfg.d_mlp;
+  const int nqkv = (H + 2 * Hkv) * hd;
+  const bool decode = rows_per_seq == 1 && pos0 > 0;
+  const bool tc = dt == NC_BF16;
+  RowMap rm{rows_per_seq, pos0};
+  for (int l = 0; l < cfg.n_layer; ++l) {
+    QkvDst dst{m->q, layer_ptr(c->k, c->layer_elems, l, dt), layer_ptr(c->v, c->layer_elems, l, dt),
+               H, Hkv, hd, c->t_max, m->cos_tab, m->sin_tab, cfg.rms_eps};
+    // Q/K/V projections + RoPE + QK norm + cache write
+    if (tc) {
+      nc_status st = nc::tc_qkv(m->tc, l, M, rm, dst, m->part, s);
+      if (st != NC_OK) return st;
+    } else {
+      const size_t kvd = (size_t)Hkv * hd;
+      nc::launch_gemm_simt(m->xn, m->wq[l], m->part, M, H * hd, d, nqkv, dt, s);
+      nc::launch_gemm_simt(m->xn, m->wk[l], m->part + (size_t)H * hd, M, Hkv * hd, d, nqkv, dt, s);
+      nc::launch_gemm_simt(m->xn, m->wv[l], m->part + (size_t)H * hd + kvd, M, Hkv * hd, d, nqkv,
+                           dt, s);
+      nc::launch_qkv_post(m->part, 1, M, rm, dst, dt, s);
+    }
+    // causal attention
+    if (decode) {
+      const int len = pos0 + 1;
+      const int ns = nc::decode_attention_splits(len);
+      nc::launch_attention_decode_simt(m->q, dst.k_cache, dst.v_cache, m->att, B, H, Hkv, len,
+                                       c->t_max, hd, dt, m->attn_scratch, ns, s);
+    } else if (tc) {
+      nc_status st = nc::tc_attention_prefill(m->tc, m->q, dst.k_cache, dst.v_cache, m->att, B, H,
+                                              Hkv, rows_per_seq, c->t_max, s);
+      if (st != NC_OK) return st;
+    } else {
+      nc::launch_attention_prefill_simt(m->q, dst.k_cache, dst.v_cache, m->att, B, H, Hkv,
+                                        rows_per_seq, c->t_max, hd, dt, s);
+    }
+    // output projection + residual, then the pre-MLP RMSNorm
+    if (tc) {
+      nc_status st = nc::tc_out_proj(m->tc, l, M, m->x, m->part, s);
+      if (st != NC_OK) return st;
+      nc::launch_rmsnorm(m->x, m->xn, dt, M, d, cfg.rms_eps, s);
+      st = nc::tc_mlp(m->tc, l, M, m->x, m->part, s);
+      if (st != NC_OK) return st;
+      nc::launch_rmsnorm(m->x, m->xn, dt, M, d, cfg.rms_eps, s);
+    } else {
+      nc::launch_gemm_simt(m->att, m->wo[l], m->part, M, d, H * hd, d, dt, s);
+      nc::launch_residual_finish(m->part, 1, m->x, M, d, m->xn, dt, cfg.rms_eps, s);
+      nc::launch_gemm_simt(m->xn, m->w_fc[l], m->part, M, F, d, F, dt, s);
+      nc::launch_relu2_finish(m->part, 1, m->h, M, F, dt, s);
+      nc::launch_gemm_simt(m->h, m->w_proj[l], m->part, M, d, F, d, dt, s);
+      nc::launch_residual_finish(m->part, 1, m->x, M, d, m->xn, dt, cfg.rms_eps, s);
+    }
+  }
+  return check_launch();
+}
+
+// logits[M, V] = xn[M, d] lm_head^T
+nc_status run_lm_head(nc_model* m, const void* xn, int64_t M, float* logits, cudaStream_t s) {
+  if (m->cfg.dtype == NC_BF16) return nc::tc_lm_head(m->tc, xn, M, logits, m->part, s);
+  nc::launch_gemm_simt(xn, m->lm_head, logits, M, m->cfg.vocab, m->cfg.d_model, m->cfg.vocab,
+                       m->cfg.dtype, s);
+  return check_launch();
+}
+
+nc_status check_prefill_args(nc_model* m, const int32_t* tokens, int32_t B, int32_t T,
+                             nc_kv_cache* c) {
+  NC_CHECK(m && c && tokens, NC_ERR_INVALID_ARG, "NULL model, cache or tokens");
+  NC_CHECK(c->model == m, NC_ERR_INVALID_ARG, "cache belongs to another model");
+  NC_CHECK(B >= 1 && B <= c->batch && B <= m->cfg.max_batch, NC_ERR_INVALID_ARG,
+           "B=%d out of range (cache batch %d, max_batch %d)", B, c->batch, m->cfg.max_batch);
+  NC_CHECK(T >= 1 && T <= c->t_max && T <= m->cfg.max_seq, NC_ERR_INVALID_ARG,
+           "T=%d out of range (cache t_max %d)", T, c->t_max);
+  NC_CHECK(aligned16(tokens) || (reinterpret_cast<uintptr_t>(tokens) & 3u) == 0,
+           NC_ERR_INVALID_ARG, "tokens must be 4-byte aligned");
+  return NC_OK;
+}
+
+nc_status prefill_common(nc_model* m, const int32_t* tokens, int32_t B, int32_t T,
+                         nc_kv_cache* c, cudaStream_t s) {
+  const int64_t M = (int64_t)B * T;
+  nc::launch_embed_norm(tokens, m->wte, m->cfg.dtype, m->x, m->xn, M, m->cfg.d_model,
+                        m->cfg.vocab, m->cfg.rms_eps, m->status, s);
+  nc_status st = run_blocks(m, c, B, T, 0, s);
+  if (st != NC_OK) return st;
+  c->len = T;
+  return NC_OK;
+}
+
+}  // namespace
+
+extern "C" {
+
+nc_status nc_prefill(nc_model* m, const int32_t* tokens, int32_t B, int32_t T, float* logits,
+                     nc_kv_cache* c, void* stream) {
+  nc_status st = check_prefill_args(m, tokens, B, T, c);
+  if (st != NC_OK) return st;
+  NC_CHECK(logits && aligned16(logits), NC_ERR_INVALID_ARG, "logits NULL or misaligned");
+  cudaStream_t s = static_cast<cudaStream_t>(stream);
+  st = prefill_common(m, tokens, B, T, c, s);
+  if (st != NC_OK) return st;
+  return run_lm_head(m, m->xn, (int64_t)B * T, logits, s);
+}
+
+nc_status nc_prefill_last(nc_model* m, const int32_t* tokens, int32_t B, int32_t T,
+                          float* logits_last, int32_t* argmax_out, nc_kv_cache* c, void* stream) {
+  nc_status st = check_prefill_args(m, tokens, B, T, c);
+  if (st != NC_OK) return st;
+  NC_CHECK(!logits_last || aligned16(logits_last), NC_ERR_INVALID_ARG, "logits misaligned");
+  cudaStream_t s = static_cast<cudaStream_t>(stream);
+  st = prefill_common(m, tokens, B, T, c, s);
+  if (st != NC_OK) return st;
+  nc::launch_gather_rows(m->x, m->xl, B, T, m->cfg.d_model, s);
+  nc::launch_rmsnorm(m->xl, m->xnl, m->cfg.dtype, B, m->cfg.d_model, m->cfg.rms_eps, s);
+  float* lg = logits_last ? logits_last : m->logits_tmp;
+  st = run_lm_head(m, m->xnl, B, lg, s);
+  if (st != NC_OK) return st;
+  if (argmax_out) nc::launch_argmax(lg, B, m->cfg.vocab, argmax_out, s);
+  return check_launch();
+}
+
+nc_status nc_decode_step(nc_model* m, const int32_t* tokens, int32_t B, int32_t pos,
+                         float* logits, int32_t* argmax_out, nc_kv_cache* c, void* stream) {
+  NC_CHECK(m && c && tokens, NC_ERR_INVALID_ARG, "NULL model, cache or tokens");
+  NC_CHECK(c->model == m, NC_ERR_INVALID_ARG, "cache belongs to another model");
+  NC_CHECK(logits || argmax_out, NC_ERR_INVALID_ARG, "need logits or argmax_out");
+  NC_CHECK(!logits || aligned16(logits), NC_ERR_INVALID_ARG, "logits misaligned");
+  NC_CHECK(B >= 1 && B <= c->batch && B <= m->cfg.max_batch, NC_ERR_INVALID_ARG,
+           "B=%d out of range", B);
+  NC_CHECK(pos == c->len, NC_ERR_INVALID_ARG, "pos %d must equal the cache length %d", pos,
+           c->len);
+  NC_CHECK(pos >= 1, NC_ERR_INVALID_ARG, "decode needs a prefilled cache (pos >= 1)");
+  NC_CHECK(pos + 1 <= c->t_max, NC_ERR_INVALID_ARG, "cache full (t_max %d)", c->t_max);
+  cudaStream_t s = static_cast<cudaStream_t>(stream);
+  nc::launch_embed_norm(tokens, m->wte, m->cfg.dtype, m->x, m->xn, B, m->cfg.d_model,
+                        m->cfg.vocab, m->cfg.rms_eps, m->status, s);
+  nc_status st = run_blocks(m, c, B, 1, pos, s);
+  if (st != NC_OK) return st;
+  float* lg = logits ? logits : m->logits_tmp;
+  st = run_lm_head(m, m->xn, B, lg, s);
+  if (st != NC_OK) return st;
+  if (argmax_out) nc::launch_argmax(lg, B, m->cfg.vocab, argmax_out, s);
+  st = check_launch();
+  if (st == NC_OK) c->len = pos + 1;
+  return st;
+}
+
+nc_status nc_generate_host(nc_model* m, const int32_t* prompt, int32_t B, int32_t T,
+                           int32_t steps, int32_t* out_tokens, nc_kv_cache* c, void* stream) {
+  NC_CHECK(m && c && prompt && out_tokens, NC_ERR_INVALID_ARG, "NULL argument");
+  NC_CHECK(steps >= 0 && T + steps <= c->t_max && steps + 1 <= m->cfg.max_seq,
+           NC_ERR_INVALID_ARG, "T + steps exceeds the cache (t_max %d)", c->t_max);
+  nc_status st = check_prefill_args(m, m->tok_dev, B, T, c);
+  if (st != NC_OK) return st;
+  cudaStream_t s = static_cast<cudaStream_t>(stream);
+  NC_CUDA(cudaMemcpyAsync(m->tok_dev, prompt, sizeof(int32_t) * B * T, cudaMemcpyHostToDevice, s));
+  c->len = 0;
+  st = nc_prefill_last(m, m->tok_dev, B, T, nullptr, m->gen_dev, c, stream);
+  if (st != NC_OK) return st;
+  for (int j = 0; j < steps; ++j) {
+    st = nc_decode_step(m, m->gen_dev + (size_t)j * B, B, T + j, nullptr,
+                        m->gen_dev + (size_t)(j + 1) * B, c, stream);
+    if (st != NC_OK) return st;
+  }
+  NC_CUDA(cudaMemcpyAsync(out_tokens, m->gen_dev, sizeof(int32_t) * B * (steps + 1),
+                          cudaMemcpyDeviceToHost, s));
+  NC_CUDA(cudaStreamSynchronize(s));
+  return NC_OK;
+}
+
+nc_status nc_model_check(nc_model* m, void* stream) {
+  NC_CHECK(m, NC_ERR_INVALID_ARG, "model is NULL");
+  cudaStream_t s = static_cast<cudaStream_t>(stream);
+  uint32_t word = 0;
+  NC_CUDA(cudaStreamSynchronize(s));
+  NC_CUDA(cudaMemcpy(&word, m->status, 4, cudaMemcpyDeviceToHost));
+  NC_CUDA(cudaMemset(m->status, 0, 4));
+  if (word & nc::ST_TIMEOUT) {
+    set_err("a kernel's bounded wait timed out (status 0x%x)", word);
+    return NC_ERR_DEVICE_TIMEOUT;
+  }
+  if (word & nc::ST_BAD_TOKEN) {
+    set_err("a token id was outside [0, vocab); row 0 was used");
+    return NC_ERR_BOUNDS;
+  }
+  return NC_OK;
+}
+
+// ------------------------------------------------------------ single steps
+nc_status nc_op_rmsnorm(const float* x, void* y, nc_dtype y_dtype, int64_t M, int32_t d,
+                        float eps, void* stream) {
+  NC_CHECK(x && y && aligned16(x) && aligned16(y), NC_ERR_INVALID_ARG, "NULL/misaligned");
+  NC_CHECK(M >= 0 && d > 0 && d % 4 == 0, NC_ERR_INVALID_ARG, "d must be a positive multiple of 4");
+  NC_CHECK(y_dtype == NC_F32 || y_dtype == NC_BF16, NC_ERR_INVALID_ARG, "bad dtype");
+  if (M == 0) return NC_OK;
+  nc::launch_rmsnorm(x, y, y_dtype, M, d, eps, static_cast<cudaStream_t>(stream));
+  return check_launch();
+}
+
+nc_status nc_op_gemm(const void* A, const void* B, float* C, int32_t M, int32_t N, int32_t K,
+                     nc_dtype dtype, void* stream) {
+  NC_CHECK(A && B && C && aligned16(A) && aligned16(B) && aligned16(C), NC_ERR_INVALID_ARG,
+           "NULL/misaligned");
+  NC_CHECK(M >= 0 && N > 0 && K > 0, NC_ERR_INVALID_ARG, "bad sizes");
+  if (M == 0) return NC_OK;
+  cudaStream_t s = static_cast<cudaStream_t>(stream);
+  if (dtype == NC_BF16) {
+    NC_CHECK(K % 64 == 0 && N % 16 == 0, NC_ERR_UNSUPPORTED, "bf16 GEMM needs K%%64==0, N%%16==0");
+    return nc::tc_gemm_f32out(A, B, C, M, N, K, s);
+  }
+  NC_CHECK(dtype == NC_F32, NC_ERR_INVALID_ARG, "bad dtype");
+  nc::launch_gemm_simt(A, B, C, M, N, K, N, dtype, s);
+  return check_launch();
+}
+
+nc_status nc_op_attention_prefill(const void* q, const void* k, const void* v, void* o, int32_t B,
+                                  int32_t H, int32_t Hkv, int32_t T, int32_t t_max, int32_t hd,
+                                  nc_dtype dtype, void* stream) {
+  NC_CHECK(q && k && v && o && aligned16(q) && aligned16(k) && aligned16(v) && aligned16(o),
+           NC_ERR_INVALID_ARG, "NULL/misaligned");
+  NC_CHECK(B > 0 && H > 0 && Hkv > 0 && H % Hkv == 0 && T > 0 && T <= t_max && hd > 0 &&
+               hd % 2 == 0 && hd <= 128,
+           NC_ERR_INVALID_ARG, "bad sizes");
+  cudaStream_t s = static_cast<cudaStream_t>(stream);
+  if (dtype == NC_BF16) {
+    NC_CHECK(hd == 128, NC_ERR_UNSUPPORTED, "bf16 attention needs head_dim 128");
+    return nc::tc_attention_prefill(nullptr, q, k, v, o, B, H, Hkv, T, t_max, s);
+  }
+  nc::launch_attention_prefill_simt(q, k, v, o, B, H, Hkv, T, t_max, hd, dtype, s);
+  return check_launch();
+}
+
+size_t nc_op_attention_decode_scratch_bytes(int32_t B, int32_t H, int32_t t_max, int32_t hd) {
+  if (B <= 0 || H <= 0 || t_max <= 0 || hd <= 0) return 0;
+  const int ns = nc::decode_attention_splits(t_max);
+  return (size_t)B * H * ns * (hd + 2) * sizeof(float);
+}
+
+nc_status nc_op_attention_decode(const void* q, const void* k, const void* v, void* o, int32_t B,
+                                 int32_t H, int32_t Hkv, int32_t len, int32_t t_max, int32_t hd,
+                                 nc_dtype dtype, void* scratch, size_t scratch_bytes,
+                                 void* stream) {
+  NC_CHECK(q && k && v && o && scratch, NC_ERR_INVALID_ARG, "NULL pointer");
+  NC_CHECK(B > 0 && H > 0 && Hkv > 0 && H % Hkv == 0 && len > 0 && len <= t_max && hd > 0 &&
+               hd % 2 == 0 && hd <= 128,
+           NC_ERR_INVALID_ARG, "bad sizes");
+  NC_CHECK(dtype == NC_F32 || dtype == NC_BF16, NC_ERR_INVALID_ARG, "bad dtype");
+  const int ns = nc::decode_attention_splits(len);
+  NC_CHECK(scratch_bytes >= (size_t)B * H * ns * (hd + 2) * sizeof(float), NC_ERR_INVALID_ARG,
+           "scratch too small");
+  nc::launch_attention_decode_simt(q, k, v, o, B, H, Hkv, len, t_max, hd, dtype,
+                                   static_cast<float*>(scratch), ns,
+                                   static_cast<cudaStream_t>(stream));
+  return check_launch();
+}
+
+nc_status nc_op_argmax(const float* x, int32_t rows, int32_t n, int32_t* out, void* stream) {
+  NC_CHECK(x && out, NC_ERR_INVALID_ARG, "NULL pointer");
+  NC_CHECK(rows >= 0 && n > 0, NC_ERR_INVALID_ARG, "bad sizes");
+  if (rows == 0) return NC_OK;
+  nc::launch_argmax(x, rows, n, out, static_cast<cudaStream_t>(stream));
+  return check_launch();
+}
+
+}  // extern "C"

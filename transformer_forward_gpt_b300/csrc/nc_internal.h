@@ -1,0 +1,57 @@
+// Internal launch interface shared by the .cu files of the library (host side).
+#pragma once
+#include <cuda.h>
+#include <cuda_runtime.h>
+#include <stdint.h>
+
+#include "../../include/nc.h"
+
+namespace nc {
+
+// Where the rows of a projection output go (prefill: rows = B*T tokens of B
+// sequences starting at position pos0 = 0; decode: rows = B, one per sequence, at
+// position pos0 = pos).
+struct RowMap {
+  int32_t rows_per_seq;   // T (prefill) or 1 (decode)
+  int32_t pos0;           // absolute position of row 0 of each sequence
+};
+
+// Destinations of the Q/K/V projection epilogue (RoPE + QK norm + scatter).
+struct QkvDst {
+  void* q;                // [B, H, rows_per_seq, hd]
+  void* k_cache;          // [B_cache, Hkv, t_max, hd] of this layer
+  void* v_cache;
+  int32_t H, Hkv, hd, t_max;
+  const float* cos_tab;   // [max_seq, hd/2]
+  const float* sin_tab;
+  float eps;
+};
+
+// ---- CUDA-core kernels (simt.cu)
+void launch_embed_norm(const int32_t* tok, const void* wte, nc_dtype dt, float* x, void* xn,
+                       int64_t M, int d, int vocab, float eps, uint32_t* status, cudaStream_t s);
+void launch_rmsnorm(const float* x, void* y, nc_dtype ydt, int64_t M, int d, float eps,
+                    cudaStream_t s);
+void launch_gemm_simt(const void* A, const void* B, float* C, int64_t M, int N, int K,
+                      int64_t ldc, nc_dtype dt, cudaStream_t s);
+// out-of-place reductions of split-K partials part[split][M][N] (split stride
+// = M*N) followed by one epilogue each
+void launch_qkv_post(const float* part, int n_split, int64_t M, const RowMap& rm,
+                     const QkvDst& dst, nc_dtype dt, cudaStream_t s);
+void launch_residual_finish(const float* part, int n_split, float* x, int64_t M, int N,
+                            void* xn_out, nc_dtype dt, float eps, cudaStream_t s);
+void launch_relu2_finish(const float* part, int n_split, void* h, int64_t M, int N, nc_dtype dt,
+                         cudaStream_t s);
+void launch_sum_splits(const float* part, int n_split, float* out, int64_t M, int N, int64_t ldo,
+                       cudaStream_t s);
+void launch_attention_prefill_simt(const void* q, const void* k, const void* v, void* o, int B,
+                                   int H, int Hkv, int T, int t_max, int hd, nc_dtype dt,
+                                   cudaStream_t s);
+int decode_attention_splits(int len);
+void launch_attention_decode_simt(const void* q, const void* k, const void* v, void* o, int B,
+                                  int H, int Hkv, int len, int t_max, int hd, nc_dtype dt,
+                                  float* scratch, int n_split, cudaStream_t s);
+void launch_argmax(const float* x, int rows, int n, int32_t* out, cudaStream_t s);
+void launch_gather_rows(const float* x, float* y, int B, int T, int d, cudaStream_t s);
+
+}  // namespace nc

@@ -1,0 +1,701 @@
+// tcgen05 GEMM for sm_103a: C = A B^T with bf16 operands staged by TMA into
+// shared memory (128-byte swizzle, K-major), fp32 accumulators in TMEM, and the
+// epilogue read back with tcgen05.ld.
+//
+// Persistent, warp-specialised CTA of 192 threads:
+//   warp 0      one thread issues the TMA loads of A and B into a ring of stages
+//   warp 1      allocates TMEM; one thread issues tcgen05.mma (128 x BN x 16) and
+//               commits to mbarriers that free a stage / publish an accumulator
+//   warps 2..5  epilogue: warp w reads TMEM lanes 32*(w%4)..+31, so each thread
+//               owns one output row of the 128-row tile
+// Two TMEM accumulators (2*BN columns) let the epilogue of one tile overlap the
+// main loop of the next.
+//
+// Two ways the projections of the forward pass are laid onto it:
+//   tile mode (many token rows): A = activations [M, K], B = weights [N, K]; the
+//     epilogue is fused: RoPE + QK norm + scatter (Q/K/V), residual add (O, PROJ),
+//     ReLU^2 (FC) or an fp32 store (LM head).
+//   swap mode (<= 128 token rows, decode): A = weights, B = activations, so the
+//     weights fill the 128-row MMA; K may be split across CTAs. The epilogue
+//     writes transposed fp32 partial sums [split][token][feature] that a
+//     finishing kernel reduces (or, unsplit, the logits directly).
+#include <limits.h>
+
+#include <algorithm>
+#include <vector>
+
+#include "common.cuh"
+#include "tc.h"
+
+namespace nc {
+
+enum Epi : int { EPI_F32 = 0, EPI_RESID = 1, EPI_RELU2 = 2, EPI_QKV = 3, EPI_SWAP = 4 };
+
+struct GemmArgs {
+  int M;                  // rows of the A operand
+  int N;                  // rows of the B operand
+  int num_m_blk, num_n_blk, num_k_blk;
+  int k_splits, k_per_split;
+  int a_split0, a_split1;  // row boundaries between A tensor maps 0 | 1 | 2
+  int b_split0, b_split1;  // the same for B (multiples of 128)
+  float* out_f32;          // EPI_F32 (C), EPI_RESID (x), EPI_SWAP (partials or logits)
+  bf16* out_bf16;          // EPI_RELU2
+  int64_t ldo;             // row pitch of the output, elements
+  int64_t split_stride;    // EPI_SWAP: elements between split slices
+  RowMap rm;               // EPI_QKV
+  QkvDst qkv;
+  uint32_t* status;
+};
+
+template <int BN>
+struct TileCfg {
+  static constexpr int kABytes = 128 * 64 * 2;
+  static constexpr int kBBytes = BN * 64 * 2;
+  static constexpr int kStageBytes = kABytes + kBBytes;
+  static constexpr int kStages = (196608 / kStageBytes) > 8 ? 8 : (196608 / kStageBytes);
+  static constexpr int kBoxRowsB = BN < 128 ? BN : 128;
+  static constexpr int kTmemCols = (2 * BN <= 32) ? 32 : (2 * BN <= 64) ? 64 : (2 * BN <= 128) ? 128
+                                   : (2 * BN <= 256) ? 256 : 512;
+  static constexpr size_t kSmemBytes = (size_t)kStages * kStageBytes + 1024 + 256;
+};
+
+__device__ __forceinline__ const CUtensorMap* pick_map(const CUtensorMap* m0, const CUtensorMap* m1,
+                                                       const CUtensorMap* m2, int row, int s0,
+                                                       int s1, int& local) {
+  if (row < s0) {
+    local = row;
+    return m0;
+  }
+  if (row < s1) {
+    local = row - s0;
+    return m1;
+  }
+  local = row - s1;
+  return m2;
+}
+
+// ----------------------------------------------------------------- epilogues
+// Each thread holds row `row` of the tile; taddr points at its TMEM lane and
+// the accumulator's first column. tcgen05.ld is warp-collective, so every lane
+// runs the loads and only the stores are predicated on the row being valid.
+template <int BN>
+__device__ __forceinline__ void epi_store_rows(const GemmArgs& p, uint32_t taddr, int row, int nb,
+                                               int mode) {
+  const bool valid = row < p.M;
+#pragma unroll 1
+  for (int c = 0; c < BN / 32; ++c) {
+    float v[32];
+    tmem_ld32_sync(taddr + c * 32, v);
+    const int n0 = nb * BN + c * 32;
+    if (!valid || n0 >= p.N) continue;
+    if (mode == EPI_F32) {
+      float* dst = p.out_f32 + (int64_t)row * p.ldo + n0;
+#pragma unroll
+      for (int i = 0; i < 8; ++i)
+        if (n0 + 4 * i < p.N)
+          st_global_cs_v4(dst + 4 * i, make_uint4(__float_as_uint(v[4 * i]), __float_as_uint(v[4 * i + 1]),
+                                                  __float_as_uint(v[4 * i + 2]), __float_as_uint(v[4 * i + 3])));
+    } else if (mode == EPI_RESID) {
+      float* dst = p.out_f32 + (int64_t)row * p.ldo + n0;
+#pragma unroll
+      for (int i = 0; i < 8; ++i)
+        if (n0 + 4 * i < p.N) {
+          float4 x = *reinterpret_cast<float4*>(dst + 4 * i);
+          x.x += v[4 * i];
+          x.y += v[4 * i + 1];
+          x.z += v[4 * i + 2];
+          x.w += v[4 * i + 3];
+          *reinterpret_cast<float4*>(dst + 4 * i) = x;
+        }
+    } else {  // EPI_RELU2
+      bf16* dst = p.out_bf16 + (int64_t)row * p.ldo + n0;
+#pragma unroll
+      for (int i = 0; i < 4; ++i)
+        if (n0 + 8 * i < p.N) {
+          float a[8];
+#pragma unroll
+          for (int j = 0; j < 8; ++j) {
+            const float r = fmaxf(v[8 * i + j], 0.f);
+            a[j] = r * r;
+          }
+          *reinterpret_cast<uint4*>(dst + 8 * i) =
+              make_uint4(pack_bf16x2(a[0], a[1]), pack_bf16x2(a[2], a[3]), pack_bf16x2(a[4], a[5]),
+                         pack_bf16x2(a[6], a[7]));
+        }
+    }
+  }
+}
+
+// Q/K/V epilogue: the tile's BN columns are BN/128 whole heads of the
+// concatenated [Q | K | V] projection. For Q and K heads: the mean square is
+// taken over the un-rotated values (the rotation keeps the norm), then pairs
+// (i, i + 64) are rotated by +theta(t, i) and scaled by the QK-norm factor.
+template <int BN>
+__device__ __forceinline__ void epi_qkv(const GemmArgs& p, uint32_t taddr, int row, int nb) {
+  const QkvDst& q = p.qkv;
+  const bool valid = row < p.M;
+  const int total_heads = q.H + 2 * q.Hkv;
+  const int b = valid ? row / p.rm.rows_per_seq : 0;
+  const int t = valid ? p.rm.pos0 + row % p.rm.rows_per_seq : 0;
+#pragma unroll 1
+  for (int hc = 0; hc < BN / 128; ++hc) {
+    const int j = nb * (BN / 128) + hc;
+    if (j >= total_heads) break;
+    const uint32_t base = taddr + hc * 128;
+    if (j >= q.H + q.Hkv) {  // V head, stored as projected
+      const int g = j - q.H - q.Hkv;
+      bf16* out = reinterpret_cast<bf16*>(q.v_cache) + (((int64_t)b * q.Hkv + g) * q.t_max + t) * 128;
+#pragma unroll 1
+      for (int c = 0; c < 4; ++c) {
+        float v[32];
+        tmem_ld32_sync(base + c * 32, v);
+        if (valid) {
+#pragma unroll
+          for (int i = 0; i < 4; ++i)
+            *reinterpret_cast<uint4*>(out + c * 32 + 8 * i) = make_uint4(
+                pack_bf16x2(v[8 * i], v[8 * i + 1]), pack_bf16x2(v[8 * i + 2], v[8 * i + 3]),
+                pack_bf16x2(v[8 * i + 4], v[8 * i + 5]), pack_bf16x2(v[8 * i + 6], v[8 * i + 7]));
+        }
+      }
+      continue;
+    }
+    float ss = 0.f;
+#pragma unroll 1
+    for (int c = 0; c < 4; ++c) {
+      float v[32];
+      tmem_ld32_sync(base + c * 32, v);
+#pragma unroll
+      for (int i = 0; i < 32; ++i) ss = fmaf(v[i], v[i], ss);
+    }
+    const float r = rsqrtf(ss * (1.f / 128.f) + q.eps);
+    bf16* out;
+    if (j < q.H)
+      out = reinterpret_cast<bf16*>(q.q) +
+            (((int64_t)b * q.H + j) * p.rm.rows_per_seq + (t - p.rm.pos0)) * 128;
+    else
+      out = reinterpret_cast<bf16*>(q.k_cache) + (((int64_t)b * q.Hkv + (j - q.H)) * q.t_max + t) * 128;
+    const float* cs = q.cos_tab + (int64_t)t * 64;
+    const float* sn = q.sin_tab + (int64_t)t * 64;
+#pragma unroll 1
+    for (int c = 0; c < 2; ++c) {
+      float lo[32], hi[32];
+      tmem_ld32_sync(base + c * 32, lo);
+      tmem_ld32_sync(base + 64 + c * 32, hi);
+      if (!valid) continue;
+#pragma unroll
+      for (int i = 0; i < 8; ++i) {
+        const float4 c4 = *reinterpret_cast<const float4*>(cs + c * 32 + 4 * i);
+        const float4 s4 = *reinterpret_cast<const float4*>(sn + c * 32 + 4 * i);
+        const float cc[4] = {c4.x, c4.y, c4.z, c4.w}, ssn[4] = {s4.x, s4.y, s4.z, s4.w};
+#pragma unroll
+        for (int u = 0; u < 4; ++u) {
+          const float a = lo[4 * i + u], h = hi[4 * i + u];
+          lo[4 * i + u] = (a * cc[u] - h * ssn[u]) * r;
+          hi[4 * i + u] = (a * ssn[u] + h * cc[u]) * r;
+        }
+      }
+#pragma unroll
+      for (int i = 0; i < 4; ++i) {
+        *reinterpret_cast<uint4*>(out + c * 32 + 8 * i) = make_uint4(
+            pack_bf16x2(lo[8 * i], lo[8 * i + 1]), pack_bf16x2(lo[8 * i + 2], lo[8 * i + 3]),
+            pack_bf16x2(lo[8 * i + 4], lo[8 * i + 5]), pack_bf16x2(lo[8 * i + 6], lo[8 * i + 7]));
+        *reinterpret_cast<uint4*>(out + 64 + c * 32 + 8 * i) = make_uint4(
+            pack_bf16x2(hi[8 * i], hi[8 * i + 1]), pack_bf16x2(hi[8 * i + 2], hi[8 * i + 3]),
+            pack_bf16x2(hi[8 * i + 4], hi[8 * i + 5]), pack_bf16x2(hi[8 * i + 6], hi[8 * i + 7]));
+      }
+    }
+  }
+}
+
+// Swap mode: the thread's row is a weight row (output feature f); TMEM columns
+// are tokens. Writes out[ks][token][f] (lanes of a warp write consecutive f).
+template <int BN>
+__device__ __forceinline__ void epi_swap(const GemmArgs& p, uint32_t taddr, int f, int nb, int ks) {
+  const bool valid = f < p.M;
+  float* base = p.out_f32 + (int64_t)ks * p.split_stride + f;
+#pragma unroll 1
+  for (int c = 0; c < BN / 16; ++c) {
+    float v[16];
+    tmem_ld16_sync(taddr + c * 16, v);
+#pragma unroll
+    for (int i = 0; i < 16; ++i) {
+      const int tok = nb * BN + c * 16 + i;
+      if (valid && tok < p.N) base[(int64_t)tok * p.ldo] = v[i];
+    }
+  }
+}
+
+// --------------------------------------------------------------------- kernel
+template <int BN, int EPI>
+__global__ void __launch_bounds__(192, 1)
+    gemm_tc_kernel(const __grid_constant__ CUtensorMap tmA0, const __grid_constant__ CUtensorMap tmA1,
+                   const __grid_constant__ CUtensorMap tmA2, const __grid_constant__ CUtensorMap tmB0,
+                   const __grid_constant__ CUtensorMap tmB1, const __grid_constant__ CUtensorMap tmB2,
+                   const GemmArgs p) {
+  using C = TileCfg<BN>;
+  constexpr int S = C::kStages;
+  extern __shared__ uint8_t smem_raw[];
+  uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) &
+                                             ~uintptr_t(1023));
+  uint64_t* full = reinterpret_cast<uint64_t*>(smem + S * C::kStageBytes);
+  uint64_t* empty = full + S;
+  uint64_t* tfull = empty + S;   // [2] accumulator ready
+  uint64_t* tempty = tfull + 2;  // [2] accumulator drained by the epilogue
+  uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(tempty + 2);
+  volatile int* abort_flag = reinterpret_cast<volatile int*>(tmem_slot + 1);
+
+  const int warp = threadIdx.x / 32, lane = threadIdx.x % 32;
+  if (threadIdx.x == 0) {
+    for (int s = 0; s < S; ++s) {
+      mbar_init(&full[s], 1);
+      mbar_init(&empty[s], 1);
+    }
+    for (int b = 0; b < 2; ++b) {
+      mbar_init(&tfull[b], 1);
+      mbar_init(&tempty[b], 4);
+    }
+    *abort_flag = 0;
+    fence_mbar_init();
+  }
+  if (warp == 0 && lane == 0) {
+    tma_prefetch_desc(&tmA0);
+    tma_prefetch_desc(&tmB0);
+  }
+  if (warp == 1) {
+    tmem_alloc(tmem_slot, C::kTmemCols);
+    tmem_relinquish();
+  }
+  tc_fence_before();
+  __syncthreads();
+  tc_fence_after();
+  const uint32_t tmem_base = *tmem_slot;
+  const int units = p.num_m_blk * p.num_n_blk * p.k_splits;
+
+  if (warp == 0) {
+    if (lane == 0) {
+      // ------------------------------------------------------------ producer
+      int stage = 0, issued = 0;
+      uint32_t phase = 0;
+      for (int u = blockIdx.x; u < units && !*abort_flag; u += gridDim.x) {
+        const int mb = u % p.num_m_blk;
+        const int rest = u / p.num_m_blk;
+        const int nb = rest % p.num_n_blk;
+        const int ks = rest / p.num_n_blk;
+        const int kb0 = ks * p.k_per_split;
+        const int kb1 = min(p.num_k_blk, kb0 + p.k_per_split);
+        for (int kb = kb0; kb < kb1; ++kb) {
+          if (!mbar_wait(&empty[stage], phase ^ 1, p.status)) {
+            *abort_flag = 1;
+            break;
+          }
+          uint8_t* sa = smem + stage * C::kStageBytes;
+          uint8_t* sb = sa + C::kABytes;
+          mbar_arrive_expect_tx(&full[stage], C::kStageBytes);
+          int local;
+          const CUtensorMap* ma = pick_map(&tmA0, &tmA1, &tmA2, mb * 128, p.a_split0, p.a_split1, local);
+          tma_load_2d(sa, ma, &full[stage], kb * 64, local);
+#pragma unroll
+          for (int h = 0; h < BN / C::kBoxRowsB; ++h) {
+            const CUtensorMap* mb_ = pick_map(&tmB0, &tmB1, &tmB2, nb * BN + h * C::kBoxRowsB,
+                                              p.b_split0, p.b_split1, local);
+            tma_load_2d(sb + h * C::kBoxRowsB * 128, mb_, &full[stage], kb * 64, local);
+          }
+          if (++stage == S) {
+            stage = 0;
+            phase ^= 1;
+          }
+          ++issued;
+        }
+      }
+      if (*abort_flag) {
+        // let the copies already issued land before the CTA's shared memory goes away
+        for (int i = 1; i <= min(issued, S); ++i) {
+          const int st = (stage - i + S) % S;
+          const uint32_t ph = (stage - i < 0) ? (phase ^ 1) : phase;
+          mbar_wait(&full[st], ph, p.status);
+        }
+      }
+    }
+  } else if (warp == 1) {
+    if (lane == 0) {
+      // ----------------------------------------------------------- MMA issuer
+      constexpr uint32_t kIdesc = idesc_bf16_f32(128, BN);
+      int stage = 0;
+      uint32_t phase = 0;
+      int acc = 0;
+      uint32_t acc_phase = 0;
+      for (int u = blockIdx.x; u < units && !*abort_flag; u += gridDim.x) {
+        const int ks = (u / p.num_m_blk) / p.num_n_blk;
+        const int kb0 = ks * p.k_per_split;
+        const int kb1 = min(p.num_k_blk, kb0 + p.k_per_split);
+        if (!mbar_wait(&tempty[acc], acc_phase ^ 1, p.status)) {
+          *abort_flag = 1;
+          break;
+        }
+        tc_fence_after();
+        const uint32_t d_tmem = tmem_base + acc * BN;
+        bool ok = true;
+        for (int kb = kb0; kb < kb1; ++kb) {
+          if (!mbar_wait(&full[stage], phase, p.status)) {
+            *abort_flag = 1;
+            ok = false;
+            break;
+          }
+          tc_fence_after();
+          const uint32_t a_addr = smem_u32(smem + stage * C::kStageBytes);
+          const uint32_t b_addr = a_addr + C::kABytes;
+#pragma unroll
+          for (int k = 0; k < 4; ++k) {
+            mma_bf16_ss(d_tmem, sdesc_kmajor_sw128(a_addr + k * 32),
+                        sdesc_kmajor_sw128(b_addr + k * 32), kIdesc, (kb > kb0 || k > 0) ? 1u : 0u);
+          }
+          mma_commit(&empty[stage]);
+          if (++stage == S) {
+            stage = 0;
+            phase ^= 1;
+          }
+        }
+        if (!ok) break;
+        mma_commit(&tfull[acc]);
+        if (++acc == 2) {
+          acc = 0;
+          acc_phase ^= 1;
+        }
+      }
+    }
+  } else {
+    // ------------------------------------------------------------- epilogue
+    const int quarter = warp % 4;
+    int acc = 0;
+    uint32_t acc_phase = 0;
+    for (int u = blockIdx.x; u < units; u += gridDim.x) {
+      const int mb = u % p.num_m_blk;
+      const int rest = u / p.num_m_blk;
+      const int nb = rest % p.num_n_blk;
+      const int ks = rest / p.num_n_blk;
+      const bool ok = __all_sync(0xffffffffu, mbar_wait(&tfull[acc], acc_phase, p.status));
+      if (!ok) {
+        *abort_flag = 1;
+        break;
+      }
+      __syncwarp();
+      tc_fence_after();
+      const int row = mb * 128 + quarter * 32 + lane;
+      const uint32_t taddr = tmem_base + ((uint32_t)(quarter * 32) << 16) + acc * BN;
+      if (EPI == EPI_QKV)
+        epi_qkv<BN>(p, taddr, row, nb);
+      else if (EPI == EPI_SWAP)
+        epi_swap<BN>(p, taddr, row, nb, ks);
+      else
+        epi_store_rows<BN>(p, taddr, row, nb, EPI);
+      tc_fence_before();
+      __syncwarp();
+      if (lane == 0) mbar_arrive(&tempty[acc]);
+      if (++acc == 2) {
+        acc = 0;
+        acc_phase ^= 1;
+      }
+    }
+  }
+  tc_fence_before();
+  __syncthreads();
+  if (warp == 1) {
+    tc_fence_after();
+    tmem_dealloc(tmem_base, C::kTmemCols);
+  }
+}
+
+// ======================================================================= host
+// Status word of the single-step entry point (timeouts of a bare GEMM call).
+__device__ uint32_t g_op_status;
+
+typedef CUresult (*EncodeTiledFn)(CUtensorMap*, CUtensorMapDataType, cuuint32_t, void*,
+                                  const cuuint64_t*, const cuuint64_t*, const cuuint32_t*,
+                                  const cuuint32_t*, CUtensorMapInterleave, CUtensorMapSwizzle,
+                                  CUtensorMapL2promotion, CUtensorMapFloatOOBfill);
+
+static EncodeTiledFn encode_fn() {
+  static EncodeTiledFn fn = nullptr;
+  if (!fn) {
+    void* p = nullptr;
+    cudaDriverEntryPointQueryResult q;
+    if (cudaGetDriverEntryPointByVersion("cuTensorMapEncodeTiled", &p, 12000, cudaEnableDefault,
+                                         &q) == cudaSuccess &&
+        q == cudaDriverEntryPointSuccess)
+      fn = reinterpret_cast<EncodeTiledFn>(p);
+  }
+  return fn;
+}
+
+// Row-major bf16 matrix [rows, cols] viewed as 2D (x = column, y = row); box of
+// 64 columns (128 bytes, the swizzle width) by box_rows rows.
+static bool make_map(CUtensorMap* map, const void* base, uint64_t rows, uint64_t cols,
+                     uint32_t box_rows) {
+  EncodeTiledFn fn = encode_fn();
+  if (!fn) return false;
+  cuuint64_t dims[2] = {cols, rows};
+  cuuint64_t strides[1] = {cols * 2};
+  cuuint32_t box[2] = {64, box_rows};
+  cuuint32_t estr[2] = {1, 1};
+  return fn(map, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 2, const_cast<void*>(base), dims, strides, box,
+            estr, CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B,
+            CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
+}
+
+struct LayerMaps {
+  CUtensorMap wq, wk, wv, wo, wfc, wproj;
+};
+
+struct TcModel {
+  nc_config cfg;
+  int sm_count = 148;
+  std::vector<LayerMaps> layers;
+  CUtensorMap lm;
+  void *xn, *att, *h, *xnl;
+  size_t max_rows;
+  uint32_t* status;
+};
+
+static int sm_count_now() {
+  int dev = 0, n = 148;
+  cudaGetDevice(&dev);
+  cudaDeviceGetAttribute(&n, cudaDevAttrMultiProcessorCount, dev);
+  return n;
+}
+
+template <int BN, int EPI>
+static nc_status launch_gemm(const CUtensorMap& a0, const CUtensorMap& a1, const CUtensorMap& a2,
+                             const CUtensorMap& b0, const CUtensorMap& b1, const CUtensorMap& b2,
+                             const GemmArgs& args, int sm_count, cudaStream_t s) {
+  using C = TileCfg<BN>;
+  auto kern = gemm_tc_kernel<BN, EPI>;
+  static bool configured = false;
+  if (!configured) {
+    if (cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                             (int)C::kSmemBytes) != cudaSuccess)
+      return NC_ERR_CUDA;
+    configured = true;
+  }
+  const int units = args.num_m_blk * args.num_n_blk * args.k_splits;
+  const int grid = std::min(units, sm_count);
+  kern<<<grid, 192, C::kSmemBytes, s>>>(a0, a1, a2, b0, b1, b2, args);
+  return cudaGetLastError() == cudaSuccess ? NC_OK : NC_ERR_CUDA;
+}
+
+static GemmArgs base_args(int M, int N, int K, int BN, uint32_t* status) {
+  GemmArgs a{};
+  a.M = M;
+  a.N = N;
+  a.num_m_blk = (M + 127) / 128;
+  a.num_n_blk = (N + BN - 1) / BN;
+  a.num_k_blk = K / 64;
+  a.k_splits = 1;
+  a.k_per_split = a.num_k_blk;
+  a.a_split0 = a.a_split1 = INT_MAX;
+  a.b_split0 = a.b_split1 = INT_MAX;
+  a.status = status;
+  return a;
+}
+
+// tile mode: N tile 128 or 256, whichever wastes less of the last wave
+static int pick_bn(int M, int N, int sm_count) {
+  const int mb = (M + 127) / 128;
+  auto cost = [&](int bn) {
+    const int units = mb * ((N + bn - 1) / bn);
+    return (int64_t)((units + sm_count - 1) / sm_count) * bn;
+  };
+  return cost(256) < cost(128) ? 256 : 128;
+}
+
+template <int EPI>
+static nc_status tile_gemm(const CUtensorMap& a, const CUtensorMap& b0, const CUtensorMap& b1,
+                           const CUtensorMap& b2, GemmArgs args, int BN, int sm_count,
+                           cudaStream_t s) {
+  if (BN == 256) return launch_gemm<256, EPI>(a, a, a, b0, b1, b2, args, sm_count, s);
+  return launch_gemm<128, EPI>(a, a, a, b0, b1, b2, args, sm_count, s);
+}
+
+// swap mode: features (weight rows, A) x tokens (B), split over K
+static void plan_splits(GemmArgs& a, int sm_count) {
+  int splits = std::max(1, sm_count / a.num_m_blk);
+  splits = std::min(splits, std::min(kMaxSplits, a.num_k_blk));
+  a.k_per_split = (a.num_k_blk + splits - 1) / splits;
+  a.k_splits = (a.num_k_blk + a.k_per_split - 1) / a.k_per_split;
+}
+
+static int swap_bn(int64_t M) { return M <= 32 ? 32 : (M <= 64 ? 64 : 128); }
+
+static nc_status swap_gemm(const CUtensorMap& a0, const CUtensorMap& a1, const CUtensorMap& a2,
+                           const void* act, int64_t M, int K, GemmArgs args, int sm_count,
+                           cudaStream_t s) {
+  const int BN = swap_bn(M);
+  CUtensorMap b;
+  if (!make_map(&b, act, (uint64_t)M, (uint64_t)K, BN)) return NC_ERR_CUDA;
+  args.num_n_blk = 1;
+  if (BN == 32) return launch_gemm<32, EPI_SWAP>(a0, a1, a2, b, b, b, args, sm_count, s);
+  if (BN == 64) return launch_gemm<64, EPI_SWAP>(a0, a1, a2, b, b, b, args, sm_count, s);
+  return launch_gemm<128, EPI_SWAP>(a0, a1, a2, b, b, b, args, sm_count, s);
+}
+
+// split-K partial sums of Y^T = W X^T, written as part[split][token][feature]
+static nc_status swap_partials(TcModel* t, const CUtensorMap& w0, const CUtensorMap& w1,
+                               const CUtensorMap& w2, int split0, int split1, int n_feat, int K,
+                               const void* act, int64_t M, float* part, int* n_split,
+                               cudaStream_t s) {
+  GemmArgs a = base_args(n_feat, (int)M, K, swap_bn(M), t->status);
+  a.a_split0 = split0;
+  a.a_split1 = split1;
+  plan_splits(a, t->sm_count);
+  a.out_f32 = part;
+  a.ldo = n_feat;
+  a.split_stride = (int64_t)M * n_feat;
+  *n_split = a.k_splits;
+  return swap_gemm(w0, w1, w2, act, M, K, a, t->sm_count, s);
+}
+
+nc_status tc_create(const nc_config& cfg, const void* wte, const void* lm_head,
+                    const void* const* wq, const void* const* wk, const void* const* wv,
+                    const void* const* wo, const void* const* w_fc, const void* const* w_proj,
+                    void* xn, void* att, void* h, void* xnl, size_t max_rows, uint32_t* status,
+                    TcModel** out) {
+  (void)wte;
+  if (!encode_fn()) return NC_ERR_CUDA;
+  TcModel* t = new TcModel();
+  t->cfg = cfg;
+  t->sm_count = sm_count_now();
+  t->xn = xn;
+  t->att = att;
+  t->h = h;
+  t->xnl = xnl;
+  t->max_rows = max_rows;
+  t->status = status;
+  const uint64_t d = cfg.d_model, qd = (uint64_t)cfg.n_head * 128, kvd = (uint64_t)cfg.n_kv_head * 128,
+                 F = cfg.d_mlp;
+  t->layers.resize(cfg.n_layer);
+  bool ok = make_map(&t->lm, lm_head, cfg.vocab, d, 128);
+  for (int l = 0; l < cfg.n_layer && ok; ++l) {
+    LayerMaps& m = t->layers[l];
+    ok = make_map(&m.wq, wq[l], qd, d, 128) && make_map(&m.wk, wk[l], kvd, d, 128) &&
+         make_map(&m.wv, wv[l], kvd, d, 128) && make_map(&m.wo, wo[l], d, qd, 128) &&
+         make_map(&m.wfc, w_fc[l], F, d, 128) && make_map(&m.wproj, w_proj[l], d, F, 128);
+  }
+  if (!ok) {
+    delete t;
+    return NC_ERR_CUDA;
+  }
+  *out = t;
+  return NC_OK;
+}
+
+void tc_destroy(TcModel* t) { delete t; }
+
+nc_status tc_qkv(TcModel* t, int l, int64_t M, const RowMap& rm, const QkvDst& dst, float* part,
+                 cudaStream_t s) {
+  const nc_config& c = t->cfg;
+  const LayerMaps& w = t->layers[l];
+  const int d = c.d_model, qd = c.n_head * 128, kvd = c.n_kv_head * 128;
+  const int nqkv = qd + 2 * kvd;
+  if (M <= kSwapMaxRows) {
+    int ns = 1;
+    nc_status st = swap_partials(t, w.wq, w.wk, w.wv, qd, qd + kvd, nqkv, d, t->xn, M, part, &ns, s);
+    if (st != NC_OK) return st;
+    launch_qkv_post(part, ns, M, rm, dst, NC_BF16, s);
+    return cudaGetLastError() == cudaSuccess ? NC_OK : NC_ERR_CUDA;
+  }
+  CUtensorMap a;
+  if (!make_map(&a, t->xn, (uint64_t)M, d, 128)) return NC_ERR_CUDA;
+  GemmArgs args = base_args((int)M, nqkv, d, 256, t->status);
+  args.b_split0 = qd;
+  args.b_split1 = qd + kvd;
+  args.rm = rm;
+  args.qkv = dst;
+  return launch_gemm<256, EPI_QKV>(a, a, a, w.wq, w.wk, w.wv, args, t->sm_count, s);
+}
+
+nc_status tc_out_proj(TcModel* t, int l, int64_t M, float* x, float* part, cudaStream_t s) {
+  const nc_config& c = t->cfg;
+  const LayerMaps& w = t->layers[l];
+  const int d = c.d_model, qd = c.n_head * 128;
+  if (M <= kSwapMaxRows) {
+    int ns = 1;
+    nc_status st = swap_partials(t, w.wo, w.wo, w.wo, INT_MAX, INT_MAX, d, qd, t->att, M, part, &ns, s);
+    if (st != NC_OK) return st;
+    launch_residual_finish(part, ns, x, M, d, nullptr, NC_BF16, c.rms_eps, s);
+    return cudaGetLastError() == cudaSuccess ? NC_OK : NC_ERR_CUDA;
+  }
+  CUtensorMap a;
+  if (!make_map(&a, t->att, (uint64_t)M, qd, 128)) return NC_ERR_CUDA;
+  const int BN = pick_bn((int)M, d, t->sm_count);
+  GemmArgs args = base_args((int)M, d, qd, BN, t->status);
+  args.out_f32 = x;
+  args.ldo = d;
+  return tile_gemm<EPI_RESID>(a, w.wo, w.wo, w.wo, args, BN, t->sm_count, s);
+}
+
+nc_status tc_mlp(TcModel* t, int l, int64_t M, float* x, float* part, cudaStream_t s) {
+  const nc_config& c = t->cfg;
+  const LayerMaps& w = t->layers[l];
+  const int d = c.d_model, F = c.d_mlp;
+  if (M <= kSwapMaxRows) {
+    int ns = 1;
+    nc_status st = swap_partials(t, w.wfc, w.wfc, w.wfc, INT_MAX, INT_MAX, F, d, t->xn, M, part, &ns, s);
+    if (st != NC_OK) return st;
+    launch_relu2_finish(part, ns, t->h, M, F, NC_BF16, s);
+    st = swap_partials(t, w.wproj, w.wproj, w.wproj, INT_MAX, INT_MAX, d, F, t->h, M, part, &ns, s);
+    if (st != NC_OK) return st;
+    launch_residual_finish(part, ns, x, M, d, nullptr, NC_BF16, c.rms_eps, s);
+    return cudaGetLastError() == cudaSuccess ? NC_OK : NC_ERR_CUDA;
+  }
+  CUtensorMap a;
+  if (!make_map(&a, t->xn, (uint64_t)M, d, 128)) return NC_ERR_CUDA;
+  int BN = pick_bn((int)M, F, t->sm_count);
+  GemmArgs args = base_args((int)M, F, d, BN, t->status);
+  args.out_bf16 = reinterpret_cast<bf16*>(t->h);
+  args.ldo = F;
+  nc_status st = tile_gemm<EPI_RELU2>(a, w.wfc, w.wfc, w.wfc, args, BN, t->sm_count, s);
+  if (st != NC_OK) return st;
+  CUtensorMap a2;
+  if (!make_map(&a2, t->h, (uint64_t)M, F, 128)) return NC_ERR_CUDA;
+  BN = pick_bn((int)M, d, t->sm_count);
+  args = base_args((int)M, d, F, BN, t->status);
+  args.out_f32 = x;
+  args.ldo = d;
+  return tile_gemm<EPI_RESID>(a2, w.wproj, w.wproj, w.wproj, args, BN, t->sm_count, s);
+}
+
+nc_status tc_lm_head(TcModel* t, const void* xn, int64_t M, float* logits, float* part,
+                     cudaStream_t s) {
+  (void)part;
+  const nc_config& c = t->cfg;
+  const int d = c.d_model, V = c.vocab;
+  if (M <= kSwapMaxRows) {
+    GemmArgs a = base_args(V, (int)M, d, swap_bn(M), t->status);
+    a.out_f32 = logits;
+    a.ldo = V;
+    a.split_stride = 0;
+    return swap_gemm(t->lm, t->lm, t->lm, xn, M, d, a, t->sm_count, s);
+  }
+  CUtensorMap a;
+  if (!make_map(&a, xn, (uint64_t)M, d, 128)) return NC_ERR_CUDA;
+  GemmArgs args = base_args((int)M, V, d, 256, t->status);
+  args.out_f32 = logits;
+  args.ldo = V;
+  return tile_gemm<EPI_F32>(a, t->lm, t->lm, t->lm, args, 256, t->sm_count, s);
+}
+
+nc_status tc_gemm_f32out(const void* A, const void* B, float* C, int M, int N, int K,
+                         cudaStream_t s) {
+  CUtensorMap a, b;
+  if (!make_map(&a, A, (uint64_t)M, (uint64_t)K, 128) || !make_map(&b, B, (uint64_t)N, (uint64_t)K, 128))
+    return NC_ERR_CUDA;
+  const int sm = sm_count_now();
+  const int BN = pick_bn(M, N, sm);
+  GemmArgs args = base_args(M, N, K, BN, nullptr);
+  if (cudaGetSymbolAddress(reinterpret_cast<void**>(&args.status), g_op_status) != cudaSuccess)
+    return NC_ERR_CUDA;
+  args.out_f32 = C;
+  args.ldo = N;
+  return tile_gemm<EPI_F32>(a, b, b, b, args, BN, sm, s);
+}
+
+}  // namespace nc
