@@ -1,0 +1,471 @@
+#!/usr/bin/env python
+"""Benchmark of the GPT forward pass on B300: d20 prefill tokens/s and d20-MQA
+KV-cache decode tokens/s, with their roofline fractions.
+
+    python bench.py [--gpus N] [--steps K] [--warmup W] [--impl ours|reference]
+
+One step = one pass of the whole path over one batch of synthetic input:
+  (a) prefill of the d20 model, batch 4 x 2048 tokens, every position's logits;
+  (b) 128 greedy decode steps of the d20 MQA model, batch 32, over a KV cache
+      prefilled (once, before timing) to 1024 positions; each step replays the
+      same decode window (cache length set back to 1024, same start tokens).
+`value` is (a)'s tokens/s; the decode rate is reported under "decode". Inputs
+(weights ~1.1-1.7 GB, logits 2.1 GB, KV cache) are larger than the 126 MB L2.
+
+N > 1 (torchrun): every rank runs an independent replica of the same work on
+its own GPU (the path has no cross-sequence exchange); times are the max over
+ranks and `value` sums the ranks' tokens. `--impl reference` times the CPU
+oracle on a bounded sample of the same workload instead.
+"""
+from __future__ import annotations
+
+import argparse
+import json
+import os
+import statistics
+import subprocess
+import sys
+import tempfile
+import time
+
+ROOT = os.path.dirname(os.path.abspath(__file__))
+sys.path.insert(0, ROOT)
+
+METRIC = "d20 bf16 prefill tok/s & KV-cache decode tok/s on 1 B300; % of roofline"
+PEAKS_FALLBACK = {"hbm_gbs": 6400.0, "bf16_tflops": 1800.0, "bf16_tflops_sustained": 1400.0}
+NOMINAL = {"hbm_gbs": 8000.0, "bf16_tflops": 2250.0}
+DECODE_STEPS = 128
+
+
+# ------------------------------------------------------------------- helpers
+def load_peaks():
+    path = os.path.join(ROOT, "MEASURED_PEAKS.json")
+    if os.path.exists(path):
+        with open(path) as f:
+            p = json.load(f)
+        return p, "measured"
+    return PEAKS_FALLBACK, "fallback"
+
+
+def dist_env():
+    world = int(os.environ.get("WORLD_SIZE", "1"))
+    rank = int(os.environ.get("RANK", "0"))
+    local = int(os.environ.get("LOCAL_RANK", "0"))
+    return world, rank, local
+
+
+def reduce_max(values, world, device=None):
+    """Element-wise max over ranks (identity for one rank)."""
+    if world == 1:
+        return list(values)
+    import torch
+    import torch.distributed as dist
+    t = torch.tensor(values, dtype=torch.float64, device=device)
+    dist.all_reduce(t, op=dist.ReduceOp.MAX)
+    return t.tolist()
+
+
+def barrier(world):
+    if world > 1:
+        import torch.distributed as dist
+        dist.barrier()
+
+
+def prefill_flops(shape, B, T):
+    """Algorithmic FLOPs of one prefill: 2 per multiply-add over the projection
+    and LM-head matrices, plus causal attention (4*hd per visible (q, k) pair and head)."""
+    d, H, Hkv, hd, F, L, V = (shape.d_model, shape.n_head, shape.n_kv_head, shape.head_dim,
+                              shape.d_mlp, shape.n_layer, shape.vocab)
+    M = B * T
+    per_layer = d * (H + 2 * Hkv) * hd + H * hd * d + 2 * d * F
+    gemm = 2 * M * (L * per_layer + d * V)
+    attn = 4 * hd * H * (T * (T + 1) // 2) * B * L
+    return gemm, attn
+
+
+def gemm_flops_by_kind(shape, M):
+    d, H, Hkv, hd, F, L, V = (shape.d_model, shape.n_head, shape.n_kv_head, shape.head_dim,
+                              shape.d_mlp, shape.n_layer, shape.vocab)
+    return {"qkv": 2 * M * d * (H + 2 * Hkv) * hd, "oproj": 2 * M * H * hd * d,
+            "fc": 2 * M * d * F, "proj": 2 * M * F * d, "lm_head": 2 * M * d * V}
+
+
+def decode_bytes(shape, B, ctx):
+    """Algorithmic HBM bytes of one decode step at context ctx (positions 0..ctx-1
+    attended): 16-bit weights read once, K/V of every position read, the new K/V
+    row written, fp32 logits written."""
+    d, H, Hkv, hd, F, L, V = (shape.d_model, shape.n_head, shape.n_kv_head, shape.head_dim,
+                              shape.d_mlp, shape.n_layer, shape.vocab)
+    weights = 2 * (L * (d * (H + 2 * Hkv) * hd + H * hd * d + 2 * d * F) + V * d)
+    kv = 2 * L * B * Hkv * hd * 2 * (ctx + 1)
+    logits = 4 * B * V
+    return weights + kv + logits
+
+
+class ClockSampler:
+    """nvidia-smi samples of SM clock and throttle reasons during the timed region."""
+    QUERY = ("index,clocks.sm,clocks.max.sm,power.draw,clocks_event_reasons.active,"
+             "clocks_event_reasons.hw_slowdown,clocks_event_reasons.hw_thermal_slowdown,"
+             "clocks_event_reasons.sw_thermal_slowdown,clocks_event_reasons.sw_power_cap")
+
+    def __init__(self, gpu_index):
+        self.gpu = gpu_index
+        self.proc = None
+        self.file = None
+
+    def __enter__(self):
+        self.file = tempfile.NamedTemporaryFile("w+", suffix=".csv", delete=False)
+        try:
+            self.proc = subprocess.Popen(
+                ["nvidia-smi", "-i", str(self.gpu), f"--query-gpu={self.QUERY}",
+                 "--format=csv,noheader,nounits", "-lms", "200"],
+                stdout=self.file, stderr=subprocess.DEVNULL)
+        except OSError:
+            self.proc = None
+        time.sleep(0.3)
+        return self
+
+    def __exit__(self, *exc):
+        if self.proc is not None:
+            self.proc.terminate()
+            try:
+                self.proc.wait(timeout=5)
+            except subprocess.TimeoutExpired:
+                self.proc.kill()
+
+    def summary(self):
+        if self.proc is None:
+            return {"sm_mhz": None, "sm_max_mhz": None, "reasons": ["nvidia-smi unavailable"]}
+        self.file.seek(0)
+        rows = [l.split(",") for l in self.file.read().strip().splitlines() if l.strip()]
+        os.unlink(self.file.name)
+        sm, smax, power, reasons = [], [], [], set()
+        names = ["hw_slowdown", "hw_thermal_slowdown", "sw_thermal_slowdown", "sw_power_cap"]
+        for r in rows:
+            r = [x.strip() for x in r]
+            try:
+                sm.append(float(r[1]))
+                smax.append(float(r[2]))
+                power.append(float(r[3]))
+            except (ValueError, IndexError):
+                continue
+            for n, v in zip(names, r[5:9]):
+                if v.lower() == "active":
+                    reasons.add(n)
+        return {"sm_mhz": statistics.median(sm) if sm else None,
+                "sm_max_mhz": max(smax) if smax else None,
+                "power_w_max": max(power) if power else None,
+                "samples": len(sm), "reasons": sorted(reasons)}
+
+
+# ------------------------------------------------------------------ our arm
+def run_ours(args):
+    import numpy as np
+    import torch
+
+    from transformer_forward_gpt_b300 import binding as nc
+    from transformer_forward_gpt_b300 import synth
+
+    world, rank, local = dist_env()
+    torch.cuda.set_device(local)
+    if world > 1:
+        import torch.distributed as dist
+        dist.init_process_group("nccl", device_id=torch.device("cuda", local))
+    dev = torch.device("cuda", local)
+    stream = torch.cuda.current_stream()
+    peaks, peak_src = load_peaks()
+
+    # (a) d20 prefill
+    wl_p = synth.WORKLOADS["d20_prefill"]
+    sp, Bp, Tp = wl_p.shape, wl_p.batch, wl_p.seq
+    Wp = synth.make_weights(sp)
+    mp = nc.Model(Wp, max_seq=Tp, max_batch=Bp)
+    del Wp
+    cp = mp.cache(Bp, Tp)
+    tok_p = torch.from_numpy(synth.make_tokens(sp, Bp, Tp)).to(dev)
+    logits_p = torch.empty(Bp, Tp, sp.vocab, device=dev)
+
+    # (b) d20-MQA decode over a 1024-position cache
+    wl_d = synth.WORKLOADS["d20_mqa_decode"]
+    sd, Bd, Td = wl_d.shape, wl_d.batch, wl_d.seq
+    steps = wl_d.decode_steps
+    Wd = synth.make_weights(sd)
+    md = nc.Model(Wd, max_seq=Td + steps, max_batch=Bd)
+    del Wd
+    cd = md.cache(Bd, Td + steps)
+    prompt_d = synth.make_tokens(sd, Bd, Td)
+    tok0 = torch.empty(Bd, dtype=torch.int32, device=dev)
+    nc.nc_prefill_last(md.handle, torch.from_numpy(prompt_d).to(dev), Bd, Td, None, tok0, cd.handle)
+    tok_buf = torch.empty(Bd, dtype=torch.int32, device=dev)
+    torch.cuda.synchronize()
+
+    def prefill_phase():
+        nc.nc_prefill(mp.handle, tok_p, Bp, Tp, logits_p, cp.handle, stream)
+
+    def decode_phase():
+        nc.nc_kv_cache_set_length(cd.handle, Td)
+        tok_buf.copy_(tok0)
+        for j in range(steps):
+            nc.nc_decode_step(md.handle, tok_buf, Bd, Td + j, None, tok_buf, cd.handle, stream)
+
+    for _ in range(args.warmup):
+        prefill_phase()
+        decode_phase()
+    torch.cuda.synchronize()
+    for m in (mp, md):
+        st = nc.nc_model_check(m.handle)
+        if st != nc.NC_OK:
+            raise RuntimeError(f"device status {st} after warm-up")
+
+    ev = [[torch.cuda.Event(enable_timing=True) for _ in range(3)] for _ in range(args.steps)]
+    barrier(world)
+    torch.cuda.synchronize()
+    launches0 = nc.nc_launch_count()
+    with ClockSampler(local) as clk:
+        t_wall0 = time.perf_counter()
+        for k in range(args.steps):
+            ev[k][0].record(stream)
+            prefill_phase()
+            ev[k][1].record(stream)
+            decode_phase()
+            ev[k][2].record(stream)
+        torch.cuda.synchronize()
+        t_wall = time.perf_counter() - t_wall0
+    barrier(world)
+    launches = nc.nc_launch_count() - launches0
+    pre_ms = sum(e[0].elapsed_time(e[1]) for e in ev)
+    dec_ms = sum(e[1].elapsed_time(e[2]) for e in ev)
+    pre_ms, dec_ms, t_wall = reduce_max([pre_ms, dec_ms, t_wall], world, dev)
+    clocks = clk.summary()
+
+    # per-kernel-class device time: one more step with the library's event pairs on
+    nc.nc_profile_begin(mp.handle)
+    prefill_phase()
+    prof_p = nc.nc_profile_end(mp.handle, stream)
+    nc.nc_profile_begin(md.handle)
+    decode_phase()
+    prof_d = nc.nc_profile_end(md.handle, stream)
+
+    # end to end through the C ABI with host buffers
+    e2e = run_e2e(nc, synth, mp, cp, md, cd, sp, Bp, Tp, sd, Bd, Td, steps, args, dev, stream)
+
+    if rank != 0:
+        return
+    K = args.steps
+    tok_pre = Bp * Tp * K * world
+    tok_dec = Bd * steps * K * world
+    value = tok_pre / (pre_ms / 1e3)
+    dec_value = tok_dec / (dec_ms / 1e3)
+    g_flops, a_flops = prefill_flops(sp, Bp, Tp)
+    bf16_peak = peaks["bf16_tflops"]
+    pre_tflops = (g_flops + a_flops) / (pre_ms / K / 1e3) / 1e12
+    ctxs = [Td + j for j in range(steps)]
+    dec_bytes = sum(decode_bytes(sd, Bd, c) for c in ctxs)
+    dec_gbs = dec_bytes / (dec_ms / K / 1e3) / 1e9
+
+    # dominant kernel class of the step (device time), its roofline
+    merged = {}
+    for name, prof in (("prefill", prof_p), ("decode", prof_d)):
+        for kind, (ms, n) in prof.items():
+            if n:
+                merged[f"{name}.{kind}"] = (ms, n)
+    dom, (dom_ms, dom_n) = max(merged.items(), key=lambda kv: kv[1][0])
+    phase, kind = dom.split(".")
+    if phase == "prefill" and kind in ("qkv", "oproj", "fc", "proj", "lm_head"):
+        fl = gemm_flops_by_kind(sp, Bp * Tp)[kind]
+        per_launch_flops = fl * (sp.n_layer if kind != "lm_head" else 1) / dom_n
+        achieved = per_launch_flops / (dom_ms / dom_n / 1e3) / 1e12
+        peak = peaks.get("bf16_tflops_sustained", bf16_peak)
+        roof = {"kernel": dom, "bound": "tensor", "achieved": round(achieved, 1),
+                "peak": peak, "unit": "TFLOP/s", "frac": round(achieved / peak, 4),
+                "traffic": None, "peak_source": f"{peak_src} bf16 sustained (fp16 operands, 1:1)",
+                "per_launch_flops": per_launch_flops, "launch_ms": dom_ms / dom_n}
+    elif phase == "prefill" and kind == "attn_prefill":
+        per_launch = a_flops / dom_n
+        achieved = per_launch / (dom_ms / dom_n / 1e3) / 1e12
+        peak = peaks.get("bf16_tflops_sustained", bf16_peak)
+        roof = {"kernel": dom, "bound": "tensor", "achieved": round(achieved, 1), "peak": peak,
+                "unit": "TFLOP/s", "frac": round(achieved / peak, 4), "traffic": None,
+                "peak_source": f"{peak_src} bf16 sustained", "per_launch_flops": per_launch,
+                "launch_ms": dom_ms / dom_n}
+    else:
+        # decode classes are HBM-bound: algorithmic bytes of the class per launch
+        roof = decode_kind_roofline(sd, Bd, ctxs, kind, dom_ms, dom_n, peaks, peak_src)
+        roof["kernel"] = dom
+
+    line = {
+        "metric": METRIC, "value": round(value, 1), "unit": "tok/s", "n_gpus": world,
+        "steps": K, "warmup": args.warmup, "ms_per_step": round((pre_ms + dec_ms) / K, 3),
+        "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": "f16",
+        "data": "synthetic (seeded N(0,1/sqrt(fan_in)) bf16 weights, uniform tokens)",
+        "config": {"workload": f"d20 prefill B{Bp}xT{Tp} + d20-MQA decode B{Bd} ctx {Td}..{Td + steps - 1}, {steps} steps",
+                   "global_batch": Bp * world, "seq_len": Tp, "parallelism": f"replicas x{world}",
+                   "l2": "inputs larger than L2 (no flush)"},
+        "prefill": {"value": round(value, 1), "unit": "tok/s", "ms": round(pre_ms / K, 3),
+                    "tflops": round(pre_tflops, 1), "algorithmic_tflop": round((g_flops + a_flops) / 1e12, 3),
+                    "frac_of_measured_peak": round(pre_tflops / bf16_peak, 4),
+                    "frac_of_nominal_peak": round(pre_tflops / NOMINAL["bf16_tflops"], 4)},
+        "decode": {"value": round(dec_value, 1), "unit": "tok/s", "ms_per_token_step": round(dec_ms / K / steps, 4),
+                   "gbs": round(dec_gbs, 1), "algorithmic_mb_per_step": round(dec_bytes / steps / 1e6, 1),
+                   "frac_of_measured_peak": round(dec_gbs / peaks["hbm_gbs"], 4),
+                   "frac_of_nominal_peak": round(dec_gbs / NOMINAL["hbm_gbs"], 4),
+                   "e2e": e2e["decode"]},
+        "roofline": roof,
+        "kernel_ms_per_step": {k: round(v[0], 3) for k, v in merged.items()},
+        "e2e": e2e["prefill"],
+        "gpu_launches": int(launches),
+        "clocks": clocks,
+        "wall_s": round(t_wall, 3),
+    }
+    if world == 1 and not args.no_cpu_baseline:
+        line["cpu_baseline"] = cpu_baseline(budget_s=args.cpu_budget)
+    print(json.dumps(line), flush=True)
+
+
+def decode_kind_roofline(shape, B, ctxs, kind, ms, n, peaks, peak_src):
+    d, H, Hkv, hd, F, L, V = (shape.d_model, shape.n_head, shape.n_kv_head, shape.head_dim,
+                              shape.d_mlp, shape.n_layer, shape.vocab)
+    steps = len(ctxs)
+    per = {"qkv": 2 * L * d * (H + 2 * Hkv) * hd, "oproj": 2 * L * H * hd * d,
+           "fc": 2 * L * d * F, "proj": 2 * L * F * d, "lm_head": 2 * V * d + 4 * B * V,
+           "attn_decode": sum(2 * L * B * Hkv * hd * 2 * (c + 1) for c in ctxs) / steps}
+    total = per.get(kind, 0) * steps
+    achieved = total / n / (ms / n / 1e3) / 1e9 if total else 0.0
+    return {"bound": "hbm", "achieved": round(achieved, 1), "peak": peaks["hbm_gbs"],
+            "unit": "GB/s", "frac": round(achieved / peaks["hbm_gbs"], 4), "traffic": None,
+            "peak_source": f"{peak_src} HBM copy", "launch_ms": ms / n}
+
+
+def run_e2e(nc, synth, mp, cp, md, cd, sp, Bp, Tp, sd, Bd, Td, steps, args, dev, stream):
+    """Prefill through the C ABI with host buffers (pinned): tokens copied in,
+    every position's logits copied out, inside the timed region. Decode through
+    nc_generate_host (prompt in, generated tokens out; includes its prefill)."""
+    import torch
+    tok_h = torch.from_numpy(synth.make_tokens(sp, Bp, Tp)).pin_memory()
+    tok_d = torch.empty(Bp, Tp, dtype=torch.int32, device=dev)
+    logits_d = torch.empty(Bp, Tp, sp.vocab, device=dev)
+    logits_h = torch.empty(Bp, Tp, sp.vocab).pin_memory()
+    reps = max(1, min(3, args.steps))
+    torch.cuda.synchronize()
+    t0 = time.perf_counter()
+    for _ in range(reps):
+        tok_d.copy_(tok_h, non_blocking=True)
+        nc.nc_prefill(mp.handle, tok_d, Bp, Tp, logits_d, cp.handle, stream)
+        logits_h.copy_(logits_d, non_blocking=True)
+        torch.cuda.synchronize()
+    t_pre = (time.perf_counter() - t0) / reps
+    prompt = torch.from_numpy(synth.make_tokens(sd, Bd, Td)).pin_memory()
+    out = torch.empty(steps + 1, Bd, dtype=torch.int32).pin_memory()
+    t0 = time.perf_counter()
+    for _ in range(reps):
+        nc.nc_generate_host(md.handle, prompt, Bd, Td, steps, out, cd.handle, stream)
+    t_gen = (time.perf_counter() - t0) / reps
+    return {"prefill": {"value": round(Bp * Tp / t_pre, 1), "unit": "tok/s",
+                        "h2d_bytes_per_step": int(tok_h.numel() * 4),
+                        "d2h_bytes_per_step": int(logits_h.numel() * 4)},
+            "decode": {"value": round(Bd * steps / t_gen, 1), "unit": "tok/s",
+                       "h2d_bytes_per_step": int(prompt.numel() * 4),
+                       "d2h_bytes_per_step": int(out.numel() * 4),
+                       "note": f"nc_generate_host: {Bd}x{Td} prompt prefill + {steps} greedy steps"}}
+
+
+# ------------------------------------------------------- CPU oracle baseline
+def host_cores():
+    try:
+        return len(os.sched_getaffinity(0))
+    except AttributeError:
+        return os.cpu_count() or 1
+
+
+def blas_threads():
+    try:
+        from threadpoolctl import threadpool_info
+        n = [i.get("num_threads", 0) for i in threadpool_info() if i.get("user_api") == "blas"]
+        return max(n) if n else host_cores()
+    except Exception:
+        return host_cores()
+
+
+def oracle_prefill_sample(T):
+    """tok/s of the oracle on one sequence of the d20 prefill workload, T tokens."""
+    from oracle import gpt_oracle as O
+    from transformer_forward_gpt_b300 import synth
+    shape = synth.D20
+    W = synth.make_weights(shape)
+    toks = synth.make_tokens(shape, 1, T)
+    t0 = time.perf_counter()
+    O.prefill(shape, W.wte, W.layers, W.lm_head, toks)
+    dt = time.perf_counter() - t0
+    return T / dt, dt
+
+
+def oracle_decode_sample(n_steps, ctx=1024):
+    """tok/s of the oracle decoding one sequence of the d20-MQA workload at ctx."""
+    from oracle import gpt_oracle as O
+    from transformer_forward_gpt_b300 import synth
+    shape = synth.D20_MQA
+    W = synth.make_weights(shape)
+    toks = synth.make_tokens(shape, 1, ctx + n_steps)
+    _, cache = O.prefill(shape, W.wte, W.layers, W.lm_head, toks[:, :ctx], t_cap=ctx + n_steps,
+                         logit_positions=[ctx - 1])
+    t0 = time.perf_counter()
+    for j in range(n_steps):
+        O.decode_step(shape, W.wte, W.layers, W.lm_head, toks[:, ctx + j], cache)
+    dt = time.perf_counter() - t0
+    return n_steps / dt, dt
+
+
+def cpu_baseline(budget_s=30.0, T=2048):
+    v, dt = oracle_prefill_sample(T)
+    dv, ddt = oracle_decode_sample(8)
+    return {"value": round(v, 2), "unit": "tok/s", "cores": blas_threads(), "kind": "oracle",
+            "sample": f"fp64 numpy oracle, 1 sequence x {T} tokens of the d20 prefill workload "
+                      f"({dt:.1f} s)", "decode_value": round(dv, 3),
+            "decode_sample": f"1 sequence of the d20-MQA workload, 8 steps at context 1024 ({ddt:.1f} s)"}
+
+
+def run_reference(args):
+    world, rank, _ = dist_env()
+    if rank != 0:
+        return
+    T = 512
+    for _ in range(args.warmup):
+        oracle_prefill_sample(T)
+    times = []
+    for _ in range(args.steps):
+        _, dt = oracle_prefill_sample(T)
+        times.append(dt)
+    total = sum(times)
+    value = T * args.steps / total
+    line = {"impl": "reference", "metric": METRIC, "value": round(value, 2), "unit": "tok/s",
+            "n_gpus": world, "steps": args.steps, "warmup": args.warmup,
+            "ms_per_step": round(total / args.steps * 1e3, 1), "higher_is_better": True,
+            "scaling": "weak", "vs_baseline": None, "dtype": "f64", "data": "synthetic",
+            "config": {"workload": f"d20 prefill, bounded sample: 1 sequence x {T} tokens per step",
+                       "global_batch": 1, "seq_len": T, "parallelism": "none (host cores)"},
+            "cpu_baseline": {"value": round(value, 2), "unit": "tok/s", "cores": blas_threads(),
+                             "kind": "oracle", "sample": f"1 x {T} tokens of d20 prefill per step"},
+            "e2e": {"value": round(value, 2), "unit": "tok/s", "h2d_bytes_per_step": 0,
+                    "d2h_bytes_per_step": 0}}
+    print(json.dumps(line), flush=True)
+
+
+def main():
+    ap = argparse.ArgumentParser(description=__doc__.splitlines()[0])
+    ap.add_argument("--gpus", type=int, default=1)
+    ap.add_argument("--steps", type=int, default=10)
+    ap.add_argument("--warmup", type=int, default=3)
+    ap.add_argument("--impl", choices=("ours", "reference"), default="ours")
+    ap.add_argument("--no-cpu-baseline", action="store_true")
+    ap.add_argument("--cpu-budget", type=float, default=30.0)
+    args = ap.parse_args()
+    if args.warmup < 3 and args.impl == "ours":
+        print("warning: fewer than 3 warm-up steps", file=sys.stderr)
+    if args.impl == "reference":
+        run_reference(args)
+    else:
+        run_ours(args)
+
+
+if __name__ == "__main__":
+    main()

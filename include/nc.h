@@ -59,24 +59,34 @@ typedef enum {
                                    the kernel used row 0 in its place */
 } nc_status;
 
-typedef enum { NC_F32 = 0, NC_BF16 = 1 } nc_dtype;
+typedef enum { NC_F32 = 0, NC_BF16 = 1, NC_F16 = 2 } nc_dtype;
 
-/* Model shape. dtype is the storage type of weights, activations and the KV
- * cache: NC_BF16 runs the tensor-core path and needs head_dim == 128,
- * d_model % 64 == 0 and d_mlp % 64 == 0; NC_F32 runs an fp32 CUDA-core path for
- * small shapes (head_dim <= 128, even). Residual stream and logits are fp32 for
- * both. max_batch * max_seq bounds the tokens of one prefill call and max_seq
- * bounds every position (cos/sin tables are built for max_seq positions). */
+/* Model shape and number formats.
+ *   dtype      storage type of the caller's weights: NC_F32, NC_BF16 or NC_F16.
+ *   act_dtype  16-bit type of the tensor-core path (ignored for NC_F32 weights,
+ *              which run an fp32 CUDA-core path for small shapes): the format of
+ *              the GEMM operands, the normalised activations, Q and the KV cache.
+ *              NC_F16 keeps 3 more mantissa bits than NC_BF16 at the same speed
+ *              and width; with bf16 rounding at every GEMM input the logits drift
+ *              ~0.03-0.04 x RMS (max) from exact arithmetic, with fp16 ~0.005.
+ *              When act_dtype differs from dtype the model keeps its own converted
+ *              copy of the projection and LM-head weights.
+ * The tensor-core path needs head_dim == 128, d_model % 64 == 0, d_mlp % 64 == 0;
+ * the fp32 path head_dim <= 128 and even. Residual stream and logits are fp32.
+ * max_batch * max_seq bounds the tokens of one prefill call and max_seq bounds
+ * every position (cos/sin tables are built for max_seq positions). */
 typedef struct {
     int32_t vocab, d_model, n_layer, n_head, n_kv_head, head_dim, d_mlp;
     float rope_base;   /* theta(t, i) = t * rope_base^(-2 i / head_dim) */
     float rms_eps;     /* x / sqrt(mean(x^2) + rms_eps) */
     int32_t max_seq, max_batch;
     nc_dtype dtype;
+    nc_dtype act_dtype;
 } nc_config;
 
 /* Weights: device pointers in cfg.dtype, row-major [out, in]. Borrowed: the
- * caller keeps them alive and unchanged for the model's lifetime. The per-layer
+ * caller keeps them alive and unchanged for the model's lifetime (wte always;
+ * the others unless the model converted them at create). The per-layer
  * members are HOST arrays of n_layer device pointers (read during create only).
  *   wte [vocab, d]      lm_head [vocab, d]       (untied)
  *   wq [H*hd, d]  wk [Hkv*hd, d]  wv [Hkv*hd, d]  wo [d, H*hd]
@@ -111,7 +121,7 @@ NC_API nc_status nc_model_create(const nc_config* cfg, const nc_weights* w, nc_m
 NC_API void nc_model_destroy(nc_model* m);
 
 /* Bytes of a KV cache: 2 (K and V) * n_layer * batch * n_kv_head * t_max * head_dim
- * * sizeof(dtype), plus 256 bytes of header. Layout of K (and V):
+ * * sizeof(activation type), plus 256 bytes of header. Layout of K (and V):
  * [n_layer][batch][n_kv_head][t_max][head_dim]; K is stored after RoPE and QK
  * norm, V as projected. */
 NC_API size_t nc_kv_cache_bytes(const nc_config* cfg, int32_t batch, int32_t t_max);
@@ -161,6 +171,11 @@ NC_API nc_status nc_decode_step(nc_model* m, const int32_t* tokens, int32_t B, i
 NC_API nc_status nc_generate_host(nc_model* m, const int32_t* prompt, int32_t B, int32_t T,
                                   int32_t steps, int32_t* out_tokens, nc_kv_cache* c, void* stream);
 
+/* Sets the cache length back to len (0 <= len <= current length): positions
+ * >= len count as empty again and are overwritten by the next prefill / decode
+ * steps (e.g. to roll back rejected tokens, or to replay a decode window). */
+NC_API nc_status nc_kv_cache_set_length(nc_kv_cache* c, int32_t len);
+
 /* Synchronises `stream`, reads and clears the device status word. Returns NC_OK,
  * NC_ERR_BOUNDS or NC_ERR_DEVICE_TIMEOUT (or NC_ERR_CUDA). */
 NC_API nc_status nc_model_check(nc_model* m, void* stream);
@@ -171,12 +186,13 @@ NC_API nc_status nc_model_check(nc_model* m, void* stream);
  * ---------------------------------------------------------------------- */
 
 /* y[m, :] = x[m, :] / sqrt(mean_j x[m, j]^2 + eps); x dev fp32 [M, d]; y dev
- * [M, d] in y_dtype. d % 4 == 0. */
+ * [M, d] in y_dtype (any of the three). d % 4 == 0. */
 NC_API nc_status nc_op_rmsnorm(const float* x, void* y, nc_dtype y_dtype, int64_t M, int32_t d,
                                float eps, void* stream);
 
-/* C = A B^T: A dev [M, K], B dev [N, K] in `dtype`, C dev fp32 [M, N]. bf16 runs
- * the tcgen05 tensor-core GEMM (K % 64 == 0); f32 runs the CUDA-core GEMM. */
+/* C = A B^T: A dev [M, K], B dev [N, K] in `dtype`, C dev fp32 [M, N]. bf16 and
+ * f16 run the tcgen05 tensor-core GEMM (K % 64 == 0, N % 16 == 0); f32 runs the
+ * CUDA-core GEMM. */
 NC_API nc_status nc_op_gemm(const void* A, const void* B, float* C, int32_t M, int32_t N,
                             int32_t K, nc_dtype dtype, void* stream);
 
@@ -201,6 +217,30 @@ NC_API nc_status nc_op_attention_decode(const void* q, const void* k, const void
 /* out[r] = index of the largest x[r, :] (lowest index on ties); x dev fp32
  * [rows, n], out dev int32 [rows]. */
 NC_API nc_status nc_op_argmax(const float* x, int32_t rows, int32_t n, int32_t* out, void* stream);
+
+/* ------------------------------------------------------------------------
+ * Measurement: per-kernel-class device time and a launch counter. Host-side
+ * bookkeeping only; results are unchanged.
+ * ---------------------------------------------------------------------- */
+typedef enum {
+    NC_K_EMBED = 0, NC_K_NORM, NC_K_QKV, NC_K_ATTN_PREFILL, NC_K_ATTN_DECODE, NC_K_OPROJ,
+    NC_K_FC, NC_K_PROJ, NC_K_LM_HEAD, NC_K_ARGMAX, NC_K_COUNT
+} nc_kernel_kind;
+
+typedef struct {
+    double ms;          /* summed device time (CUDA events on the launching stream) */
+    int64_t launches;   /* kernel launches in this class */
+} nc_kernel_time;
+
+/* From now on the model records a CUDA event pair around each kernel class it
+ * enqueues (one pair per projection / attention / norm call; a split-K
+ * projection's finishing kernel counts with its GEMM). */
+NC_API nc_status nc_profile_begin(nc_model* m);
+/* Synchronises `stream`, sums the recorded intervals into out[NC_K_COUNT] and
+ * stops recording. */
+NC_API nc_status nc_profile_end(nc_model* m, void* stream, nc_kernel_time* out);
+/* Number of kernels the library has launched in this process so far. */
+NC_API int64_t nc_launch_count(void);
 
 #ifdef __cplusplus
 }

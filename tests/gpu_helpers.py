@@ -6,7 +6,7 @@ from oracle import gpt_oracle as O
 from transformer_forward_gpt_b300 import binding as nc
 from transformer_forward_gpt_b300 import synth
 
-POISON = -1536.0   # planted in unwritten cache slots (exact in bf16); must survive exactly
+POISON = -1536.0   # planted in unwritten cache slots (exact in bf16 and fp16); must survive exactly
 
 
 def tol_for(shape):

@@ -9,20 +9,37 @@ from transformer_forward_gpt_b300 import binding as nc
 pytestmark = pytest.mark.gpu
 
 
-def _bf16(rng, shape, scale=1.0):
+UNIT_ROUNDOFF = {nc.NC_BF16: 2.0 ** -8, nc.NC_F16: 2.0 ** -11, nc.NC_F32: 2.0 ** -24}
+
+
+def _torch_dt(dt):
+    import torch
+    return {nc.NC_BF16: torch.bfloat16, nc.NC_F16: torch.float16, nc.NC_F32: torch.float32}[dt]
+
+
+def _rand(rng, shape, dt, scale=1.0):
     import torch
     return (torch.from_numpy(rng.standard_normal(shape).astype(np.float32) * scale)
-            .to("cuda").to(torch.bfloat16))
+            .to("cuda").to(_torch_dt(dt)))
 
 
+def assert_rounding_bound(got, ref, u, extra=0.0, what=""):
+    """|got - ref| <= u |ref| + extra elementwise (u = unit roundoff of the stored format)."""
+    d = np.abs(got - ref)
+    bound = u * np.abs(ref) + extra + 1e-6
+    worst = float((d / bound).max())
+    assert worst <= 1.0, f"{what}: error reaches {worst:.3g} x the rounding bound"
+
+
+@pytest.mark.parametrize("dt", [nc.NC_BF16, nc.NC_F16])
 @pytest.mark.parametrize("M,N,K", [(128, 256, 64), (300, 1664, 1280), (37, 384, 768),
                                    (1000, 4992, 1664), (257, 65536, 1280), (8192, 1280, 5120)])
-def test_gemm_bf16_tcgen05(cuda_device, M, N, K):
+def test_gemm_tcgen05(cuda_device, M, N, K, dt):
     import torch
     rng = np.random.default_rng(M + N + K)
-    A, B = _bf16(rng, (M, K)), _bf16(rng, (N, K), 1 / np.sqrt(K))
+    A, B = _rand(rng, (M, K), dt), _rand(rng, (N, K), dt, 1 / np.sqrt(K))
     C = torch.full((M, N), float("nan"), device="cuda")
-    nc.nc_op_gemm(A, B, C, M, N, K, nc.NC_BF16)
+    nc.nc_op_gemm(A, B, C, M, N, K, dt)
     torch.cuda.synchronize()
     rows = np.unique(np.linspace(0, M - 1, min(M, 64)).astype(int))
     ref = O.linear(to_np(A[rows]), to_np(B))
@@ -41,22 +58,23 @@ def test_gemm_f32_simt(cuda_device):
     assert_close(to_np(C), O.linear(to_np(A), to_np(B)), 1e-6, "fp32 gemm")
 
 
-@pytest.mark.parametrize("dt", [nc.NC_F32, nc.NC_BF16])
+@pytest.mark.parametrize("dt", [nc.NC_F32, nc.NC_BF16, nc.NC_F16])
 def test_rmsnorm(cuda_device, dt):
     import torch
     rng = np.random.default_rng(2)
     M, d = 77, 1280
     x = torch.from_numpy(rng.standard_normal((M, d)).astype(np.float32) * 3).cuda()
-    y = torch.empty(M, d, device="cuda", dtype=torch.float32 if dt == nc.NC_F32 else torch.bfloat16)
+    y = torch.empty(M, d, device="cuda", dtype=_torch_dt(dt))
     nc.nc_op_rmsnorm(x, y, dt, M, d, 1e-5)
     torch.cuda.synchronize()
     ref = O.rmsnorm(to_np(x), 1e-5)
-    assert_close(to_np(y), ref, 1e-6 if dt == nc.NC_F32 else 8e-3, "rmsnorm")
+    # fp32 arithmetic, then one rounding to the stored format
+    assert_rounding_bound(to_np(y), ref, max(UNIT_ROUNDOFF[dt], 2.0 ** -20), what="rmsnorm")
 
 
 def _attn_inputs(rng, B, H, Hkv, T, t_max, hd, dt):
     import torch
-    tdt = torch.bfloat16 if dt == nc.NC_BF16 else torch.float32
+    tdt = _torch_dt(dt)
     q = torch.from_numpy(rng.standard_normal((B, H, T, hd)).astype(np.float32)).cuda().to(tdt)
     k = torch.from_numpy(rng.standard_normal((B, Hkv, t_max, hd)).astype(np.float32)).cuda().to(tdt)
     v = torch.from_numpy(rng.standard_normal((B, Hkv, t_max, hd)).astype(np.float32)).cuda().to(tdt)
@@ -65,12 +83,14 @@ def _attn_inputs(rng, B, H, Hkv, T, t_max, hd, dt):
     return q, k, v
 
 
-@pytest.mark.parametrize("B,H,Hkv,T,dt", [(2, 4, 2, 200, nc.NC_BF16), (1, 10, 1, 129, nc.NC_BF16),
-                                          (3, 2, 2, 64, nc.NC_BF16), (1, 3, 3, 1, nc.NC_BF16),
-                                          (2, 4, 4, 37, nc.NC_F32)])
+@pytest.mark.parametrize("B,H,Hkv,T,dt", [(2, 4, 2, 200, nc.NC_BF16), (1, 10, 1, 129, nc.NC_F16),
+                                          (3, 2, 2, 64, nc.NC_F16), (1, 3, 3, 1, nc.NC_F16),
+                                          (2, 13, 13, 300, nc.NC_F16), (2, 4, 4, 37, nc.NC_F32)])
 def test_attention_prefill(cuda_device, B, H, Hkv, T, dt):
+    """Bound: the output is rounded once (u |o|) and the probabilities are rounded
+    to the operand format before P V (u max|v| at most); fp32 elsewhere."""
     import torch
-    hd = 128 if dt == nc.NC_BF16 else 8
+    hd = 8 if dt == nc.NC_F32 else 128
     t_max = T + 5
     rng = np.random.default_rng(T)
     q, k, v = _attn_inputs(rng, B, H, Hkv, T, t_max, hd, dt)
@@ -80,17 +100,20 @@ def test_attention_prefill(cuda_device, B, H, Hkv, T, dt):
     for b in range(B):
         ref = O.attend(to_np(q[b]), np.arange(T), to_np(k[b, :, :T]), to_np(v[b, :, :T]))
         got = to_np(o[b]).reshape(T, H, hd).transpose(1, 0, 2)
-        assert_close(got, ref, 2e-2 if dt == nc.NC_BF16 else 1e-5, f"attention seq {b}")
+        u = UNIT_ROUNDOFF[dt] if dt != nc.NC_F32 else 1e-5
+        vmax = float(np.abs(to_np(v[b, :, :T])).max())
+        assert_rounding_bound(got, ref, u, u * vmax, f"attention seq {b}")
         if T == 1:   # one position: output is that position's V
             g = np.arange(H) // (H // Hkv)
             assert_close(got[:, 0], to_np(v[b, g, 0]), 1e-2, "length-1 attention")
 
 
-@pytest.mark.parametrize("B,H,Hkv,length,dt", [(4, 10, 1, 1100, nc.NC_BF16), (2, 13, 13, 2049, nc.NC_BF16),
-                                               (3, 4, 2, 5, nc.NC_F32), (1, 2, 1, 1, nc.NC_BF16)])
+@pytest.mark.parametrize("B,H,Hkv,length,dt", [(4, 10, 1, 1100, nc.NC_F16), (2, 13, 13, 2049, nc.NC_F16),
+                                               (3, 4, 2, 5, nc.NC_F32), (1, 2, 1, 1, nc.NC_BF16),
+                                               (2, 10, 1, 300, nc.NC_BF16)])
 def test_attention_decode(cuda_device, B, H, Hkv, length, dt):
     import torch
-    hd = 128 if dt == nc.NC_BF16 else 8
+    hd = 8 if dt == nc.NC_F32 else 128
     t_max = length + 3
     rng = np.random.default_rng(length)
     q, k, v = _attn_inputs(rng, B, H, Hkv, length, t_max, hd, dt)
@@ -103,8 +126,8 @@ def test_attention_decode(cuda_device, B, H, Hkv, length, dt):
     for b in range(B):
         ref = O.attend(to_np(q[b]), np.array([length - 1]), to_np(k[b, :, :length]),
                        to_np(v[b, :, :length]))[:, 0]
-        assert_close(to_np(o[b]).reshape(H, hd), ref, 2e-2 if dt == nc.NC_BF16 else 1e-5,
-                     f"decode attention seq {b}")
+        u = UNIT_ROUNDOFF[dt] if dt != nc.NC_F32 else 1e-5
+        assert_rounding_bound(to_np(o[b]).reshape(H, hd), ref, u, 1e-5, f"decode attention seq {b}")
 
 
 def test_argmax_ties_and_sizes(cuda_device):

@@ -15,7 +15,7 @@ LIB_PATH = os.path.join(PKG, "libnc.so")
 
 NC_OK, NC_ERR_INVALID_ARG, NC_ERR_UNSUPPORTED, NC_ERR_OOM, NC_ERR_CUDA, \
     NC_ERR_DEVICE_TIMEOUT, NC_ERR_BOUNDS = range(7)
-NC_F32, NC_BF16 = 0, 1
+NC_F32, NC_BF16, NC_F16 = 0, 1, 2
 
 EXPORTS = (
     "nc_version", "nc_status_string", "nc_last_error", "nc_param_count", "nc_model_create",
@@ -23,14 +23,23 @@ EXPORTS = (
     "nc_kv_cache_free", "nc_prefill", "nc_prefill_last", "nc_decode_step", "nc_generate_host",
     "nc_model_check", "nc_op_rmsnorm", "nc_op_gemm", "nc_op_attention_prefill",
     "nc_op_attention_decode_scratch_bytes", "nc_op_attention_decode", "nc_op_argmax",
+    "nc_kv_cache_set_length", "nc_profile_begin", "nc_profile_end", "nc_launch_count",
 )
+
+KERNEL_KINDS = ("embed", "norm", "qkv", "attn_prefill", "attn_decode", "oproj", "fc", "proj",
+                "lm_head", "argmax")
 
 
 class NcConfig(C.Structure):
     _fields_ = [("vocab", C.c_int32), ("d_model", C.c_int32), ("n_layer", C.c_int32),
                 ("n_head", C.c_int32), ("n_kv_head", C.c_int32), ("head_dim", C.c_int32),
                 ("d_mlp", C.c_int32), ("rope_base", C.c_float), ("rms_eps", C.c_float),
-                ("max_seq", C.c_int32), ("max_batch", C.c_int32), ("dtype", C.c_int)]
+                ("max_seq", C.c_int32), ("max_batch", C.c_int32), ("dtype", C.c_int),
+                ("act_dtype", C.c_int)]
+
+
+class NcKernelTime(C.Structure):
+    _fields_ = [("ms", C.c_double), ("launches", C.c_int64)]
 
 
 class NcWeights(C.Structure):
@@ -78,6 +87,10 @@ def load(path: str = LIB_PATH):
         "nc_op_attention_decode": (C.c_int, [vp, vp, vp, vp, i32, i32, i32, i32, i32, i32,
                                              C.c_int, vp, sz, vp]),
         "nc_op_argmax": (C.c_int, [vp, i32, i32, vp, vp]),
+        "nc_kv_cache_set_length": (C.c_int, [vp, i32]),
+        "nc_profile_begin": (C.c_int, [vp]),
+        "nc_profile_end": (C.c_int, [vp, vp, C.POINTER(NcKernelTime)]),
+        "nc_launch_count": (i64, []),
     }
     for name, (res, args) in sig.items():
         f = getattr(lib, name)
@@ -118,10 +131,13 @@ def _stream(stream):
     return stream.cuda_stream
 
 
-def make_config(shape, max_seq, max_batch) -> NcConfig:
+def make_config(shape, max_seq, max_batch, act_dtype=NC_F16) -> NcConfig:
+    """Config of a synthetic shape: weights in the shape's dtype; the tensor-core
+    path keeps activations / KV cache in `act_dtype` (fp16 by default)."""
+    wdt = NC_BF16 if shape.dtype == "bf16" else NC_F32
     return NcConfig(shape.vocab, shape.d_model, shape.n_layer, shape.n_head, shape.n_kv_head,
                     shape.head_dim, shape.d_mlp, shape.rope_base, shape.rms_eps, max_seq,
-                    max_batch, NC_BF16 if shape.dtype == "bf16" else NC_F32)
+                    max_batch, wdt, NC_F32 if wdt == NC_F32 else act_dtype)
 
 
 # ------------------------------------------------------------ same-name calls
@@ -227,6 +243,25 @@ def nc_op_argmax(x, rows, n, out, stream=None):
     _check(load().nc_op_argmax(_ptr(x), rows, n, _ptr(out), _stream(stream)), "nc_op_argmax")
 
 
+def nc_kv_cache_set_length(cache, length):
+    _check(load().nc_kv_cache_set_length(cache, length), "nc_kv_cache_set_length")
+
+
+def nc_profile_begin(model):
+    _check(load().nc_profile_begin(model), "nc_profile_begin")
+
+
+def nc_profile_end(model, stream=None):
+    """{kind: (ms, launches)} of the intervals recorded since nc_profile_begin."""
+    out = (NcKernelTime * len(KERNEL_KINDS))()
+    _check(load().nc_profile_end(model, _stream(stream), out), "nc_profile_end")
+    return {k: (out[i].ms, out[i].launches) for i, k in enumerate(KERNEL_KINDS)}
+
+
+def nc_launch_count():
+    return load().nc_launch_count()
+
+
 # ----------------------------------------------------------------- helpers
 class Model:
     """Owns device copies of one synthetic model's weights plus the nc_model.
@@ -235,11 +270,11 @@ class Model:
     step runs in libnc.
     """
 
-    def __init__(self, weights, max_seq, max_batch, device="cuda"):
+    def __init__(self, weights, max_seq, max_batch, device="cuda", act_dtype=NC_F16):
         import torch
         shape = weights.shape
         self.shape = shape
-        self.cfg = make_config(shape, max_seq, max_batch)
+        self.cfg = make_config(shape, max_seq, max_batch, act_dtype)
         self.device = device
 
         def dev(name, arr):
@@ -280,7 +315,8 @@ class KVCache:
         import torch
         s = self.model.shape
         kp, vp, _, _, _ = nc_kv_cache_view(self.handle)
-        dt = torch.bfloat16 if s.dtype == "bf16" else torch.float32
+        dt = {NC_BF16: torch.bfloat16, NC_F16: torch.float16,
+              NC_F32: torch.float32}[self.model.cfg.act_dtype]
         n = s.n_layer * self.batch * s.n_kv_head * self.t_max * s.head_dim
         shp = (s.n_layer, self.batch, s.n_kv_head, self.t_max, s.head_dim)
         return tuple(_wrap_device(p, n, dt, self.model.device).view(shp) for p in (kp, vp))

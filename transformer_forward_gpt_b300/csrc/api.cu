@@ -6,6 +6,7 @@
 #include <string.h>
 
 #include <algorithm>
+#include <atomic>
 #include <vector>
 
 #include "common.cuh"
@@ -41,7 +42,9 @@ void set_err(const char* fmt, ...) {
   } while (0)
 
 bool aligned16(const void* p) { return (reinterpret_cast<uintptr_t>(p) & 15u) == 0; }
-size_t dtype_size(nc_dtype d) { return d == NC_BF16 ? 2 : 4; }
+size_t dtype_size(nc_dtype d) { return d == NC_F32 ? 4 : 2; }
+// number format of activations, Q and the KV cache
+nc_dtype act_type(const nc_config& c) { return c.dtype == NC_F32 ? NC_F32 : c.act_dtype; }
 size_t round_up(size_t x, size_t a) { return (x + a - 1) / a * a; }
 
 nc_status check_launch() {
@@ -53,10 +56,23 @@ nc_status check_launch() {
   return NC_OK;
 }
 
+std::atomic<int64_t> g_launches{0};
+
+struct ProfRec {
+  int kind;
+  int64_t launches;
+  cudaEvent_t a, b;
+};
+
 }  // namespace
+
+namespace nc {
+void count_launches(int n) { g_launches.fetch_add(n, std::memory_order_relaxed); }
+}  // namespace nc
 
 struct nc_model {
   nc_config cfg;
+  nc_dtype adt;              // activation / KV-cache format
   int device;
   const void* wte;
   const void* lm_head;
@@ -81,8 +97,46 @@ struct nc_model {
   int32_t* gen_dev = nullptr;   // [max_seq + 1, max_batch] generated tokens
   float* attn_scratch = nullptr;
   size_t attn_scratch_bytes = 0;
-  nc::TcModel* tc = nullptr;    // tensor-core state (bf16 models)
+  nc::TcModel* tc = nullptr;    // tensor-core state (16-bit models)
+  void* wcopy = nullptr;        // weights converted to adt (when it differs from cfg.dtype)
+  // measurement
+  bool prof = false;
+  std::vector<ProfRec> recs;
+  std::vector<cudaEvent_t> event_pool;
 };
+
+namespace {
+// Records a CUDA event pair around one kernel class while profiling is on.
+struct ProfScope {
+  nc_model* m;
+  int kind;
+  cudaStream_t s;
+  cudaEvent_t a = nullptr;
+  int64_t l0 = 0;
+  cudaEvent_t take() {
+    if (m->event_pool.empty()) {
+      cudaEvent_t e;
+      cudaEventCreate(&e);
+      return e;
+    }
+    cudaEvent_t e = m->event_pool.back();
+    m->event_pool.pop_back();
+    return e;
+  }
+  ProfScope(nc_model* m_, int kind_, cudaStream_t s_) : m(m_), kind(kind_), s(s_) {
+    if (!m->prof) return;
+    a = take();
+    cudaEventRecord(a, s);
+    l0 = g_launches.load();
+  }
+  ~ProfScope() {
+    if (!a) return;
+    cudaEvent_t b = take();
+    cudaEventRecord(b, s);
+    m->recs.push_back({kind, g_launches.load() - l0, a, b});
+  }
+};
+}  // namespace
 
 struct nc_kv_cache {
   const nc_model* model;
@@ -134,10 +188,13 @@ static nc_status validate_config(const nc_config* c) {
   NC_CHECK(c->d_model % 4 == 0 && c->d_mlp % 4 == 0, NC_ERR_UNSUPPORTED,
            "d_model and d_mlp must be multiples of 4");
   NC_CHECK(c->rms_eps >= 0.f && c->rope_base > 0.f, NC_ERR_INVALID_ARG, "bad eps / rope base");
-  NC_CHECK(c->dtype == NC_F32 || c->dtype == NC_BF16, NC_ERR_INVALID_ARG, "bad dtype");
-  if (c->dtype == NC_BF16) {
+  NC_CHECK(c->dtype == NC_F32 || c->dtype == NC_BF16 || c->dtype == NC_F16, NC_ERR_INVALID_ARG,
+           "bad dtype");
+  if (c->dtype != NC_F32) {
+    NC_CHECK(c->act_dtype == NC_BF16 || c->act_dtype == NC_F16, NC_ERR_INVALID_ARG,
+             "act_dtype must be NC_BF16 or NC_F16 for 16-bit weights");
     NC_CHECK(c->head_dim == 128 && c->d_model % 64 == 0 && c->d_mlp % 64 == 0, NC_ERR_UNSUPPORTED,
-             "bf16 path needs head_dim 128 and d_model, d_mlp multiples of 64");
+             "tensor-core path needs head_dim 128 and d_model, d_mlp multiples of 64");
   }
   return NC_OK;
 }
@@ -148,6 +205,12 @@ void nc_model_destroy(nc_model* m) {
   cudaGetDevice(&prev);
   cudaSetDevice(m->device);
   if (m->tc) nc::tc_destroy(m->tc);
+  for (auto& r : m->recs) {
+    cudaEventDestroy(r.a);
+    cudaEventDestroy(r.b);
+  }
+  for (auto e : m->event_pool) cudaEventDestroy(e);
+  cudaFree(m->wcopy);
   cudaFree(m->ws);
   cudaFree(m->cos_tab);
   cudaFree(m->sin_tab);
@@ -173,6 +236,8 @@ nc_status nc_model_create(const nc_config* cfg, const nc_weights* w, nc_model** 
   }
   nc_model* m = new nc_model();
   m->cfg = *cfg;
+  m->adt = act_type(*cfg);
+  m->cfg.act_dtype = m->adt;
   cudaGetDevice(&m->device);
   m->wte = w->wte;
   m->lm_head = w->lm_head;
@@ -210,14 +275,14 @@ nc_status nc_model_create(const nc_config* cfg, const nc_weights* w, nc_model** 
   }
 
   // workspace
-  const size_t es = dtype_size(cfg->dtype);
+  const size_t es = dtype_size(m->adt);
   const size_t Mmax = (size_t)cfg->max_batch * cfg->max_seq;
   const size_t d = cfg->d_model, qd = (size_t)cfg->n_head * cfg->head_dim, F = cfg->d_mlp;
   const size_t nqkv = (size_t)(cfg->n_head + 2 * cfg->n_kv_head) * cfg->head_dim;
   const size_t widest = std::max(std::max(nqkv, F), d);
   // fp32 path keeps every projection output in `part`; the bf16 path uses it
   // for split-K partials of the batch rows only.
-  size_t part_elems = cfg->dtype == NC_F32 ? Mmax * widest
+  size_t part_elems = m->adt == NC_F32 ? Mmax * widest
                                            : (size_t)nc::kMaxSplits * nc::kSwapMaxRows * widest;
   m->part_elems = part_elems;
   m->attn_scratch_bytes =
@@ -257,10 +322,43 @@ nc_status nc_model_create(const nc_config* cfg, const nc_weights* w, nc_model** 
   m->gen_dev = reinterpret_cast<int32_t*>(base + o_gen);
   m->attn_scratch = reinterpret_cast<float*>(base + o_as);
 
-  if (cfg->dtype == NC_BF16) {
-    st = nc::tc_create(m->cfg, m->wte, m->lm_head, m->wq.data(), m->wk.data(), m->wv.data(),
-                       m->wo.data(), m->w_fc.data(), m->w_proj.data(), m->xn, m->att, m->h,
-                       m->xnl, Mmax, m->status, &m->tc);
+  if (m->adt != NC_F32) {
+    if (m->adt != cfg->dtype) {
+      // working copies of the projection / LM-head weights in the activation format
+      const size_t kvd = (size_t)cfg->n_kv_head * cfg->head_dim;
+      const size_t sizes[6] = {qd * d, kvd * d, kvd * d, d * qd, F * d, d * F};
+      size_t bytes = round_up((size_t)cfg->vocab * d * 2, 256);
+      for (int l = 0; l < L; ++l)
+        for (size_t z : sizes) bytes += round_up(z * 2, 256);
+      if (cudaMalloc(&m->wcopy, bytes) != cudaSuccess) {
+        m->wcopy = nullptr;
+        cudaGetLastError();
+        set_err("weight copy allocation of %zu bytes failed", bytes);
+        return fail(NC_ERR_OOM);
+      }
+      char* wp = static_cast<char*>(m->wcopy);
+      auto conv = [&](const void*& ptr, size_t n) {
+        nc::launch_convert16(ptr, cfg->dtype, wp, m->adt, (int64_t)n, 0);
+        ptr = wp;
+        wp += round_up(n * 2, 256);
+      };
+      for (int l = 0; l < L; ++l) {
+        conv(m->wq[l], sizes[0]);
+        conv(m->wk[l], sizes[1]);
+        conv(m->wv[l], sizes[2]);
+        conv(m->wo[l], sizes[3]);
+        conv(m->w_fc[l], sizes[4]);
+        conv(m->w_proj[l], sizes[5]);
+      }
+      conv(m->lm_head, (size_t)cfg->vocab * d);
+      if (cudaDeviceSynchronize() != cudaSuccess) {
+        set_err("weight conversion failed");
+        return fail(NC_ERR_CUDA);
+      }
+    }
+    st = nc::tc_create(m->cfg, m->lm_head, m->wq.data(), m->wk.data(), m->wv.data(), m->wo.data(),
+                       m->w_fc.data(), m->w_proj.data(), m->xn, m->att, m->h, m->xnl, Mmax,
+                       m->status, &m->tc);
     if (st != NC_OK) return fail(st);
   }
   *out = m;
@@ -270,7 +368,7 @@ nc_status nc_model_create(const nc_config* cfg, const nc_weights* w, nc_model** 
 size_t nc_kv_cache_bytes(const nc_config* cfg, int32_t batch, int32_t t_max) {
   if (!cfg || batch <= 0 || t_max <= 0) return 0;
   const size_t per = (size_t)cfg->n_layer * batch * cfg->n_kv_head * t_max * cfg->head_dim *
-                     dtype_size(cfg->dtype);
+                     dtype_size(act_type(*cfg));
   return 256 + 2 * round_up(per, 256);
 }
 
@@ -300,8 +398,7 @@ nc_status nc_kv_cache_alloc(const nc_model* m, int32_t batch, int32_t t_max, voi
   } else {
     c->mem = mem;
   }
-  const size_t per = round_up((size_t)m->cfg.n_layer * c->layer_elems * dtype_size(m->cfg.dtype),
-                              256);
+  const size_t per = round_up((size_t)m->cfg.n_layer * c->layer_elems * dtype_size(m->adt), 256);
   c->k = static_cast<char*>(c->mem) + 256;
   c->v = static_cast<char*>(c->mem) + 256 + per;
   *out = c;
@@ -344,18 +441,20 @@ void* layer_ptr(void* base, size_t layer_elems, int l, nc_dtype dt) {
 nc_status run_blocks(nc_model* m, nc_kv_cache* c, int B, int rows_per_seq, int pos0,
                      cudaStream_t s) {
   const nc_config& cfg = m->cfg;
-  const nc_dtype dt = cfg.dtype;
+  const nc_dtype dt = m->adt;
   const int64_t M = (int64_t)B * rows_per_seq;
   const int H = cfg.n_head, Hkv = cfg.n_kv_head, hd = cfg.head_dim, d = cfg.d_model,
             F = cfg.d_mlp;
   const int nqkv = (H + 2 * Hkv) * hd;
   const bool decode = rows_per_seq == 1 && pos0 > 0;
-  const bool tc = dt == NC_BF16;
+  const bool tc = dt != NC_F32;
   RowMap rm{rows_per_seq, pos0};
   for (int l = 0; l < cfg.n_layer; ++l) {
     QkvDst dst{m->q, layer_ptr(c->k, c->layer_elems, l, dt), layer_ptr(c->v, c->layer_elems, l, dt),
                H, Hkv, hd, c->t_max, m->cos_tab, m->sin_tab, cfg.rms_eps};
     // Q/K/V projections + RoPE + QK norm + cache write
+    {
+    ProfScope ps(m, NC_K_QKV, s);
     if (tc) {
       nc_status st = nc::tc_qkv(m->tc, l, M, rm, dst, m->part, s);
       if (st != NC_OK) return st;
@@ -367,28 +466,50 @@ nc_status run_blocks(nc_model* m, nc_kv_cache* c, int B, int rows_per_seq, int p
                            dt, s);
       nc::launch_qkv_post(m->part, 1, M, rm, dst, dt, s);
     }
+    }
     // causal attention
+    {
+    ProfScope ps(m, decode ? NC_K_ATTN_DECODE : NC_K_ATTN_PREFILL, s);
     if (decode) {
       const int len = pos0 + 1;
       const int ns = nc::decode_attention_splits(len);
       nc::launch_attention_decode_simt(m->q, dst.k_cache, dst.v_cache, m->att, B, H, Hkv, len,
                                        c->t_max, hd, dt, m->attn_scratch, ns, s);
     } else if (tc) {
-      nc_status st = nc::tc_attention_prefill(m->tc, m->q, dst.k_cache, dst.v_cache, m->att, B, H,
-                                              Hkv, rows_per_seq, c->t_max, s);
+      nc_status st = nc::tc_attention_prefill(m->q, dst.k_cache, dst.v_cache, m->att, B, H, Hkv,
+                                              rows_per_seq, c->t_max, dt, s);
       if (st != NC_OK) return st;
     } else {
       nc::launch_attention_prefill_simt(m->q, dst.k_cache, dst.v_cache, m->att, B, H, Hkv,
                                         rows_per_seq, c->t_max, hd, dt, s);
     }
+    }
     // output projection + residual, then the pre-MLP RMSNorm
     if (tc) {
-      nc_status st = nc::tc_out_proj(m->tc, l, M, m->x, m->part, s);
+      nc_status st;
+      {
+        ProfScope ps(m, NC_K_OPROJ, s);
+        st = nc::tc_out_proj(m->tc, l, M, m->x, m->part, s);
+      }
       if (st != NC_OK) return st;
-      nc::launch_rmsnorm(m->x, m->xn, dt, M, d, cfg.rms_eps, s);
-      st = nc::tc_mlp(m->tc, l, M, m->x, m->part, s);
+      {
+        ProfScope ps(m, NC_K_NORM, s);
+        nc::launch_rmsnorm(m->x, m->xn, dt, M, d, cfg.rms_eps, s);
+      }
+      {
+        ProfScope ps(m, NC_K_FC, s);
+        st = nc::tc_fc(m->tc, l, M, m->part, s);
+      }
       if (st != NC_OK) return st;
-      nc::launch_rmsnorm(m->x, m->xn, dt, M, d, cfg.rms_eps, s);
+      {
+        ProfScope ps(m, NC_K_PROJ, s);
+        st = nc::tc_proj(m->tc, l, M, m->x, m->part, s);
+      }
+      if (st != NC_OK) return st;
+      {
+        ProfScope ps(m, NC_K_NORM, s);
+        nc::launch_rmsnorm(m->x, m->xn, dt, M, d, cfg.rms_eps, s);
+      }
     } else {
       nc::launch_gemm_simt(m->att, m->wo[l], m->part, M, d, H * hd, d, dt, s);
       nc::launch_residual_finish(m->part, 1, m->x, M, d, m->xn, dt, cfg.rms_eps, s);
@@ -403,9 +524,10 @@ nc_status run_blocks(nc_model* m, nc_kv_cache* c, int B, int rows_per_seq, int p
 
 // logits[M, V] = xn[M, d] lm_head^T
 nc_status run_lm_head(nc_model* m, const void* xn, int64_t M, float* logits, cudaStream_t s) {
-  if (m->cfg.dtype == NC_BF16) return nc::tc_lm_head(m->tc, xn, M, logits, m->part, s);
+  ProfScope ps(m, NC_K_LM_HEAD, s);
+  if (m->adt != NC_F32) return nc::tc_lm_head(m->tc, xn, M, logits, m->part, s);
   nc::launch_gemm_simt(xn, m->lm_head, logits, M, m->cfg.vocab, m->cfg.d_model, m->cfg.vocab,
-                       m->cfg.dtype, s);
+                       NC_F32, s);
   return check_launch();
 }
 
@@ -425,8 +547,11 @@ nc_status check_prefill_args(nc_model* m, const int32_t* tokens, int32_t B, int3
 nc_status prefill_common(nc_model* m, const int32_t* tokens, int32_t B, int32_t T,
                          nc_kv_cache* c, cudaStream_t s) {
   const int64_t M = (int64_t)B * T;
-  nc::launch_embed_norm(tokens, m->wte, m->cfg.dtype, m->x, m->xn, M, m->cfg.d_model,
-                        m->cfg.vocab, m->cfg.rms_eps, m->status, s);
+  {
+    ProfScope ps(m, NC_K_EMBED, s);
+    nc::launch_embed_norm(tokens, m->wte, m->cfg.dtype, m->x, m->xn, m->adt, M, m->cfg.d_model,
+                          m->cfg.vocab, m->cfg.rms_eps, m->status, s);
+  }
   nc_status st = run_blocks(m, c, B, T, 0, s);
   if (st != NC_OK) return st;
   c->len = T;
@@ -456,12 +581,18 @@ nc_status nc_prefill_last(nc_model* m, const int32_t* tokens, int32_t B, int32_t
   cudaStream_t s = static_cast<cudaStream_t>(stream);
   st = prefill_common(m, tokens, B, T, c, s);
   if (st != NC_OK) return st;
-  nc::launch_gather_rows(m->x, m->xl, B, T, m->cfg.d_model, s);
-  nc::launch_rmsnorm(m->xl, m->xnl, m->cfg.dtype, B, m->cfg.d_model, m->cfg.rms_eps, s);
+  {
+    ProfScope ps(m, NC_K_NORM, s);
+    nc::launch_gather_rows(m->x, m->xl, B, T, m->cfg.d_model, s);
+    nc::launch_rmsnorm(m->xl, m->xnl, m->adt, B, m->cfg.d_model, m->cfg.rms_eps, s);
+  }
   float* lg = logits_last ? logits_last : m->logits_tmp;
   st = run_lm_head(m, m->xnl, B, lg, s);
   if (st != NC_OK) return st;
-  if (argmax_out) nc::launch_argmax(lg, B, m->cfg.vocab, argmax_out, s);
+  if (argmax_out) {
+    ProfScope ps(m, NC_K_ARGMAX, s);
+    nc::launch_argmax(lg, B, m->cfg.vocab, argmax_out, s);
+  }
   return check_launch();
 }
 
@@ -478,14 +609,20 @@ nc_status nc_decode_step(nc_model* m, const int32_t* tokens, int32_t B, int32_t 
   NC_CHECK(pos >= 1, NC_ERR_INVALID_ARG, "decode needs a prefilled cache (pos >= 1)");
   NC_CHECK(pos + 1 <= c->t_max, NC_ERR_INVALID_ARG, "cache full (t_max %d)", c->t_max);
   cudaStream_t s = static_cast<cudaStream_t>(stream);
-  nc::launch_embed_norm(tokens, m->wte, m->cfg.dtype, m->x, m->xn, B, m->cfg.d_model,
-                        m->cfg.vocab, m->cfg.rms_eps, m->status, s);
+  {
+    ProfScope ps(m, NC_K_EMBED, s);
+    nc::launch_embed_norm(tokens, m->wte, m->cfg.dtype, m->x, m->xn, m->adt, B, m->cfg.d_model,
+                          m->cfg.vocab, m->cfg.rms_eps, m->status, s);
+  }
   nc_status st = run_blocks(m, c, B, 1, pos, s);
   if (st != NC_OK) return st;
   float* lg = logits ? logits : m->logits_tmp;
   st = run_lm_head(m, m->xn, B, lg, s);
   if (st != NC_OK) return st;
-  if (argmax_out) nc::launch_argmax(lg, B, m->cfg.vocab, argmax_out, s);
+  if (argmax_out) {
+    ProfScope ps(m, NC_K_ARGMAX, s);
+    nc::launch_argmax(lg, B, m->cfg.vocab, argmax_out, s);
+  }
   st = check_launch();
   if (st == NC_OK) c->len = pos + 1;
   return st;
@@ -514,6 +651,38 @@ nc_status nc_generate_host(nc_model* m, const int32_t* prompt, int32_t B, int32_
   return NC_OK;
 }
 
+nc_status nc_kv_cache_set_length(nc_kv_cache* c, int32_t len) {
+  NC_CHECK(c, NC_ERR_INVALID_ARG, "cache is NULL");
+  NC_CHECK(len >= 0 && len <= c->len, NC_ERR_INVALID_ARG, "length %d outside [0, %d]", len, c->len);
+  c->len = len;
+  return NC_OK;
+}
+
+nc_status nc_profile_begin(nc_model* m) {
+  NC_CHECK(m, NC_ERR_INVALID_ARG, "model is NULL");
+  m->prof = true;
+  return NC_OK;
+}
+
+nc_status nc_profile_end(nc_model* m, void* stream, nc_kernel_time* out) {
+  NC_CHECK(m && out, NC_ERR_INVALID_ARG, "NULL argument");
+  NC_CUDA(cudaStreamSynchronize(static_cast<cudaStream_t>(stream)));
+  for (int k = 0; k < NC_K_COUNT; ++k) out[k] = nc_kernel_time{0.0, 0};
+  for (auto& r : m->recs) {
+    float ms = 0.f;
+    cudaEventElapsedTime(&ms, r.a, r.b);
+    out[r.kind].ms += ms;
+    out[r.kind].launches += r.launches;
+    m->event_pool.push_back(r.a);
+    m->event_pool.push_back(r.b);
+  }
+  m->recs.clear();
+  m->prof = false;
+  return NC_OK;
+}
+
+int64_t nc_launch_count(void) { return g_launches.load(); }
+
 nc_status nc_model_check(nc_model* m, void* stream) {
   NC_CHECK(m, NC_ERR_INVALID_ARG, "model is NULL");
   cudaStream_t s = static_cast<cudaStream_t>(stream);
@@ -537,7 +706,8 @@ nc_status nc_op_rmsnorm(const float* x, void* y, nc_dtype y_dtype, int64_t M, in
                         float eps, void* stream) {
   NC_CHECK(x && y && aligned16(x) && aligned16(y), NC_ERR_INVALID_ARG, "NULL/misaligned");
   NC_CHECK(M >= 0 && d > 0 && d % 4 == 0, NC_ERR_INVALID_ARG, "d must be a positive multiple of 4");
-  NC_CHECK(y_dtype == NC_F32 || y_dtype == NC_BF16, NC_ERR_INVALID_ARG, "bad dtype");
+  NC_CHECK(y_dtype == NC_F32 || y_dtype == NC_BF16 || y_dtype == NC_F16, NC_ERR_INVALID_ARG,
+           "bad dtype");
   if (M == 0) return NC_OK;
   nc::launch_rmsnorm(x, y, y_dtype, M, d, eps, static_cast<cudaStream_t>(stream));
   return check_launch();
@@ -550,9 +720,9 @@ nc_status nc_op_gemm(const void* A, const void* B, float* C, int32_t M, int32_t 
   NC_CHECK(M >= 0 && N > 0 && K > 0, NC_ERR_INVALID_ARG, "bad sizes");
   if (M == 0) return NC_OK;
   cudaStream_t s = static_cast<cudaStream_t>(stream);
-  if (dtype == NC_BF16) {
-    NC_CHECK(K % 64 == 0 && N % 16 == 0, NC_ERR_UNSUPPORTED, "bf16 GEMM needs K%%64==0, N%%16==0");
-    return nc::tc_gemm_f32out(A, B, C, M, N, K, s);
+  if (dtype == NC_BF16 || dtype == NC_F16) {
+    NC_CHECK(K % 64 == 0 && N % 16 == 0, NC_ERR_UNSUPPORTED, "16-bit GEMM needs K%%64==0, N%%16==0");
+    return nc::tc_gemm_f32out(A, B, C, M, N, K, dtype, s);
   }
   NC_CHECK(dtype == NC_F32, NC_ERR_INVALID_ARG, "bad dtype");
   nc::launch_gemm_simt(A, B, C, M, N, K, N, dtype, s);
@@ -568,10 +738,11 @@ nc_status nc_op_attention_prefill(const void* q, const void* k, const void* v, v
                hd % 2 == 0 && hd <= 128,
            NC_ERR_INVALID_ARG, "bad sizes");
   cudaStream_t s = static_cast<cudaStream_t>(stream);
-  if (dtype == NC_BF16) {
-    NC_CHECK(hd == 128, NC_ERR_UNSUPPORTED, "bf16 attention needs head_dim 128");
-    return nc::tc_attention_prefill(nullptr, q, k, v, o, B, H, Hkv, T, t_max, s);
+  if (dtype == NC_BF16 || dtype == NC_F16) {
+    NC_CHECK(hd == 128, NC_ERR_UNSUPPORTED, "16-bit attention needs head_dim 128");
+    return nc::tc_attention_prefill(q, k, v, o, B, H, Hkv, T, t_max, dtype, s);
   }
+  NC_CHECK(dtype == NC_F32, NC_ERR_INVALID_ARG, "bad dtype");
   nc::launch_attention_prefill_simt(q, k, v, o, B, H, Hkv, T, t_max, hd, dtype, s);
   return check_launch();
 }
@@ -590,7 +761,7 @@ nc_status nc_op_attention_decode(const void* q, const void* k, const void* v, vo
   NC_CHECK(B > 0 && H > 0 && Hkv > 0 && H % Hkv == 0 && len > 0 && len <= t_max && hd > 0 &&
                hd % 2 == 0 && hd <= 128,
            NC_ERR_INVALID_ARG, "bad sizes");
-  NC_CHECK(dtype == NC_F32 || dtype == NC_BF16, NC_ERR_INVALID_ARG, "bad dtype");
+  NC_CHECK(dtype == NC_F32 || dtype == NC_BF16 || dtype == NC_F16, NC_ERR_INVALID_ARG, "bad dtype");
   const int ns = nc::decode_attention_splits(len);
   NC_CHECK(scratch_bytes >= (size_t)B * H * ns * (hd + 2) * sizeof(float), NC_ERR_INVALID_ARG,
            "scratch too small");

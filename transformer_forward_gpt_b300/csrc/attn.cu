@@ -49,10 +49,23 @@ __device__ __forceinline__ void ldsm_x4_t(uint32_t addr, uint32_t& r0, uint32_t&
                : "=r"(r0), "=r"(r1), "=r"(r2), "=r"(r3)
                : "r"(addr));
 }
+template <class T16>
 __device__ __forceinline__ void mma16816(float (&c)[4], uint32_t a0, uint32_t a1, uint32_t a2,
-                                         uint32_t a3, uint32_t b0, uint32_t b1) {
+                                         uint32_t a3, uint32_t b0, uint32_t b1);
+template <>
+__device__ __forceinline__ void mma16816<bf16>(float (&c)[4], uint32_t a0, uint32_t a1,
+                                               uint32_t a2, uint32_t a3, uint32_t b0, uint32_t b1) {
   asm volatile(
       "mma.sync.aligned.m16n8k16.row.col.f32.bf16.bf16.f32 {%0,%1,%2,%3}, {%4,%5,%6,%7}, "
+      "{%8,%9}, {%0,%1,%2,%3};"
+      : "+f"(c[0]), "+f"(c[1]), "+f"(c[2]), "+f"(c[3])
+      : "r"(a0), "r"(a1), "r"(a2), "r"(a3), "r"(b0), "r"(b1));
+}
+template <>
+__device__ __forceinline__ void mma16816<f16>(float (&c)[4], uint32_t a0, uint32_t a1,
+                                              uint32_t a2, uint32_t a3, uint32_t b0, uint32_t b1) {
+  asm volatile(
+      "mma.sync.aligned.m16n8k16.row.col.f32.f16.f16.f32 {%0,%1,%2,%3}, {%4,%5,%6,%7}, "
       "{%8,%9}, {%0,%1,%2,%3};"
       : "+f"(c[0]), "+f"(c[1]), "+f"(c[2]), "+f"(c[3])
       : "r"(a0), "r"(a1), "r"(a2), "r"(a3), "r"(b0), "r"(b1));
@@ -60,19 +73,21 @@ __device__ __forceinline__ void mma16816(float (&c)[4], uint32_t a0, uint32_t a1
 
 // Loads rows [row0, row0 + 64) of a [rows, 128] bf16 matrix into a swizzled
 // tile; rows >= row_limit are zero-filled.
-__device__ __forceinline__ void load_tile(uint32_t dst, const bf16* src, int row0, int row_limit) {
+template <class T16>
+__device__ __forceinline__ void load_tile(uint32_t dst, const T16* src, int row0, int row_limit) {
   for (int i = threadIdx.x; i < kBk * 16; i += 128) {
     const int r = i / 16, c = i % 16;
     const bool ok = row0 + r < row_limit;
-    const bf16* p = src + (int64_t)(ok ? row0 + r : 0) * kHd + c * 8;
+    const T16* p = src + (int64_t)(ok ? row0 + r : 0) * kHd + c * 8;
     cp_async16(dst + swz(r, c), p, ok);
   }
 }
 
-__global__ void __launch_bounds__(128) attn_prefill_mma_kernel(const bf16* __restrict__ q,
-                                                               const bf16* __restrict__ k,
-                                                               const bf16* __restrict__ v,
-                                                               bf16* __restrict__ o, int H, int Hkv,
+template <class T16>
+__global__ void __launch_bounds__(128) attn_prefill_mma_kernel(const T16* __restrict__ q,
+                                                               const T16* __restrict__ k,
+                                                               const T16* __restrict__ v,
+                                                               T16* __restrict__ o, int H, int Hkv,
                                                                int T, int t_max, float scale_log2) {
   extern __shared__ __align__(128) uint8_t smem[];
   const uint32_t sQ = smem_u32(smem);
@@ -84,9 +99,9 @@ __global__ void __launch_bounds__(128) attn_prefill_mma_kernel(const bf16* __res
   const int g = h / (H / Hkv);
   const int q0 = qt * kBq;
   const int warp = threadIdx.x / 32, lane = threadIdx.x % 32;
-  const bf16* qb = q + ((int64_t)b * H + h) * T * kHd;
-  const bf16* kb = k + ((int64_t)b * Hkv + g) * t_max * kHd;
-  const bf16* vb = v + ((int64_t)b * Hkv + g) * t_max * kHd;
+  const T16* qb = q + ((int64_t)b * H + h) * T * kHd;
+  const T16* kb = k + ((int64_t)b * Hkv + g) * t_max * kHd;
+  const T16* vb = v + ((int64_t)b * Hkv + g) * t_max * kHd;
 
   const int n_kv = qt + 1;   // causal: key tiles 0..qt
   load_tile(sQ, qb, q0, T);
@@ -135,8 +150,8 @@ __global__ void __launch_bounds__(128) attn_prefill_mma_kernel(const bf16* __res
         const int c = ks * 2 + (lane / 8) % 2;
         uint32_t b0, b1, b2, b3;
         ldsm_x4(sK + swz(r, c), b0, b1, b2, b3);
-        mma16816(s[2 * np], qf[ks][0], qf[ks][1], qf[ks][2], qf[ks][3], b0, b1);
-        mma16816(s[2 * np + 1], qf[ks][0], qf[ks][1], qf[ks][2], qf[ks][3], b2, b3);
+        mma16816<T16>(s[2 * np], qf[ks][0], qf[ks][1], qf[ks][2], qf[ks][3], b0, b1);
+        mma16816<T16>(s[2 * np + 1], qf[ks][0], qf[ks][1], qf[ks][2], qf[ks][3], b2, b3);
       }
     }
     // causal mask on the diagonal tile
@@ -174,8 +189,8 @@ __global__ void __launch_bounds__(128) attn_prefill_mma_kernel(const bf16* __res
       const float p3 = exp2f((s[n][3] - mx[1]) * scale_log2);
       rs[0] += p0 + p1;
       rs[1] += p2 + p3;
-      pf[n][0] = pack_bf16x2(p0, p1);
-      pf[n][1] = pack_bf16x2(p2, p3);
+      pf[n][0] = pack2<T16>(p0, p1);
+      pf[n][1] = pack2<T16>(p2, p3);
     }
 #pragma unroll
     for (int r = 0; r < 2; ++r) {
@@ -202,8 +217,8 @@ __global__ void __launch_bounds__(128) attn_prefill_mma_kernel(const bf16* __res
         const int c = dp * 2 + lane / 16;
         uint32_t b0, b1, b2, b3;
         ldsm_x4_t(sV + swz(r, c), b0, b1, b2, b3);
-        mma16816(oacc[2 * dp], a0, a1, a2, a3, b0, b1);
-        mma16816(oacc[2 * dp + 1], a0, a1, a2, a3, b2, b3);
+        mma16816<T16>(oacc[2 * dp], a0, a1, a2, a3, b0, b1);
+        mma16816<T16>(oacc[2 * dp + 1], a0, a1, a2, a3, b2, b3);
       }
     }
     __syncthreads();
@@ -214,34 +229,42 @@ __global__ void __launch_bounds__(128) attn_prefill_mma_kernel(const bf16* __res
   for (int r = 0; r < 2; ++r) {
     const int t = q0 + warp * 16 + gq + r * 8;
     if (t >= T) continue;
-    bf16* out = o + ((int64_t)b * T + t) * H * kHd + (int64_t)h * kHd;
+    T16* out = o + ((int64_t)b * T + t) * H * kHd + (int64_t)h * kHd;
 #pragma unroll
     for (int i = 0; i < 16; ++i) {
       const int dim = i * 8 + 2 * tq;
       *reinterpret_cast<uint32_t*>(out + dim) =
-          pack_bf16x2(oacc[i][2 * r] * inv[r], oacc[i][2 * r + 1] * inv[r]);
+          pack2<T16>(oacc[i][2 * r] * inv[r], oacc[i][2 * r + 1] * inv[r]);
     }
   }
 }
 
-}  // namespace
-
-nc_status tc_attention_prefill(TcModel* t, const void* q, const void* k, const void* v, void* o,
-                               int B, int H, int Hkv, int T, int t_max, cudaStream_t s) {
-  (void)t;
+template <class T16>
+nc_status launch_attn(const void* q, const void* k, const void* v, void* o, int B, int H, int Hkv,
+                      int T, int t_max, cudaStream_t s) {
   const size_t smem = 5 * kTileBytes;
   static bool configured = false;
   if (!configured) {
-    if (cudaFuncSetAttribute(attn_prefill_mma_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize,
-                             (int)smem) != cudaSuccess)
+    if (cudaFuncSetAttribute(attn_prefill_mma_kernel<T16>,
+                             cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem) != cudaSuccess)
       return NC_ERR_CUDA;
     configured = true;
   }
   dim3 grid((T + kBq - 1) / kBq, B * H);
   const float scale_log2 = 1.4426950408889634f / sqrtf((float)kHd);
-  attn_prefill_mma_kernel<<<grid, 128, smem, s>>>((const bf16*)q, (const bf16*)k, (const bf16*)v,
-                                                  (bf16*)o, H, Hkv, T, t_max, scale_log2);
+  attn_prefill_mma_kernel<T16><<<grid, 128, smem, s>>>((const T16*)q, (const T16*)k,
+                                                       (const T16*)v, (T16*)o, H, Hkv, T, t_max,
+                                                       scale_log2);
+  count_launches(1);
   return cudaGetLastError() == cudaSuccess ? NC_OK : NC_ERR_CUDA;
+}
+
+}  // namespace
+
+nc_status tc_attention_prefill(const void* q, const void* k, const void* v, void* o, int B, int H,
+                               int Hkv, int T, int t_max, nc_dtype dt, cudaStream_t s) {
+  if (dt == NC_F16) return launch_attn<f16>(q, k, v, o, B, H, Hkv, T, t_max, s);
+  return launch_attn<bf16>(q, k, v, o, B, H, Hkv, T, t_max, s);
 }
 
 }  // namespace nc

@@ -8,6 +8,9 @@
 
 namespace nc {
 
+// Process-wide count of kernel launches made by the library (measurement only).
+void count_launches(int n);
+
 // Where the rows of a projection output go (prefill: rows = B*T tokens of B
 // sequences starting at position pos0 = 0; decode: rows = B, one per sequence, at
 // position pos0 = pos).
@@ -28,8 +31,9 @@ struct QkvDst {
 };
 
 // ---- CUDA-core kernels (simt.cu)
-void launch_embed_norm(const int32_t* tok, const void* wte, nc_dtype dt, float* x, void* xn,
-                       int64_t M, int d, int vocab, float eps, uint32_t* status, cudaStream_t s);
+void launch_embed_norm(const int32_t* tok, const void* wte, nc_dtype wdt, float* x, void* xn,
+                       nc_dtype adt, int64_t M, int d, int vocab, float eps, uint32_t* status,
+                       cudaStream_t s);
 void launch_rmsnorm(const float* x, void* y, nc_dtype ydt, int64_t M, int d, float eps,
                     cudaStream_t s);
 void launch_gemm_simt(const void* A, const void* B, float* C, int64_t M, int N, int K,
@@ -51,6 +55,9 @@ int decode_attention_splits(int len);
 void launch_attention_decode_simt(const void* q, const void* k, const void* v, void* o, int B,
                                   int H, int Hkv, int len, int t_max, int hd, nc_dtype dt,
                                   float* scratch, int n_split, cudaStream_t s);
+// dst[i] = src[i] converted between number formats (weight copies).
+void launch_convert16(const void* src, nc_dtype from, void* dst, nc_dtype to, int64_t n,
+                      cudaStream_t s);
 void launch_argmax(const float* x, int rows, int n, int32_t* out, cudaStream_t s);
 void launch_gather_rows(const float* x, float* y, int B, int T, int d, cudaStream_t s);
 

@@ -11,29 +11,25 @@
 namespace nc {
 
 // ---------------------------------------------------------------- row helpers
-template <class T> struct Vec4;
+template <class T> struct Vec4 {   // 16-bit types: 8-byte accesses
+  __device__ static float4 load(const T* p) {
+    uint2 u = *reinterpret_cast<const uint2*>(p);
+    float2 fa = unpack2<T>(u.x), fb = unpack2<T>(u.y);
+    return make_float4(fa.x, fa.y, fb.x, fb.y);
+  }
+  __device__ static void store(T* p, float4 v) {
+    *reinterpret_cast<uint2*>(p) = make_uint2(pack2<T>(v.x, v.y), pack2<T>(v.z, v.w));
+  }
+};
 template <> struct Vec4<float> {
   __device__ static float4 load(const float* p) { return *reinterpret_cast<const float4*>(p); }
   __device__ static void store(float* p, float4 v) { *reinterpret_cast<float4*>(p) = v; }
 };
-template <> struct Vec4<bf16> {
-  __device__ static float4 load(const bf16* p) {
-    uint2 u = *reinterpret_cast<const uint2*>(p);
-    __nv_bfloat162 a = *reinterpret_cast<__nv_bfloat162*>(&u.x);
-    __nv_bfloat162 b = *reinterpret_cast<__nv_bfloat162*>(&u.y);
-    float2 fa = __bfloat1622float2(a), fb = __bfloat1622float2(b);
-    return make_float4(fa.x, fa.y, fb.x, fb.y);
-  }
-  __device__ static void store(bf16* p, float4 v) {
-    uint2 u = make_uint2(pack_bf16x2(v.x, v.y), pack_bf16x2(v.z, v.w));
-    *reinterpret_cast<uint2*>(p) = u;
-  }
-};
 
 // Embedding row gather (RMSNorm of the block-1 input fused in): one warp per
 // token row. x = wte[tok] in fp32; xn = x / sqrt(mean x^2 + eps) in T.
-template <class T>
-__global__ void embed_norm_kernel(const int32_t* __restrict__ tok, const T* __restrict__ wte,
+template <class TW, class T>
+__global__ void embed_norm_kernel(const int32_t* __restrict__ tok, const TW* __restrict__ wte,
                                   float* __restrict__ x, T* __restrict__ xn, int64_t M, int d,
                                   int vocab, float eps, uint32_t* status) {
   const int64_t row = (int64_t)blockIdx.x * (blockDim.x / 32) + threadIdx.x / 32;
@@ -44,11 +40,11 @@ __global__ void embed_norm_kernel(const int32_t* __restrict__ tok, const T* __re
     if (lane == 0) atomicOr(status, ST_BAD_TOKEN);
     id = 0;
   }
-  const T* src = wte + (int64_t)id * d;
+  const TW* src = wte + (int64_t)id * d;
   float* xr = x + row * d;
   float ss = 0.f;
   for (int j = lane * 4; j < d; j += 128) {
-    float4 v = Vec4<T>::load(src + j);
+    float4 v = Vec4<TW>::load(src + j);
     Vec4<float>::store(xr + j, v);
     ss += v.x * v.x + v.y * v.y + v.z * v.z + v.w * v.w;
   }
@@ -437,81 +433,80 @@ static inline unsigned grid_rows(int64_t rows, int per_block) {
   return (unsigned)((rows + per_block - 1) / per_block);
 }
 
-void launch_embed_norm(const int32_t* tok, const void* wte, nc_dtype dt, float* x, void* xn,
-                       int64_t M, int d, int vocab, float eps, uint32_t* status, cudaStream_t s) {
-  if (dt == NC_BF16)
-    embed_norm_kernel<bf16><<<grid_rows(M, 8), 256, 0, s>>>(
-        tok, (const bf16*)wte, x, (bf16*)xn, M, d, vocab, eps, status);
-  else
-    embed_norm_kernel<float><<<grid_rows(M, 8), 256, 0, s>>>(
-        tok, (const float*)wte, x, (float*)xn, M, d, vocab, eps, status);
+// Calls F<T>() with T the C++ type of an nc_dtype.
+#define NC_DISPATCH(dt, T, ...)            \
+  do {                                     \
+    if ((dt) == NC_BF16) {                 \
+      typedef bf16 T;                      \
+      __VA_ARGS__;                         \
+    } else if ((dt) == NC_F16) {           \
+      typedef f16 T;                       \
+      __VA_ARGS__;                         \
+    } else {                               \
+      typedef float T;                     \
+      __VA_ARGS__;                         \
+    }                                      \
+  } while (0)
+
+void launch_embed_norm(const int32_t* tok, const void* wte, nc_dtype wdt, float* x, void* xn,
+                       nc_dtype adt, int64_t M, int d, int vocab, float eps, uint32_t* status,
+                       cudaStream_t s) {
+  count_launches(1);
+  NC_DISPATCH(wdt, TW, NC_DISPATCH(adt, TA, (embed_norm_kernel<TW, TA><<<grid_rows(M, 8), 256, 0, s>>>(
+                                              tok, (const TW*)wte, x, (TA*)xn, M, d, vocab, eps, status))));
 }
 
 void launch_rmsnorm(const float* x, void* y, nc_dtype ydt, int64_t M, int d, float eps,
                     cudaStream_t s) {
-  if (ydt == NC_BF16)
-    rmsnorm_kernel<bf16><<<grid_rows(M, 8), 256, 0, s>>>(x, (bf16*)y, M, d, eps);
-  else
-    rmsnorm_kernel<float><<<grid_rows(M, 8), 256, 0, s>>>(x, (float*)y, M, d, eps);
+  count_launches(1);
+  NC_DISPATCH(ydt, T, (rmsnorm_kernel<T><<<grid_rows(M, 8), 256, 0, s>>>(x, (T*)y, M, d, eps)));
 }
 
 void launch_gemm_simt(const void* A, const void* B, float* C, int64_t M, int N, int K,
                       int64_t ldc, nc_dtype dt, cudaStream_t s) {
+  count_launches(1);
   dim3 grid((N + 63) / 64, (unsigned)((M + 63) / 64));
-  if (dt == NC_BF16)
-    gemm_simt_kernel<bf16><<<grid, 256, 0, s>>>((const bf16*)A, (const bf16*)B, C, M, N, K, ldc);
-  else
-    gemm_simt_kernel<float><<<grid, 256, 0, s>>>((const float*)A, (const float*)B, C, M, N, K,
-                                                 ldc);
+  NC_DISPATCH(dt, T, (gemm_simt_kernel<T><<<grid, 256, 0, s>>>((const T*)A, (const T*)B, C, M, N, K, ldc)));
 }
 
 void launch_qkv_post(const float* part, int n_split, int64_t M, const RowMap& rm,
                      const QkvDst& dst, nc_dtype dt, cudaStream_t s) {
+  count_launches(1);
   const int64_t warps = M * (dst.H + 2 * dst.Hkv);
-  if (dt == NC_BF16)
-    qkv_post_kernel<bf16><<<grid_rows(warps, 8), 256, 0, s>>>(part, n_split, M, rm, dst);
-  else
-    qkv_post_kernel<float><<<grid_rows(warps, 8), 256, 0, s>>>(part, n_split, M, rm, dst);
+  NC_DISPATCH(dt, T, (qkv_post_kernel<T><<<grid_rows(warps, 8), 256, 0, s>>>(part, n_split, M, rm, dst)));
 }
 
 void launch_residual_finish(const float* part, int n_split, float* x, int64_t M, int N,
                             void* xn_out, nc_dtype dt, float eps, cudaStream_t s) {
-  if (dt == NC_BF16)
-    residual_finish_kernel<bf16><<<grid_rows(M, 8), 256, 0, s>>>(part, n_split, x, M, N,
-                                                                 (bf16*)xn_out, eps);
-  else
-    residual_finish_kernel<float><<<grid_rows(M, 8), 256, 0, s>>>(part, n_split, x, M, N,
-                                                                  (float*)xn_out, eps);
+  count_launches(1);
+  NC_DISPATCH(dt, T, (residual_finish_kernel<T><<<grid_rows(M, 8), 256, 0, s>>>(part, n_split, x, M, N,
+                                                                             (T*)xn_out, eps)));
 }
 
 void launch_relu2_finish(const float* part, int n_split, void* h, int64_t M, int N, nc_dtype dt,
                          cudaStream_t s) {
+  count_launches(1);
   const int64_t total = M * N;
   const unsigned grid = (unsigned)std::min<int64_t>((total + 255) / 256, 148 * 16);
-  if (dt == NC_BF16)
-    relu2_finish_kernel<bf16><<<grid, 256, 0, s>>>(part, n_split, (bf16*)h, total);
-  else
-    relu2_finish_kernel<float><<<grid, 256, 0, s>>>(part, n_split, (float*)h, total);
+  NC_DISPATCH(dt, T, (relu2_finish_kernel<T><<<grid, 256, 0, s>>>(part, n_split, (T*)h, total)));
 }
 
 void launch_sum_splits(const float* part, int n_split, float* out, int64_t M, int N, int64_t ldo,
                        cudaStream_t s) {
+  count_launches(1);
   const int64_t total = M * N;
   const unsigned grid = (unsigned)std::min<int64_t>((total + 255) / 256, 148 * 16);
   sum_splits_kernel<<<grid, 256, 0, s>>>(part, n_split, out, M, N, ldo);
 }
 
 void launch_attention_prefill_simt(const void* q, const void* k, const void* v, void* o, int B,
-                                   int H, int Hkv, int T, int t_max, int hd, nc_dtype dt,
+                                   int H, int Hkv, int T_, int t_max, int hd, nc_dtype dt,
                                    cudaStream_t s) {
-  const int64_t warps = (int64_t)B * H * T;
+  count_launches(1);
+  const int64_t warps = (int64_t)B * H * T_;
   const size_t smem = 8 * hd * sizeof(float);
-  if (dt == NC_BF16)
-    attention_prefill_simt_kernel<bf16><<<grid_rows(warps, 8), 256, smem, s>>>(
-        (const bf16*)q, (const bf16*)k, (const bf16*)v, (bf16*)o, B, H, Hkv, T, t_max, hd);
-  else
-    attention_prefill_simt_kernel<float><<<grid_rows(warps, 8), 256, smem, s>>>(
-        (const float*)q, (const float*)k, (const float*)v, (float*)o, B, H, Hkv, T, t_max, hd);
+  NC_DISPATCH(dt, T, (attention_prefill_simt_kernel<T><<<grid_rows(warps, 8), 256, smem, s>>>(
+                         (const T*)q, (const T*)k, (const T*)v, (T*)o, B, H, Hkv, T_, t_max, hd)));
 }
 
 int decode_attention_splits(int len) {
@@ -522,27 +517,39 @@ int decode_attention_splits(int len) {
 void launch_attention_decode_simt(const void* q, const void* k, const void* v, void* o, int B,
                                   int H, int Hkv, int len, int t_max, int hd, nc_dtype dt,
                                   float* scratch, int n_split, cudaStream_t s) {
+  count_launches(2);
   dim3 grid(B * H, n_split);
   const size_t smem = hd * sizeof(float);
-  if (dt == NC_BF16) {
-    attention_decode_simt_kernel<bf16><<<grid, 32, smem, s>>>(
-        (const bf16*)q, (const bf16*)k, (const bf16*)v, scratch, B, H, Hkv, len, t_max, hd,
-        n_split);
-    attention_combine_kernel<bf16><<<B * H, 128, 0, s>>>(scratch, (bf16*)o, B * H, hd, n_split);
-  } else {
-    attention_decode_simt_kernel<float><<<grid, 32, smem, s>>>(
-        (const float*)q, (const float*)k, (const float*)v, scratch, B, H, Hkv, len, t_max, hd,
-        n_split);
-    attention_combine_kernel<float><<<B * H, 128, 0, s>>>(scratch, (float*)o, B * H, hd, n_split);
-  }
+  NC_DISPATCH(dt, T, (attention_decode_simt_kernel<T><<<grid, 32, smem, s>>>(
+                          (const T*)q, (const T*)k, (const T*)v, scratch, B, H, Hkv, len, t_max, hd,
+                          n_split),
+                      attention_combine_kernel<T><<<B * H, 128, 0, s>>>(scratch, (T*)o, B * H, hd,
+                                                                        n_split)));
 }
 
 void launch_argmax(const float* x, int rows, int n, int32_t* out, cudaStream_t s) {
+  count_launches(1);
   argmax_kernel<<<rows, 1024, 0, s>>>(x, n, out);
 }
 
 void launch_gather_rows(const float* x, float* y, int B, int T, int d, cudaStream_t s) {
+  count_launches(1);
   gather_last_rows_kernel<<<B, 256, 0, s>>>(x, y, T, d);
+}
+
+template <class TI, class TO>
+__global__ void convert_kernel(const TI* __restrict__ src, TO* __restrict__ dst, int64_t n) {
+  for (int64_t i = (int64_t)blockIdx.x * blockDim.x + threadIdx.x; i < n;
+       i += (int64_t)gridDim.x * blockDim.x)
+    dst[i] = from_f32<TO>(to_f32(src[i]));
+}
+
+void launch_convert16(const void* src, nc_dtype from, void* dst, nc_dtype to, int64_t n,
+                      cudaStream_t s) {
+  count_launches(1);
+  const unsigned grid = (unsigned)std::min<int64_t>((n + 255) / 256, 148 * 32);
+  NC_DISPATCH(from, TI, NC_DISPATCH(to, TO, (convert_kernel<TI, TO><<<grid, 256, 0, s>>>(
+                                                 (const TI*)src, (TO*)dst, n))));
 }
 
 }  // namespace nc

@@ -10,11 +10,11 @@ constexpr int kSwapMaxRows = 128;   // M <= this runs weight-stationary (swap-AB
 
 struct TcModel;
 
-nc_status tc_create(const nc_config& cfg, const void* wte, const void* lm_head,
-                    const void* const* wq, const void* const* wk, const void* const* wv,
-                    const void* const* wo, const void* const* w_fc, const void* const* w_proj,
-                    void* xn, void* att, void* h, void* xnl, size_t max_rows, uint32_t* status,
-                    TcModel** out);
+// Weight pointers are in cfg.act_dtype (the caller converts first if needed).
+nc_status tc_create(const nc_config& cfg, const void* lm_head, const void* const* wq,
+                    const void* const* wk, const void* const* wv, const void* const* wo,
+                    const void* const* w_fc, const void* const* w_proj, void* xn, void* att,
+                    void* h, void* xnl, size_t max_rows, uint32_t* status, TcModel** out);
 void tc_destroy(TcModel* t);
 
 // Q/K/V projections of rows xn[M, d] with RoPE, QK norm and the scatter to q and
@@ -23,16 +23,19 @@ nc_status tc_qkv(TcModel* t, int layer, int64_t M, const RowMap& rm, const QkvDs
                  float* part, cudaStream_t s);
 // x += att W_o^T
 nc_status tc_out_proj(TcModel* t, int layer, int64_t M, float* x, float* part, cudaStream_t s);
-// x += relu(xn W_fc^T)^2 W_proj^T
-nc_status tc_mlp(TcModel* t, int layer, int64_t M, float* x, float* part, cudaStream_t s);
+// h = relu(xn W_fc^T)^2
+nc_status tc_fc(TcModel* t, int layer, int64_t M, float* part, cudaStream_t s);
+// x += h W_proj^T
+nc_status tc_proj(TcModel* t, int layer, int64_t M, float* x, float* part, cudaStream_t s);
 // logits[M, V] = xn lm_head^T (xn is the model's xn or xnl buffer)
 nc_status tc_lm_head(TcModel* t, const void* xn, int64_t M, float* logits, float* part,
                      cudaStream_t s);
-// Causal attention; t may be NULL (single-step entry point).
-nc_status tc_attention_prefill(TcModel* t, const void* q, const void* k, const void* v, void* o,
-                               int B, int H, int Hkv, int T, int t_max, cudaStream_t s);
+// Causal attention over q [B, H, T, 128], cache k/v [B, Hkv, t_max, 128] -> o [B, T, H*128].
+nc_status tc_attention_prefill(const void* q, const void* k, const void* v, void* o, int B, int H,
+                               int Hkv, int T, int t_max, nc_dtype dt, cudaStream_t s);
 // C[M, N] = A[M, K] B[N, K]^T, fp32 out (single-step entry point).
-nc_status tc_gemm_f32out(const void* A, const void* B, float* C, int M, int N, int K,
+nc_status tc_gemm_f32out(const void* A, const void* B, float* C, int M, int N, int K, nc_dtype dt,
                          cudaStream_t s);
+
 
 }  // namespace nc

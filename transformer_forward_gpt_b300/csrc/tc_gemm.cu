@@ -39,7 +39,7 @@ struct GemmArgs {
   int a_split0, a_split1;  // row boundaries between A tensor maps 0 | 1 | 2
   int b_split0, b_split1;  // the same for B (multiples of 128)
   float* out_f32;          // EPI_F32 (C), EPI_RESID (x), EPI_SWAP (partials or logits)
-  bf16* out_bf16;          // EPI_RELU2
+  void* out_16;            // EPI_RELU2 (16-bit type of the kernel)
   int64_t ldo;             // row pitch of the output, elements
   int64_t split_stride;    // EPI_SWAP: elements between split slices
   RowMap rm;               // EPI_QKV
@@ -78,7 +78,7 @@ __device__ __forceinline__ const CUtensorMap* pick_map(const CUtensorMap* m0, co
 // Each thread holds row `row` of the tile; taddr points at its TMEM lane and
 // the accumulator's first column. tcgen05.ld is warp-collective, so every lane
 // runs the loads and only the stores are predicated on the row being valid.
-template <int BN>
+template <int BN, class T16>
 __device__ __forceinline__ void epi_store_rows(const GemmArgs& p, uint32_t taddr, int row, int nb,
                                                int mode) {
   const bool valid = row < p.M;
@@ -108,7 +108,7 @@ __device__ __forceinline__ void epi_store_rows(const GemmArgs& p, uint32_t taddr
           *reinterpret_cast<float4*>(dst + 4 * i) = x;
         }
     } else {  // EPI_RELU2
-      bf16* dst = p.out_bf16 + (int64_t)row * p.ldo + n0;
+      T16* dst = reinterpret_cast<T16*>(p.out_16) + (int64_t)row * p.ldo + n0;
 #pragma unroll
       for (int i = 0; i < 4; ++i)
         if (n0 + 8 * i < p.N) {
@@ -119,8 +119,8 @@ __device__ __forceinline__ void epi_store_rows(const GemmArgs& p, uint32_t taddr
             a[j] = r * r;
           }
           *reinterpret_cast<uint4*>(dst + 8 * i) =
-              make_uint4(pack_bf16x2(a[0], a[1]), pack_bf16x2(a[2], a[3]), pack_bf16x2(a[4], a[5]),
-                         pack_bf16x2(a[6], a[7]));
+              make_uint4(pack2<T16>(a[0], a[1]), pack2<T16>(a[2], a[3]), pack2<T16>(a[4], a[5]),
+                         pack2<T16>(a[6], a[7]));
         }
     }
   }
@@ -130,7 +130,7 @@ __device__ __forceinline__ void epi_store_rows(const GemmArgs& p, uint32_t taddr
 // concatenated [Q | K | V] projection. For Q and K heads: the mean square is
 // taken over the un-rotated values (the rotation keeps the norm), then pairs
 // (i, i + 64) are rotated by +theta(t, i) and scaled by the QK-norm factor.
-template <int BN>
+template <int BN, class T16>
 __device__ __forceinline__ void epi_qkv(const GemmArgs& p, uint32_t taddr, int row, int nb) {
   const QkvDst& q = p.qkv;
   const bool valid = row < p.M;
@@ -144,7 +144,7 @@ __device__ __forceinline__ void epi_qkv(const GemmArgs& p, uint32_t taddr, int r
     const uint32_t base = taddr + hc * 128;
     if (j >= q.H + q.Hkv) {  // V head, stored as projected
       const int g = j - q.H - q.Hkv;
-      bf16* out = reinterpret_cast<bf16*>(q.v_cache) + (((int64_t)b * q.Hkv + g) * q.t_max + t) * 128;
+      T16* out = reinterpret_cast<T16*>(q.v_cache) + (((int64_t)b * q.Hkv + g) * q.t_max + t) * 128;
 #pragma unroll 1
       for (int c = 0; c < 4; ++c) {
         float v[32];
@@ -153,8 +153,8 @@ __device__ __forceinline__ void epi_qkv(const GemmArgs& p, uint32_t taddr, int r
 #pragma unroll
           for (int i = 0; i < 4; ++i)
             *reinterpret_cast<uint4*>(out + c * 32 + 8 * i) = make_uint4(
-                pack_bf16x2(v[8 * i], v[8 * i + 1]), pack_bf16x2(v[8 * i + 2], v[8 * i + 3]),
-                pack_bf16x2(v[8 * i + 4], v[8 * i + 5]), pack_bf16x2(v[8 * i + 6], v[8 * i + 7]));
+                pack2<T16>(v[8 * i], v[8 * i + 1]), pack2<T16>(v[8 * i + 2], v[8 * i + 3]),
+                pack2<T16>(v[8 * i + 4], v[8 * i + 5]), pack2<T16>(v[8 * i + 6], v[8 * i + 7]));
         }
       }
       continue;
@@ -168,12 +168,12 @@ __device__ __forceinline__ void epi_qkv(const GemmArgs& p, uint32_t taddr, int r
       for (int i = 0; i < 32; ++i) ss = fmaf(v[i], v[i], ss);
     }
     const float r = rsqrtf(ss * (1.f / 128.f) + q.eps);
-    bf16* out;
+    T16* out;
     if (j < q.H)
-      out = reinterpret_cast<bf16*>(q.q) +
+      out = reinterpret_cast<T16*>(q.q) +
             (((int64_t)b * q.H + j) * p.rm.rows_per_seq + (t - p.rm.pos0)) * 128;
     else
-      out = reinterpret_cast<bf16*>(q.k_cache) + (((int64_t)b * q.Hkv + (j - q.H)) * q.t_max + t) * 128;
+      out = reinterpret_cast<T16*>(q.k_cache) + (((int64_t)b * q.Hkv + (j - q.H)) * q.t_max + t) * 128;
     const float* cs = q.cos_tab + (int64_t)t * 64;
     const float* sn = q.sin_tab + (int64_t)t * 64;
 #pragma unroll 1
@@ -197,11 +197,11 @@ __device__ __forceinline__ void epi_qkv(const GemmArgs& p, uint32_t taddr, int r
 #pragma unroll
       for (int i = 0; i < 4; ++i) {
         *reinterpret_cast<uint4*>(out + c * 32 + 8 * i) = make_uint4(
-            pack_bf16x2(lo[8 * i], lo[8 * i + 1]), pack_bf16x2(lo[8 * i + 2], lo[8 * i + 3]),
-            pack_bf16x2(lo[8 * i + 4], lo[8 * i + 5]), pack_bf16x2(lo[8 * i + 6], lo[8 * i + 7]));
+            pack2<T16>(lo[8 * i], lo[8 * i + 1]), pack2<T16>(lo[8 * i + 2], lo[8 * i + 3]),
+            pack2<T16>(lo[8 * i + 4], lo[8 * i + 5]), pack2<T16>(lo[8 * i + 6], lo[8 * i + 7]));
         *reinterpret_cast<uint4*>(out + 64 + c * 32 + 8 * i) = make_uint4(
-            pack_bf16x2(hi[8 * i], hi[8 * i + 1]), pack_bf16x2(hi[8 * i + 2], hi[8 * i + 3]),
-            pack_bf16x2(hi[8 * i + 4], hi[8 * i + 5]), pack_bf16x2(hi[8 * i + 6], hi[8 * i + 7]));
+            pack2<T16>(hi[8 * i], hi[8 * i + 1]), pack2<T16>(hi[8 * i + 2], hi[8 * i + 3]),
+            pack2<T16>(hi[8 * i + 4], hi[8 * i + 5]), pack2<T16>(hi[8 * i + 6], hi[8 * i + 7]));
       }
     }
   }
@@ -226,7 +226,7 @@ __device__ __forceinline__ void epi_swap(const GemmArgs& p, uint32_t taddr, int 
 }
 
 // --------------------------------------------------------------------- kernel
-template <int BN, int EPI>
+template <int BN, int EPI, class T16>
 __global__ void __launch_bounds__(192, 1)
     gemm_tc_kernel(const __grid_constant__ CUtensorMap tmA0, const __grid_constant__ CUtensorMap tmA1,
                    const __grid_constant__ CUtensorMap tmA2, const __grid_constant__ CUtensorMap tmB0,
@@ -319,7 +319,7 @@ __global__ void __launch_bounds__(192, 1)
   } else if (warp == 1) {
     if (lane == 0) {
       // ----------------------------------------------------------- MMA issuer
-      constexpr uint32_t kIdesc = idesc_bf16_f32(128, BN);
+      constexpr uint32_t kIdesc = idesc_f32acc(Fmt16<T16>::code, 128, BN);
       int stage = 0;
       uint32_t phase = 0;
       int acc = 0;
@@ -346,7 +346,7 @@ __global__ void __launch_bounds__(192, 1)
           const uint32_t b_addr = a_addr + C::kABytes;
 #pragma unroll
           for (int k = 0; k < 4; ++k) {
-            mma_bf16_ss(d_tmem, sdesc_kmajor_sw128(a_addr + k * 32),
+            mma_f16kind_ss(d_tmem, sdesc_kmajor_sw128(a_addr + k * 32),
                         sdesc_kmajor_sw128(b_addr + k * 32), kIdesc, (kb > kb0 || k > 0) ? 1u : 0u);
           }
           mma_commit(&empty[stage]);
@@ -383,11 +383,11 @@ __global__ void __launch_bounds__(192, 1)
       const int row = mb * 128 + quarter * 32 + lane;
       const uint32_t taddr = tmem_base + ((uint32_t)(quarter * 32) << 16) + acc * BN;
       if (EPI == EPI_QKV)
-        epi_qkv<BN>(p, taddr, row, nb);
+        epi_qkv<BN, T16>(p, taddr, row, nb);
       else if (EPI == EPI_SWAP)
         epi_swap<BN>(p, taddr, row, nb, ks);
       else
-        epi_store_rows<BN>(p, taddr, row, nb, EPI);
+        epi_store_rows<BN, T16>(p, taddr, row, nb, EPI);
       tc_fence_before();
       __syncwarp();
       if (lane == 0) mbar_arrive(&tempty[acc]);
@@ -404,6 +404,7 @@ __global__ void __launch_bounds__(192, 1)
     tmem_dealloc(tmem_base, C::kTmemCols);
   }
 }
+
 
 // ======================================================================= host
 // Status word of the single-step entry point (timeouts of a bare GEMM call).
@@ -427,8 +428,13 @@ static EncodeTiledFn encode_fn() {
   return fn;
 }
 
-// Row-major bf16 matrix [rows, cols] viewed as 2D (x = column, y = row); box of
+template <class T16> struct MapType;
+template <> struct MapType<bf16> { static constexpr CUtensorMapDataType v = CU_TENSOR_MAP_DATA_TYPE_BFLOAT16; };
+template <> struct MapType<f16> { static constexpr CUtensorMapDataType v = CU_TENSOR_MAP_DATA_TYPE_FLOAT16; };
+
+// Row-major 16-bit matrix [rows, cols] viewed as 2D (x = column, y = row); box of
 // 64 columns (128 bytes, the swizzle width) by box_rows rows.
+template <class T16>
 static bool make_map(CUtensorMap* map, const void* base, uint64_t rows, uint64_t cols,
                      uint32_t box_rows) {
   EncodeTiledFn fn = encode_fn();
@@ -437,8 +443,8 @@ static bool make_map(CUtensorMap* map, const void* base, uint64_t rows, uint64_t
   cuuint64_t strides[1] = {cols * 2};
   cuuint32_t box[2] = {64, box_rows};
   cuuint32_t estr[2] = {1, 1};
-  return fn(map, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 2, const_cast<void*>(base), dims, strides, box,
-            estr, CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B,
+  return fn(map, MapType<T16>::v, 2, const_cast<void*>(base), dims, strides, box, estr,
+            CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B,
             CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
 }
 
@@ -448,6 +454,7 @@ struct LayerMaps {
 
 struct TcModel {
   nc_config cfg;
+  bool f16 = true;   // 16-bit type of operands, activations and KV cache
   int sm_count = 148;
   std::vector<LayerMaps> layers;
   CUtensorMap lm;
@@ -463,12 +470,12 @@ static int sm_count_now() {
   return n;
 }
 
-template <int BN, int EPI>
+template <int BN, int EPI, class T16>
 static nc_status launch_gemm(const CUtensorMap& a0, const CUtensorMap& a1, const CUtensorMap& a2,
                              const CUtensorMap& b0, const CUtensorMap& b1, const CUtensorMap& b2,
                              const GemmArgs& args, int sm_count, cudaStream_t s) {
   using C = TileCfg<BN>;
-  auto kern = gemm_tc_kernel<BN, EPI>;
+  auto kern = gemm_tc_kernel<BN, EPI, T16>;
   static bool configured = false;
   if (!configured) {
     if (cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize,
@@ -479,6 +486,7 @@ static nc_status launch_gemm(const CUtensorMap& a0, const CUtensorMap& a1, const
   const int units = args.num_m_blk * args.num_n_blk * args.k_splits;
   const int grid = std::min(units, sm_count);
   kern<<<grid, 192, C::kSmemBytes, s>>>(a0, a1, a2, b0, b1, b2, args);
+  count_launches(1);
   return cudaGetLastError() == cudaSuccess ? NC_OK : NC_ERR_CUDA;
 }
 
@@ -507,12 +515,13 @@ static int pick_bn(int M, int N, int sm_count) {
   return cost(256) < cost(128) ? 256 : 128;
 }
 
-template <int EPI>
+template <int EPI, class T16>
 static nc_status tile_gemm(const CUtensorMap& a, const CUtensorMap& b0, const CUtensorMap& b1,
                            const CUtensorMap& b2, GemmArgs args, int BN, int sm_count,
                            cudaStream_t s) {
-  if (BN == 256) return launch_gemm<256, EPI>(a, a, a, b0, b1, b2, args, sm_count, s);
-  return launch_gemm<128, EPI>(a, a, a, b0, b1, b2, args, sm_count, s);
+  args.num_n_blk = (args.N + BN - 1) / BN;
+  if (BN == 256) return launch_gemm<256, EPI, T16>(a, a, a, b0, b1, b2, args, sm_count, s);
+  return launch_gemm<128, EPI, T16>(a, a, a, b0, b1, b2, args, sm_count, s);
 }
 
 // swap mode: features (weight rows, A) x tokens (B), split over K
@@ -525,19 +534,21 @@ static void plan_splits(GemmArgs& a, int sm_count) {
 
 static int swap_bn(int64_t M) { return M <= 32 ? 32 : (M <= 64 ? 64 : 128); }
 
+template <class T16>
 static nc_status swap_gemm(const CUtensorMap& a0, const CUtensorMap& a1, const CUtensorMap& a2,
                            const void* act, int64_t M, int K, GemmArgs args, int sm_count,
                            cudaStream_t s) {
   const int BN = swap_bn(M);
   CUtensorMap b;
-  if (!make_map(&b, act, (uint64_t)M, (uint64_t)K, BN)) return NC_ERR_CUDA;
+  if (!make_map<T16>(&b, act, (uint64_t)M, (uint64_t)K, BN)) return NC_ERR_CUDA;
   args.num_n_blk = 1;
-  if (BN == 32) return launch_gemm<32, EPI_SWAP>(a0, a1, a2, b, b, b, args, sm_count, s);
-  if (BN == 64) return launch_gemm<64, EPI_SWAP>(a0, a1, a2, b, b, b, args, sm_count, s);
-  return launch_gemm<128, EPI_SWAP>(a0, a1, a2, b, b, b, args, sm_count, s);
+  if (BN == 32) return launch_gemm<32, EPI_SWAP, T16>(a0, a1, a2, b, b, b, args, sm_count, s);
+  if (BN == 64) return launch_gemm<64, EPI_SWAP, T16>(a0, a1, a2, b, b, b, args, sm_count, s);
+  return launch_gemm<128, EPI_SWAP, T16>(a0, a1, a2, b, b, b, args, sm_count, s);
 }
 
 // split-K partial sums of Y^T = W X^T, written as part[split][token][feature]
+template <class T16>
 static nc_status swap_partials(TcModel* t, const CUtensorMap& w0, const CUtensorMap& w1,
                                const CUtensorMap& w2, int split0, int split1, int n_feat, int K,
                                const void* act, int64_t M, float* part, int* n_split,
@@ -550,18 +561,148 @@ static nc_status swap_partials(TcModel* t, const CUtensorMap& w0, const CUtensor
   a.ldo = n_feat;
   a.split_stride = (int64_t)M * n_feat;
   *n_split = a.k_splits;
-  return swap_gemm(w0, w1, w2, act, M, K, a, t->sm_count, s);
+  return swap_gemm<T16>(w0, w1, w2, act, M, K, a, t->sm_count, s);
 }
 
-nc_status tc_create(const nc_config& cfg, const void* wte, const void* lm_head,
-                    const void* const* wq, const void* const* wk, const void* const* wv,
-                    const void* const* wo, const void* const* w_fc, const void* const* w_proj,
-                    void* xn, void* att, void* h, void* xnl, size_t max_rows, uint32_t* status,
-                    TcModel** out) {
-  (void)wte;
+static nc_dtype act_of(const TcModel* t) { return t->f16 ? NC_F16 : NC_BF16; }
+
+template <class T16>
+static nc_status qkv_impl(TcModel* t, int l, int64_t M, const RowMap& rm, const QkvDst& dst,
+                          float* part, cudaStream_t s) {
+  const nc_config& c = t->cfg;
+  const LayerMaps& w = t->layers[l];
+  const int d = c.d_model, qd = c.n_head * 128, kvd = c.n_kv_head * 128;
+  const int nqkv = qd + 2 * kvd;
+  if (M <= kSwapMaxRows) {
+    int ns = 1;
+    nc_status st = swap_partials<T16>(t, w.wq, w.wk, w.wv, qd, qd + kvd, nqkv, d, t->xn, M, part,
+                                      &ns, s);
+    if (st != NC_OK) return st;
+    launch_qkv_post(part, ns, M, rm, dst, act_of(t), s);
+    return cudaGetLastError() == cudaSuccess ? NC_OK : NC_ERR_CUDA;
+  }
+  CUtensorMap a;
+  if (!make_map<T16>(&a, t->xn, (uint64_t)M, d, 128)) return NC_ERR_CUDA;
+  GemmArgs args = base_args((int)M, nqkv, d, 256, t->status);
+  args.b_split0 = qd;
+  args.b_split1 = qd + kvd;
+  args.rm = rm;
+  args.qkv = dst;
+  return launch_gemm<256, EPI_QKV, T16>(a, a, a, w.wq, w.wk, w.wv, args, t->sm_count, s);
+}
+
+template <class T16>
+static nc_status out_proj_impl(TcModel* t, int l, int64_t M, float* x, float* part,
+                               cudaStream_t s) {
+  const nc_config& c = t->cfg;
+  const LayerMaps& w = t->layers[l];
+  const int d = c.d_model, qd = c.n_head * 128;
+  if (M <= kSwapMaxRows) {
+    int ns = 1;
+    nc_status st = swap_partials<T16>(t, w.wo, w.wo, w.wo, INT_MAX, INT_MAX, d, qd, t->att, M,
+                                      part, &ns, s);
+    if (st != NC_OK) return st;
+    launch_residual_finish(part, ns, x, M, d, nullptr, act_of(t), c.rms_eps, s);
+    return cudaGetLastError() == cudaSuccess ? NC_OK : NC_ERR_CUDA;
+  }
+  CUtensorMap a;
+  if (!make_map<T16>(&a, t->att, (uint64_t)M, qd, 128)) return NC_ERR_CUDA;
+  const int BN = pick_bn((int)M, d, t->sm_count);
+  GemmArgs args = base_args((int)M, d, qd, BN, t->status);
+  args.out_f32 = x;
+  args.ldo = d;
+  return tile_gemm<EPI_RESID, T16>(a, w.wo, w.wo, w.wo, args, BN, t->sm_count, s);
+}
+
+template <class T16>
+static nc_status fc_impl(TcModel* t, int l, int64_t M, float* part, cudaStream_t s) {
+  const nc_config& c = t->cfg;
+  const LayerMaps& w = t->layers[l];
+  const int d = c.d_model, F = c.d_mlp;
+  if (M <= kSwapMaxRows) {
+    int ns = 1;
+    nc_status st = swap_partials<T16>(t, w.wfc, w.wfc, w.wfc, INT_MAX, INT_MAX, F, d, t->xn, M,
+                                      part, &ns, s);
+    if (st != NC_OK) return st;
+    launch_relu2_finish(part, ns, t->h, M, F, act_of(t), s);
+    return cudaGetLastError() == cudaSuccess ? NC_OK : NC_ERR_CUDA;
+  }
+  CUtensorMap a;
+  if (!make_map<T16>(&a, t->xn, (uint64_t)M, d, 128)) return NC_ERR_CUDA;
+  const int BN = pick_bn((int)M, F, t->sm_count);
+  GemmArgs args = base_args((int)M, F, d, BN, t->status);
+  args.out_16 = t->h;
+  args.ldo = F;
+  return tile_gemm<EPI_RELU2, T16>(a, w.wfc, w.wfc, w.wfc, args, BN, t->sm_count, s);
+}
+
+template <class T16>
+static nc_status proj_impl(TcModel* t, int l, int64_t M, float* x, float* part, cudaStream_t s) {
+  const nc_config& c = t->cfg;
+  const LayerMaps& w = t->layers[l];
+  const int d = c.d_model, F = c.d_mlp;
+  if (M <= kSwapMaxRows) {
+    int ns = 1;
+    nc_status st = swap_partials<T16>(t, w.wproj, w.wproj, w.wproj, INT_MAX, INT_MAX, d, F, t->h,
+                                      M, part, &ns, s);
+    if (st != NC_OK) return st;
+    launch_residual_finish(part, ns, x, M, d, nullptr, act_of(t), c.rms_eps, s);
+    return cudaGetLastError() == cudaSuccess ? NC_OK : NC_ERR_CUDA;
+  }
+  CUtensorMap a;
+  if (!make_map<T16>(&a, t->h, (uint64_t)M, F, 128)) return NC_ERR_CUDA;
+  const int BN = pick_bn((int)M, d, t->sm_count);
+  GemmArgs args = base_args((int)M, d, F, BN, t->status);
+  args.out_f32 = x;
+  args.ldo = d;
+  return tile_gemm<EPI_RESID, T16>(a, w.wproj, w.wproj, w.wproj, args, BN, t->sm_count, s);
+}
+
+template <class T16>
+static nc_status lm_impl(TcModel* t, const void* xn, int64_t M, float* logits, cudaStream_t s) {
+  const nc_config& c = t->cfg;
+  const int d = c.d_model, V = c.vocab;
+  if (M <= kSwapMaxRows) {
+    GemmArgs a = base_args(V, (int)M, d, swap_bn(M), t->status);
+    a.out_f32 = logits;
+    a.ldo = V;
+    a.split_stride = 0;
+    return swap_gemm<T16>(t->lm, t->lm, t->lm, xn, M, d, a, t->sm_count, s);
+  }
+  CUtensorMap a;
+  if (!make_map<T16>(&a, xn, (uint64_t)M, d, 128)) return NC_ERR_CUDA;
+  GemmArgs args = base_args((int)M, V, d, 256, t->status);
+  args.out_f32 = logits;
+  args.ldo = V;
+  return tile_gemm<EPI_F32, T16>(a, t->lm, t->lm, t->lm, args, 256, t->sm_count, s);
+}
+
+template <class T16>
+static bool build_maps(TcModel* t, const void* lm_head, const void* const* wq,
+                       const void* const* wk, const void* const* wv, const void* const* wo,
+                       const void* const* w_fc, const void* const* w_proj) {
+  const nc_config& cfg = t->cfg;
+  const uint64_t d = cfg.d_model, qd = (uint64_t)cfg.n_head * 128,
+                 kvd = (uint64_t)cfg.n_kv_head * 128, F = cfg.d_mlp;
+  t->layers.resize(cfg.n_layer);
+  bool ok = make_map<T16>(&t->lm, lm_head, cfg.vocab, d, 128);
+  for (int l = 0; l < cfg.n_layer && ok; ++l) {
+    LayerMaps& m = t->layers[l];
+    ok = make_map<T16>(&m.wq, wq[l], qd, d, 128) && make_map<T16>(&m.wk, wk[l], kvd, d, 128) &&
+         make_map<T16>(&m.wv, wv[l], kvd, d, 128) && make_map<T16>(&m.wo, wo[l], d, qd, 128) &&
+         make_map<T16>(&m.wfc, w_fc[l], F, d, 128) && make_map<T16>(&m.wproj, w_proj[l], d, F, 128);
+  }
+  return ok;
+}
+
+nc_status tc_create(const nc_config& cfg, const void* lm_head, const void* const* wq,
+                    const void* const* wk, const void* const* wv, const void* const* wo,
+                    const void* const* w_fc, const void* const* w_proj, void* xn, void* att,
+                    void* h, void* xnl, size_t max_rows, uint32_t* status, TcModel** out) {
   if (!encode_fn()) return NC_ERR_CUDA;
   TcModel* t = new TcModel();
   t->cfg = cfg;
+  t->f16 = cfg.act_dtype == NC_F16;
   t->sm_count = sm_count_now();
   t->xn = xn;
   t->att = att;
@@ -569,16 +710,8 @@ nc_status tc_create(const nc_config& cfg, const void* wte, const void* lm_head,
   t->xnl = xnl;
   t->max_rows = max_rows;
   t->status = status;
-  const uint64_t d = cfg.d_model, qd = (uint64_t)cfg.n_head * 128, kvd = (uint64_t)cfg.n_kv_head * 128,
-                 F = cfg.d_mlp;
-  t->layers.resize(cfg.n_layer);
-  bool ok = make_map(&t->lm, lm_head, cfg.vocab, d, 128);
-  for (int l = 0; l < cfg.n_layer && ok; ++l) {
-    LayerMaps& m = t->layers[l];
-    ok = make_map(&m.wq, wq[l], qd, d, 128) && make_map(&m.wk, wk[l], kvd, d, 128) &&
-         make_map(&m.wv, wv[l], kvd, d, 128) && make_map(&m.wo, wo[l], d, qd, 128) &&
-         make_map(&m.wfc, w_fc[l], F, d, 128) && make_map(&m.wproj, w_proj[l], d, F, 128);
-  }
+  const bool ok = t->f16 ? build_maps<f16>(t, lm_head, wq, wk, wv, wo, w_fc, w_proj)
+                         : build_maps<bf16>(t, lm_head, wq, wk, wv, wo, w_fc, w_proj);
   if (!ok) {
     delete t;
     return NC_ERR_CUDA;
@@ -591,103 +724,30 @@ void tc_destroy(TcModel* t) { delete t; }
 
 nc_status tc_qkv(TcModel* t, int l, int64_t M, const RowMap& rm, const QkvDst& dst, float* part,
                  cudaStream_t s) {
-  const nc_config& c = t->cfg;
-  const LayerMaps& w = t->layers[l];
-  const int d = c.d_model, qd = c.n_head * 128, kvd = c.n_kv_head * 128;
-  const int nqkv = qd + 2 * kvd;
-  if (M <= kSwapMaxRows) {
-    int ns = 1;
-    nc_status st = swap_partials(t, w.wq, w.wk, w.wv, qd, qd + kvd, nqkv, d, t->xn, M, part, &ns, s);
-    if (st != NC_OK) return st;
-    launch_qkv_post(part, ns, M, rm, dst, NC_BF16, s);
-    return cudaGetLastError() == cudaSuccess ? NC_OK : NC_ERR_CUDA;
-  }
-  CUtensorMap a;
-  if (!make_map(&a, t->xn, (uint64_t)M, d, 128)) return NC_ERR_CUDA;
-  GemmArgs args = base_args((int)M, nqkv, d, 256, t->status);
-  args.b_split0 = qd;
-  args.b_split1 = qd + kvd;
-  args.rm = rm;
-  args.qkv = dst;
-  return launch_gemm<256, EPI_QKV>(a, a, a, w.wq, w.wk, w.wv, args, t->sm_count, s);
+  return t->f16 ? qkv_impl<f16>(t, l, M, rm, dst, part, s) : qkv_impl<bf16>(t, l, M, rm, dst, part, s);
 }
-
 nc_status tc_out_proj(TcModel* t, int l, int64_t M, float* x, float* part, cudaStream_t s) {
-  const nc_config& c = t->cfg;
-  const LayerMaps& w = t->layers[l];
-  const int d = c.d_model, qd = c.n_head * 128;
-  if (M <= kSwapMaxRows) {
-    int ns = 1;
-    nc_status st = swap_partials(t, w.wo, w.wo, w.wo, INT_MAX, INT_MAX, d, qd, t->att, M, part, &ns, s);
-    if (st != NC_OK) return st;
-    launch_residual_finish(part, ns, x, M, d, nullptr, NC_BF16, c.rms_eps, s);
-    return cudaGetLastError() == cudaSuccess ? NC_OK : NC_ERR_CUDA;
-  }
-  CUtensorMap a;
-  if (!make_map(&a, t->att, (uint64_t)M, qd, 128)) return NC_ERR_CUDA;
-  const int BN = pick_bn((int)M, d, t->sm_count);
-  GemmArgs args = base_args((int)M, d, qd, BN, t->status);
-  args.out_f32 = x;
-  args.ldo = d;
-  return tile_gemm<EPI_RESID>(a, w.wo, w.wo, w.wo, args, BN, t->sm_count, s);
+  return t->f16 ? out_proj_impl<f16>(t, l, M, x, part, s) : out_proj_impl<bf16>(t, l, M, x, part, s);
 }
-
-nc_status tc_mlp(TcModel* t, int l, int64_t M, float* x, float* part, cudaStream_t s) {
-  const nc_config& c = t->cfg;
-  const LayerMaps& w = t->layers[l];
-  const int d = c.d_model, F = c.d_mlp;
-  if (M <= kSwapMaxRows) {
-    int ns = 1;
-    nc_status st = swap_partials(t, w.wfc, w.wfc, w.wfc, INT_MAX, INT_MAX, F, d, t->xn, M, part, &ns, s);
-    if (st != NC_OK) return st;
-    launch_relu2_finish(part, ns, t->h, M, F, NC_BF16, s);
-    st = swap_partials(t, w.wproj, w.wproj, w.wproj, INT_MAX, INT_MAX, d, F, t->h, M, part, &ns, s);
-    if (st != NC_OK) return st;
-    launch_residual_finish(part, ns, x, M, d, nullptr, NC_BF16, c.rms_eps, s);
-    return cudaGetLastError() == cudaSuccess ? NC_OK : NC_ERR_CUDA;
-  }
-  CUtensorMap a;
-  if (!make_map(&a, t->xn, (uint64_t)M, d, 128)) return NC_ERR_CUDA;
-  int BN = pick_bn((int)M, F, t->sm_count);
-  GemmArgs args = base_args((int)M, F, d, BN, t->status);
-  args.out_bf16 = reinterpret_cast<bf16*>(t->h);
-  args.ldo = F;
-  nc_status st = tile_gemm<EPI_RELU2>(a, w.wfc, w.wfc, w.wfc, args, BN, t->sm_count, s);
-  if (st != NC_OK) return st;
-  CUtensorMap a2;
-  if (!make_map(&a2, t->h, (uint64_t)M, F, 128)) return NC_ERR_CUDA;
-  BN = pick_bn((int)M, d, t->sm_count);
-  args = base_args((int)M, d, F, BN, t->status);
-  args.out_f32 = x;
-  args.ldo = d;
-  return tile_gemm<EPI_RESID>(a2, w.wproj, w.wproj, w.wproj, args, BN, t->sm_count, s);
+nc_status tc_fc(TcModel* t, int l, int64_t M, float* part, cudaStream_t s) {
+  return t->f16 ? fc_impl<f16>(t, l, M, part, s) : fc_impl<bf16>(t, l, M, part, s);
 }
-
+nc_status tc_proj(TcModel* t, int l, int64_t M, float* x, float* part, cudaStream_t s) {
+  return t->f16 ? proj_impl<f16>(t, l, M, x, part, s) : proj_impl<bf16>(t, l, M, x, part, s);
+}
 nc_status tc_lm_head(TcModel* t, const void* xn, int64_t M, float* logits, float* part,
                      cudaStream_t s) {
   (void)part;
-  const nc_config& c = t->cfg;
-  const int d = c.d_model, V = c.vocab;
-  if (M <= kSwapMaxRows) {
-    GemmArgs a = base_args(V, (int)M, d, swap_bn(M), t->status);
-    a.out_f32 = logits;
-    a.ldo = V;
-    a.split_stride = 0;
-    return swap_gemm(t->lm, t->lm, t->lm, xn, M, d, a, t->sm_count, s);
-  }
-  CUtensorMap a;
-  if (!make_map(&a, xn, (uint64_t)M, d, 128)) return NC_ERR_CUDA;
-  GemmArgs args = base_args((int)M, V, d, 256, t->status);
-  args.out_f32 = logits;
-  args.ldo = V;
-  return tile_gemm<EPI_F32>(a, t->lm, t->lm, t->lm, args, 256, t->sm_count, s);
+  return t->f16 ? lm_impl<f16>(t, xn, M, logits, s) : lm_impl<bf16>(t, xn, M, logits, s);
 }
 
 nc_status tc_gemm_f32out(const void* A, const void* B, float* C, int M, int N, int K,
-                         cudaStream_t s) {
+                         nc_dtype dt, cudaStream_t s) {
   CUtensorMap a, b;
-  if (!make_map(&a, A, (uint64_t)M, (uint64_t)K, 128) || !make_map(&b, B, (uint64_t)N, (uint64_t)K, 128))
-    return NC_ERR_CUDA;
+  const bool h = dt == NC_F16;
+  const bool ok = h ? (make_map<f16>(&a, A, M, K, 128) && make_map<f16>(&b, B, N, K, 128))
+                    : (make_map<bf16>(&a, A, M, K, 128) && make_map<bf16>(&b, B, N, K, 128));
+  if (!ok) return NC_ERR_CUDA;
   const int sm = sm_count_now();
   const int BN = pick_bn(M, N, sm);
   GemmArgs args = base_args(M, N, K, BN, nullptr);
@@ -695,7 +755,8 @@ nc_status tc_gemm_f32out(const void* A, const void* B, float* C, int M, int N, i
     return NC_ERR_CUDA;
   args.out_f32 = C;
   args.ldo = N;
-  return tile_gemm<EPI_F32>(a, b, b, b, args, BN, sm, s);
+  return h ? tile_gemm<EPI_F32, f16>(a, b, b, b, args, BN, sm, s)
+           : tile_gemm<EPI_F32, bf16>(a, b, b, b, args, BN, sm, s);
 }
 
 }  // namespace nc
