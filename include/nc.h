@@ -214,6 +214,29 @@ NC_API nc_status nc_op_attention_decode(const void* q, const void* k, const void
                                         int32_t t_max, int32_t hd, nc_dtype dtype, void* scratch,
                                         size_t scratch_bytes, void* stream);
 
+/* The same decode attention for callers that cannot allocate device memory
+ * (an engine that owns all device memory through its own pool and forbids side
+ * allocations, a plugin inside such a host, a latency-critical loop that cannot
+ * take an allocation's implicit synchronisation). The paper has no counterpart:
+ * this is a deployment variant. Arguments as nc_op_attention_decode, without the
+ * scratch buffer: the split partial states go to one fixed 8 MiB array in the
+ * library's device memory, held on every GPU that loads the library until the
+ * process exits. It calls no cudaMalloc, cudaFree or other allocating routine.
+ *   - B * H * splits * (head_dim + 2) * 4 bytes must fit in 8 MiB (splits =
+ *     ceil(len / 128), at most 64); larger calls return NC_ERR_INVALID_ARG and
+ *     nc_last_error() says how much was needed.
+ *   - The first call on each device looks up the array's device address
+ *     (cudaGetSymbolAddress, with that device current); make that first call
+ *     before any stream capture.
+ *   - Every call shares the one array, which keeps the last call's contents.
+ *     Each call writes every partial state it reads, so nothing needs clearing,
+ *     but calls that overlap on the GPU (other streams, other threads) race on
+ *     the array: serialise them. */
+NC_API nc_status nc_op_attention_decode_noalloc(const void* q, const void* k, const void* v,
+                                                void* o, int32_t B, int32_t H, int32_t Hkv,
+                                                int32_t len, int32_t t_max, int32_t hd,
+                                                nc_dtype dtype, void* stream);
+
 /* out[r] = index of the largest x[r, :] (lowest index on ties); x dev fp32
  * [rows, n], out dev int32 [rows]. */
 NC_API nc_status nc_op_argmax(const float* x, int32_t rows, int32_t n, int32_t* out, void* stream);

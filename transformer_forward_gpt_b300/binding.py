@@ -24,6 +24,7 @@ EXPORTS = (
     "nc_model_check", "nc_op_rmsnorm", "nc_op_gemm", "nc_op_attention_prefill",
     "nc_op_attention_decode_scratch_bytes", "nc_op_attention_decode", "nc_op_argmax",
     "nc_kv_cache_set_length", "nc_profile_begin", "nc_profile_end", "nc_launch_count",
+    "nc_op_attention_decode_noalloc",
 )
 
 KERNEL_KINDS = ("embed", "norm", "qkv", "attn_prefill", "attn_decode", "oproj", "fc", "proj",
@@ -91,6 +92,8 @@ def load(path: str = LIB_PATH):
         "nc_profile_begin": (C.c_int, [vp]),
         "nc_profile_end": (C.c_int, [vp, vp, C.POINTER(NcKernelTime)]),
         "nc_launch_count": (i64, []),
+        "nc_op_attention_decode_noalloc": (C.c_int, [vp, vp, vp, vp, i32, i32, i32, i32, i32,
+                                                     i32, C.c_int, vp]),
     }
     for name, (res, args) in sig.items():
         f = getattr(lib, name)
@@ -241,6 +244,13 @@ def nc_op_attention_decode(q, k, v, o, B, H, Hkv, length, t_max, hd, dtype, scra
 
 def nc_op_argmax(x, rows, n, out, stream=None):
     _check(load().nc_op_argmax(_ptr(x), rows, n, _ptr(out), _stream(stream)), "nc_op_argmax")
+
+
+def nc_op_attention_decode_noalloc(q, k, v, o, B, H, Hkv, length, t_max, hd, dtype, stream=None):
+    """Decode attention whose scratch is a fixed array inside the library (no allocation)."""
+    _check(load().nc_op_attention_decode_noalloc(_ptr(q), _ptr(k), _ptr(v), _ptr(o), B, H, Hkv,
+                                                 length, t_max, hd, dtype, _stream(stream)),
+           "nc_op_attention_decode_noalloc")
 
 
 def nc_kv_cache_set_length(cache, length):

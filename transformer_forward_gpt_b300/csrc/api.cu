@@ -68,6 +68,12 @@ struct ProfRec {
 
 namespace nc {
 void count_launches(int n) { g_launches.fetch_add(n, std::memory_order_relaxed); }
+void set_last_error(const char* fmt, ...) {
+  va_list ap;
+  va_start(ap, fmt);
+  vsnprintf(g_err, sizeof(g_err), fmt, ap);
+  va_end(ap);
+}
 }  // namespace nc
 
 struct nc_model {

@@ -10,6 +10,8 @@ namespace nc {
 
 // Process-wide count of kernel launches made by the library (measurement only).
 void count_launches(int n);
+// Sets the thread-local text nc_last_error() returns.
+void set_last_error(const char* fmt, ...);
 
 // Where the rows of a projection output go (prefill: rows = B*T tokens of B
 // sequences starting at position pos0 = 0; decode: rows = B, one per sequence, at
