@@ -178,6 +178,9 @@ def run_ours(args):
     # (a) d20 prefill
     wl_p = synth.WORKLOADS["d20_prefill"]
     sp, Bp, Tp = wl_p.shape, wl_p.batch, wl_p.seq
+    profiling_aid = args.phase != "both" or args.prefill_batch is not None
+    if args.prefill_batch:
+        Bp = args.prefill_batch
     Wp = synth.make_weights(sp)
     mp = nc.Model(Wp, max_seq=Tp, max_batch=Bp)
     del Wp
@@ -200,9 +203,13 @@ def run_ours(args):
     torch.cuda.synchronize()
 
     def prefill_phase():
+        if args.phase == "decode":
+            return
         nc.nc_prefill(mp.handle, tok_p, Bp, Tp, logits_p, cp.handle, stream)
 
     def decode_phase():
+        if args.phase == "prefill":
+            return
         nc.nc_kv_cache_set_length(cd.handle, Td)
         tok_buf.copy_(tok0)
         for j in range(steps):
@@ -246,8 +253,11 @@ def run_ours(args):
     decode_phase()
     prof_d = nc.nc_profile_end(md.handle, stream)
 
+    if profiling_aid:
+        return
     # end to end through the C ABI with host buffers
-    e2e = run_e2e(nc, synth, mp, cp, md, cd, sp, Bp, Tp, sd, Bd, Td, steps, args, dev, stream)
+    e2e = (run_e2e(nc, synth, mp, cp, md, cd, sp, Bp, Tp, sd, Bd, Td, steps, args, dev, stream)
+           if not args.no_e2e else {"prefill": None, "decode": None})
 
     if rank != 0:
         return
@@ -457,6 +467,11 @@ def main():
     ap.add_argument("--warmup", type=int, default=3)
     ap.add_argument("--impl", choices=("ours", "reference"), default="ours")
     ap.add_argument("--no-cpu-baseline", action="store_true")
+    ap.add_argument("--no-e2e", action="store_true", help="skip the host-buffer runs")
+    ap.add_argument("--phase", choices=("both", "prefill", "decode"), default="both",
+                    help="profiling aid: run only one phase of the step (no JSON line)")
+    ap.add_argument("--prefill-batch", type=int, default=None,
+                    help="profiling aid: smaller prefill batch (no JSON line)")
     ap.add_argument("--cpu-budget", type=float, default=30.0)
     args = ap.parse_args()
     if args.warmup < 3 and args.impl == "ours":

@@ -205,9 +205,11 @@ NC_API nc_status nc_op_attention_prefill(const void* q, const void* k, const voi
 
 /* Attention of one query per sequence (decode) over cache positions 0..len-1.
  * q dev [B, H, hd]; k, v dev [B, Hkv, t_max, hd]; o dev [B, H*hd]. Splits the
- * positions into chunks whose partial softmax states go to `scratch` (dev,
- * >= nc_op_attention_decode_scratch_bytes() bytes, caller-owned) and are merged
- * by log-sum-exp. */
+ * positions into ranges whose partial softmax states go to `scratch` (dev,
+ * caller-owned, at least nc_op_attention_decode_scratch_bytes(B, H, t_max, hd)
+ * bytes, an upper bound for every len <= t_max) and are merged by log-sum-exp.
+ * 16-bit types with hd 128 and H/Hkv <= 16 run on tensor cores (mma.sync; one
+ * pass over K/V serves all query heads of a KV head); others on CUDA cores. */
 NC_API size_t nc_op_attention_decode_scratch_bytes(int32_t B, int32_t H, int32_t t_max, int32_t hd);
 NC_API nc_status nc_op_attention_decode(const void* q, const void* k, const void* v, void* o,
                                         int32_t B, int32_t H, int32_t Hkv, int32_t len,
@@ -222,8 +224,9 @@ NC_API nc_status nc_op_attention_decode(const void* q, const void* k, const void
  * scratch buffer: the split partial states go to one fixed 8 MiB array in the
  * library's device memory, held on every GPU that loads the library until the
  * process exits. It calls no cudaMalloc, cudaFree or other allocating routine.
- *   - B * H * splits * (head_dim + 2) * 4 bytes must fit in 8 MiB (splits =
- *     ceil(len / 128), at most 64); larger calls return NC_ERR_INVALID_ARG and
+ *   - B * H * splits * (head_dim + 2) * 4 bytes must fit in 8 MiB (splits: the
+ *     key range is cut so that about 2 CTAs per SM are busy, at most 64 and at
+ *     most ceil(len / 64)); larger calls return NC_ERR_INVALID_ARG and
  *     nc_last_error() says how much was needed.
  *   - The first call on each device looks up the array's device address
  *     (cudaGetSymbolAddress, with that device current); make that first call

@@ -44,9 +44,11 @@ def test_noalloc_matches_scratch_entry_point_twice(cuda_device, B, H, Hkv, lengt
 
 def test_noalloc_rejects_sizes_beyond_its_array(cuda_device):
     import torch
-    B, H, Hkv, length, hd = 64, 16, 16, 8192, 128   # 64 splits: 34 MB > 8 MiB
+    # 1024 sequences x 16 heads x 1 split x 130 floats = 8.5 MB > 8 MiB. The
+    # buffers are real and large enough, so nothing could read out of bounds.
+    B, H, Hkv, length, hd = 1024, 16, 16, 64, 128
     q = torch.zeros(B, H, hd, device="cuda", dtype=torch.float16)
-    kv = torch.zeros(1, device="cuda", dtype=torch.float16)
+    kv = torch.zeros(B, Hkv, length, hd, device="cuda", dtype=torch.float16)
     o = torch.zeros(B, H * hd, device="cuda", dtype=torch.float16)
     with pytest.raises(nc.NcError) as e:
         nc.nc_op_attention_decode_noalloc(q, kv, kv, o, B, H, Hkv, length, length, hd, nc.NC_F16)

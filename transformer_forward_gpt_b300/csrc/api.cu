@@ -477,10 +477,8 @@ nc_status run_blocks(nc_model* m, nc_kv_cache* c, int B, int rows_per_seq, int p
     {
     ProfScope ps(m, decode ? NC_K_ATTN_DECODE : NC_K_ATTN_PREFILL, s);
     if (decode) {
-      const int len = pos0 + 1;
-      const int ns = nc::decode_attention_splits(len);
-      nc::launch_attention_decode_simt(m->q, dst.k_cache, dst.v_cache, m->att, B, H, Hkv, len,
-                                       c->t_max, hd, dt, m->attn_scratch, ns, s);
+      nc::launch_attention_decode(m->q, dst.k_cache, dst.v_cache, m->att, B, H, Hkv, pos0 + 1,
+                                  c->t_max, hd, dt, m->attn_scratch, s);
     } else if (tc) {
       nc_status st = nc::tc_attention_prefill(m->q, dst.k_cache, dst.v_cache, m->att, B, H, Hkv,
                                               rows_per_seq, c->t_max, dt, s);
@@ -755,7 +753,7 @@ nc_status nc_op_attention_prefill(const void* q, const void* k, const void* v, v
 
 size_t nc_op_attention_decode_scratch_bytes(int32_t B, int32_t H, int32_t t_max, int32_t hd) {
   if (B <= 0 || H <= 0 || t_max <= 0 || hd <= 0) return 0;
-  const int ns = nc::decode_attention_splits(t_max);
+  const int ns = std::min(64, (t_max + 63) / 64);   // the most splits any call can use
   return (size_t)B * H * ns * (hd + 2) * sizeof(float);
 }
 
@@ -768,12 +766,10 @@ nc_status nc_op_attention_decode(const void* q, const void* k, const void* v, vo
                hd % 2 == 0 && hd <= 128,
            NC_ERR_INVALID_ARG, "bad sizes");
   NC_CHECK(dtype == NC_F32 || dtype == NC_BF16 || dtype == NC_F16, NC_ERR_INVALID_ARG, "bad dtype");
-  const int ns = nc::decode_attention_splits(len);
-  NC_CHECK(scratch_bytes >= (size_t)B * H * ns * (hd + 2) * sizeof(float), NC_ERR_INVALID_ARG,
-           "scratch too small");
-  nc::launch_attention_decode_simt(q, k, v, o, B, H, Hkv, len, t_max, hd, dtype,
-                                   static_cast<float*>(scratch), ns,
-                                   static_cast<cudaStream_t>(stream));
+  NC_CHECK(scratch_bytes >= nc::decode_attention_scratch_bytes(B, H, Hkv, len, hd),
+           NC_ERR_INVALID_ARG, "scratch too small");
+  nc::launch_attention_decode(q, k, v, o, B, H, Hkv, len, t_max, hd, dtype,
+                              static_cast<float*>(scratch), static_cast<cudaStream_t>(stream));
   return check_launch();
 }
 

@@ -53,10 +53,24 @@ void launch_sum_splits(const float* part, int n_split, float* out, int64_t M, in
 void launch_attention_prefill_simt(const void* q, const void* k, const void* v, void* o, int B,
                                    int H, int Hkv, int T, int t_max, int hd, nc_dtype dt,
                                    cudaStream_t s);
-int decode_attention_splits(int len);
+// Decode attention: the key range [0, len) of each (sequence, KV head) is cut into
+// n_split ranges of tiles_per_split 64-key tiles; each range writes one partial
+// (m, l, o[hd]) per query head to scratch[((b*H + h)*n_split + split)*(hd + 2)].
+void decode_attention_plan(int len, int bg, int* tiles_per_split, int* n_split);
+size_t decode_attention_scratch_bytes(int B, int H, int Hkv, int len, int hd);
+bool decode_attention_mma_ok(int H, int Hkv, int hd, nc_dtype dt);
+// Picks the tensor-core kernel when it applies, else the CUDA-core one; then merges.
+void launch_attention_decode(const void* q, const void* k, const void* v, void* o, int B, int H,
+                             int Hkv, int len, int t_max, int hd, nc_dtype dt, float* scratch,
+                             cudaStream_t s);
+void launch_attention_decode_mma(const void* q, const void* k, const void* v, void* o, int B,
+                                 int H, int Hkv, int len, int t_max, nc_dtype dt, float* scratch,
+                                 cudaStream_t s);
 void launch_attention_decode_simt(const void* q, const void* k, const void* v, void* o, int B,
                                   int H, int Hkv, int len, int t_max, int hd, nc_dtype dt,
                                   float* scratch, int n_split, cudaStream_t s);
+void launch_attention_combine(const float* scratch, void* o, int BH, int hd, int n_split,
+                              nc_dtype dt, cudaStream_t s);
 // dst[i] = src[i] converted between number formats (weight copies).
 void launch_convert16(const void* src, nc_dtype from, void* dst, nc_dtype to, int64_t n,
                       cudaStream_t s);

@@ -64,11 +64,10 @@ extern "C" nc_status nc_op_attention_decode_noalloc(const void* q, const void* k
     nc::set_last_error("bad dtype");
     return NC_ERR_INVALID_ARG;
   }
-  const int ns = nc::decode_attention_splits(len);
-  const size_t need = (size_t)B * H * ns * (hd + 2) * sizeof(float);
+  const size_t need = nc::decode_attention_scratch_bytes(B, H, Hkv, len, hd);
   if (need > nc::kNoAllocScratchBytes) {
     nc::set_last_error("needs %zu bytes of scratch; the fixed array holds %zu (B * H * splits * "
-                       "(head_dim + 2) * 4, splits = ceil(len / 128) up to 64)",
+                       "(head_dim + 2) * 4, at most 64 splits)",
                        need, nc::kNoAllocScratchBytes);
     return NC_ERR_INVALID_ARG;
   }
@@ -78,8 +77,7 @@ extern "C" nc_status nc_op_attention_decode_noalloc(const void* q, const void* k
     nc::set_last_error("cudaGetSymbolAddress failed: %s", cudaGetErrorString(e));
     return NC_ERR_CUDA;
   }
-  nc::launch_attention_decode_simt(q, k, v, o, B, H, Hkv, len, t_max, hd, dtype,
-                                   static_cast<float*>(scratch), ns,
-                                   static_cast<cudaStream_t>(stream));
+  nc::launch_attention_decode(q, k, v, o, B, H, Hkv, len, t_max, hd, dtype,
+                              static_cast<float*>(scratch), static_cast<cudaStream_t>(stream));
   return cudaGetLastError() == cudaSuccess ? NC_OK : NC_ERR_CUDA;
 }

@@ -509,22 +509,41 @@ void launch_attention_prefill_simt(const void* q, const void* k, const void* v, 
                          (const T*)q, (const T*)k, (const T*)v, (T*)o, B, H, Hkv, T_, t_max, hd)));
 }
 
-int decode_attention_splits(int len) {
-  int n = (len + 127) / 128;
-  return n < 1 ? 1 : (n > 64 ? 64 : n);
-}
-
 void launch_attention_decode_simt(const void* q, const void* k, const void* v, void* o, int B,
                                   int H, int Hkv, int len, int t_max, int hd, nc_dtype dt,
                                   float* scratch, int n_split, cudaStream_t s) {
-  count_launches(2);
+  count_launches(1);
   dim3 grid(B * H, n_split);
   const size_t smem = hd * sizeof(float);
   NC_DISPATCH(dt, T, (attention_decode_simt_kernel<T><<<grid, 32, smem, s>>>(
                           (const T*)q, (const T*)k, (const T*)v, scratch, B, H, Hkv, len, t_max, hd,
-                          n_split),
-                      attention_combine_kernel<T><<<B * H, 128, 0, s>>>(scratch, (T*)o, B * H, hd,
-                                                                        n_split)));
+                          n_split)));
+  launch_attention_combine(scratch, o, B * H, hd, n_split, dt, s);
+}
+
+void launch_attention_combine(const float* scratch, void* o, int BH, int hd, int n_split,
+                              nc_dtype dt, cudaStream_t s) {
+  count_launches(1);
+  NC_DISPATCH(dt, T, (attention_combine_kernel<T><<<BH, 128, 0, s>>>(scratch, (T*)o, BH, hd,
+                                                                     n_split)));
+}
+
+size_t decode_attention_scratch_bytes(int B, int H, int Hkv, int len, int hd) {
+  int tps = 1, ns = 1;
+  decode_attention_plan(len, B * Hkv, &tps, &ns);
+  return (size_t)B * H * ns * (hd + 2) * sizeof(float);
+}
+
+void launch_attention_decode(const void* q, const void* k, const void* v, void* o, int B, int H,
+                             int Hkv, int len, int t_max, int hd, nc_dtype dt, float* scratch,
+                             cudaStream_t s) {
+  if (decode_attention_mma_ok(H, Hkv, hd, dt)) {
+    launch_attention_decode_mma(q, k, v, o, B, H, Hkv, len, t_max, dt, scratch, s);
+    return;
+  }
+  int tps = 1, ns = 1;
+  decode_attention_plan(len, B * Hkv, &tps, &ns);
+  launch_attention_decode_simt(q, k, v, o, B, H, Hkv, len, t_max, hd, dt, scratch, ns, s);
 }
 
 void launch_argmax(const float* x, int rows, int n, int32_t* out, cudaStream_t s) {
