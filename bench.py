@@ -178,7 +178,8 @@ def run_ours(args):
     # (a) d20 prefill
     wl_p = synth.WORKLOADS["d20_prefill"]
     sp, Bp, Tp = wl_p.shape, wl_p.batch, wl_p.seq
-    profiling_aid = args.phase != "both" or args.prefill_batch is not None
+    profiling_aid = (args.phase != "both" or args.prefill_batch is not None
+                     or args.decode_steps is not None)
     if args.prefill_batch:
         Bp = args.prefill_batch
     mp = cp = tok_p = logits_p = None
@@ -193,7 +194,7 @@ def run_ours(args):
     # (b) d20-MQA decode over a 1024-position cache
     wl_d = synth.WORKLOADS["d20_mqa_decode"]
     sd, Bd, Td = wl_d.shape, wl_d.batch, wl_d.seq
-    steps = wl_d.decode_steps
+    steps = args.decode_steps or wl_d.decode_steps
     md = cd = tok0 = tok_buf = None
     if args.phase != "prefill":
         Wd = synth.make_weights(sd)
@@ -479,6 +480,8 @@ def main():
                     help="profiling aid: run only one phase of the step (no JSON line)")
     ap.add_argument("--prefill-batch", type=int, default=None,
                     help="profiling aid: smaller prefill batch (no JSON line)")
+    ap.add_argument("--decode-steps", type=int, default=None,
+                    help="profiling aid: fewer decode steps per step (no JSON line)")
     ap.add_argument("--cpu-budget", type=float, default=30.0)
     args = ap.parse_args()
     if args.warmup < 3 and args.impl == "ours":
