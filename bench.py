@@ -346,7 +346,8 @@ def decode_kind_roofline(shape, B, ctxs, kind, ms, n, peaks, peak_src):
     steps = len(ctxs)
     per = {"qkv": 2 * L * d * (H + 2 * Hkv) * hd, "oproj": 2 * L * H * hd * d,
            "fc": 2 * L * d * F, "proj": 2 * L * F * d, "lm_head": 2 * V * d + 4 * B * V,
-           "attn_decode": sum(2 * L * B * Hkv * hd * 2 * (c + 1) for c in ctxs) / steps}
+           "attn_decode": sum(2 * L * B * Hkv * hd * 2 * (c + 1) for c in ctxs) / steps,
+           "decode_step": sum(decode_bytes(shape, B, c) for c in ctxs) / steps}
     total = per.get(kind, 0) * steps
     achieved = total / n / (ms / n / 1e3) / 1e9 if total else 0.0
     return {"bound": "hbm", "achieved": round(achieved, 1), "peak": peaks["hbm_gbs"],

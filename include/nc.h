@@ -160,6 +160,24 @@ NC_API nc_status nc_prefill_last(nc_model* m, const int32_t* tokens, int32_t B, 
 NC_API nc_status nc_decode_step(nc_model* m, const int32_t* tokens, int32_t B, int32_t pos,
                                 float* logits, int32_t* argmax_out, nc_kv_cache* c, void* stream);
 
+/* How nc_decode_step runs on the 16-bit path.
+ *   NC_DECODE_AUTO        the persistent kernel where the shape allows it
+ *                         (head_dim 128, n_head / n_kv_head <= 16, d_model and
+ *                         d_mlp multiples of 128, vocab a multiple of 4), else
+ *                         one kernel per projection / attention / norm.
+ *   NC_DECODE_PERSISTENT  always the persistent kernel (NC_ERR_UNSUPPORTED where
+ *                         the shape does not allow it).
+ *   NC_DECODE_KERNELS     always one kernel per step of the block.
+ * The persistent kernel runs a whole decode step for up to 32 sequences as one
+ * cooperative launch with one CTA per SM: a producer warp streams every weight
+ * matrix (packed once, on first use, into a model-owned copy in mma-fragment
+ * order) and the KV cache through shared memory, while the other warps compute
+ * the phases of the step between grid-wide barriers. Larger batches run as
+ * several launches of up to 32 sequences. Projection partial sums are added in
+ * fp32 in a run-dependent order. The fp32 path always uses kernels. */
+typedef enum { NC_DECODE_AUTO = 0, NC_DECODE_PERSISTENT = 1, NC_DECODE_KERNELS = 2 } nc_decode_path;
+NC_API nc_status nc_model_set_decode_path(nc_model* m, nc_decode_path path);
+
 /* Greedy generation with HOST buffers: copies prompt (host int32 [B, T]) to the
  * device, prefills (token 0 = argmax of the last prompt position), then runs
  * `steps` decode steps, step j feeding token j back at position T + j and
@@ -250,7 +268,7 @@ NC_API nc_status nc_op_argmax(const float* x, int32_t rows, int32_t n, int32_t* 
  * ---------------------------------------------------------------------- */
 typedef enum {
     NC_K_EMBED = 0, NC_K_NORM, NC_K_QKV, NC_K_ATTN_PREFILL, NC_K_ATTN_DECODE, NC_K_OPROJ,
-    NC_K_FC, NC_K_PROJ, NC_K_LM_HEAD, NC_K_ARGMAX, NC_K_COUNT
+    NC_K_FC, NC_K_PROJ, NC_K_LM_HEAD, NC_K_ARGMAX, NC_K_DECODE_STEP, NC_K_COUNT
 } nc_kernel_kind;
 
 typedef struct {
@@ -267,6 +285,18 @@ NC_API nc_status nc_profile_begin(nc_model* m);
 NC_API nc_status nc_profile_end(nc_model* m, void* stream, nc_kernel_time* out);
 /* Number of kernels the library has launched in this process so far. */
 NC_API int64_t nc_launch_count(void);
+
+/* Phase timeline of the persistent decode step. While dev_buf (device uint64
+ * [capacity], caller-owned) is set, every persistent step overwrites it with
+ * %globaltimer readings (ns) taken by CTA 0: entry 0 at the start, entries
+ * 2k-1 and 2k when it arrives at and leaves grid barrier k (k = 1 after the
+ * embedding phase, then five per layer: after QKV, attention, O, FC, PROJ; then
+ * after the final norm and after the LM head), and the last entry at the end.
+ * capacity must be at least nc_decode_trace_entries(cfg), else nothing is
+ * recorded. dev_buf NULL switches it off. Only the first 32 sequences' launch of
+ * a step is traced. The readings cost one store each. */
+NC_API nc_status nc_decode_trace(nc_model* m, uint64_t* dev_buf, int32_t capacity);
+NC_API int32_t nc_decode_trace_entries(const nc_config* cfg);
 
 #ifdef __cplusplus
 }

@@ -1,0 +1,100 @@
+"""The persistent single-launch decode step against the oracle (GPU).
+
+Each case prefills B sequences to T0 positions, then runs decode steps through
+nc_decode_step with the persistent path forced on, and compares every step's
+logits with the oracle (max |delta| <= 2e-2 x RMS), the greedy token wherever
+the oracle's top-1 margin exceeds the tolerance, and the KV cache (filled slots
+within tolerance, slots past the length still holding the poison value).
+
+The shapes cover: every N-tile width of the kernel (B = 1, 5, 12, 20, 32) and
+batches above 32 (several launches), MQA / GQA / MHA (one query head per KV
+head), contexts whose last 16-position tile is partial, long contexts where
+one (sequence, KV head) spans several CTAs (the partial softmax states are
+merged by the last of them), d_model 768 / 1280 / 1664, and bf16 storage.
+"""
+import numpy as np
+import pytest
+
+from oracle import gpt_oracle as O
+from tests.gpu_helpers import (argmax_agreement, assert_close, check_cache, oracle_weights,
+                               poison_cache, to_np)
+from transformer_forward_gpt_b300 import binding as nc
+from transformer_forward_gpt_b300 import synth
+
+pytestmark = pytest.mark.gpu
+
+
+def _run(shape, B, T0, steps, path=nc.NC_DECODE_PERSISTENT, act=nc.NC_F16, tol=2e-2, seqs=None):
+    import torch
+    W = synth.make_weights(shape)
+    t_cap = T0 + steps
+    seqs = list(range(B)) if seqs is None else seqs
+    toks = synth.make_tokens(shape, B, t_cap)
+    full, ocache = O.prefill(shape, *oracle_weights(W), toks[seqs])
+    model = nc.Model(W, max_seq=t_cap, max_batch=B, act_dtype=act)
+    nc.nc_model_set_decode_path(model.handle, path)
+    cache = model.cache(B, t_cap)
+    poison_cache(cache)
+    tok_d = torch.from_numpy(toks).cuda()
+    lg = torch.empty(B, shape.vocab, device="cuda")
+    am = torch.empty(B, dtype=torch.int32, device="cuda")
+    nc.nc_prefill_last(model.handle, tok_d[:, :T0].contiguous(), B, T0, lg, am, cache.handle)
+    errs = []
+    idx = torch.tensor(seqs, device="cuda")
+    for j in range(steps):
+        nc.nc_decode_step(model.handle, tok_d[:, T0 + j].contiguous(), B, T0 + j, lg, am,
+                          cache.handle)
+        torch.cuda.synchronize()
+        ref = full[:, T0 + j]
+        errs.append(assert_close(to_np(lg[idx]), ref, tol, f"{shape.name} B{B} step {j}"))
+        argmax_agreement(am[idx].cpu().numpy(), ref, tol)
+    assert nc.nc_model_check(model.handle) == nc.NC_OK
+    check_cache(cache, ocache, shape, seqs, t_cap, tol)
+    cache.close()
+    model.close()
+    return max(errs)
+
+
+def _small(base, **kw):
+    return synth.with_changes(base, name=base.name + "_small", **kw)
+
+
+@pytest.mark.parametrize("B", [1, 5, 12, 20, 32])
+def test_batch_widths_mqa(cuda_device, B):
+    _run(_small(synth.D20_MQA, n_layer=2, vocab=1000), B, 45, 3)
+
+
+@pytest.mark.parametrize("kv", [10, 2])
+def test_gqa_and_mha(cuda_device, kv):
+    _run(_small(synth.D20, n_layer=2, vocab=1000, n_kv_head=kv), 6, 37, 3)
+
+
+def test_batch_above_32_runs_in_chunks(cuda_device):
+    _run(_small(synth.D20_MQA, n_layer=2, vocab=512), 45, 20, 2, seqs=[0, 31, 32, 44])
+
+
+def test_long_context_spans_ctas(cuda_device):
+    # 2 sequences x 1 KV head x 63 tiles: each (sequence, KV head) covers ~74 CTAs
+    _run(_small(synth.D20_MQA, n_layer=2, vocab=1000), 2, 1000, 3)
+
+
+@pytest.mark.parametrize("base", [synth.D12, synth.D26])
+def test_other_widths(cuda_device, base):
+    _run(_small(base, n_layer=2, vocab=768), 4, 70, 2)
+
+
+def test_bf16_storage(cuda_device):
+    _run(_small(synth.D20_MQA, n_layer=2, vocab=1000), 8, 50, 2, act=nc.NC_BF16, tol=6e-2)
+
+
+def test_paths_agree(cuda_device):
+    """The persistent path and the per-kernel path on the same inputs."""
+    shape = _small(synth.D20_MQA, n_layer=3, vocab=2048)
+    a = _run(shape, 7, 60, 3, path=nc.NC_DECODE_PERSISTENT)
+    b = _run(shape, 7, 60, 3, path=nc.NC_DECODE_KERNELS)
+    assert a < 2e-2 and b < 2e-2
+
+
+def test_many_steps_keep_barrier_state(cuda_device):
+    """Forty steps in a row: the grid barrier counter carries over between launches."""
+    _run(_small(synth.D20_MQA, n_layer=1, vocab=512), 3, 16, 40)

@@ -24,11 +24,12 @@ EXPORTS = (
     "nc_model_check", "nc_op_rmsnorm", "nc_op_gemm", "nc_op_attention_prefill",
     "nc_op_attention_decode_scratch_bytes", "nc_op_attention_decode", "nc_op_argmax",
     "nc_kv_cache_set_length", "nc_profile_begin", "nc_profile_end", "nc_launch_count",
-    "nc_op_attention_decode_noalloc",
+    "nc_op_attention_decode_noalloc", "nc_model_set_decode_path", "nc_decode_trace",
+    "nc_decode_trace_entries",
 )
 
 KERNEL_KINDS = ("embed", "norm", "qkv", "attn_prefill", "attn_decode", "oproj", "fc", "proj",
-                "lm_head", "argmax")
+                "lm_head", "argmax", "decode_step")
 
 
 class NcConfig(C.Structure):
@@ -94,6 +95,9 @@ def load(path: str = LIB_PATH):
         "nc_launch_count": (i64, []),
         "nc_op_attention_decode_noalloc": (C.c_int, [vp, vp, vp, vp, i32, i32, i32, i32, i32,
                                                      i32, C.c_int, vp]),
+        "nc_model_set_decode_path": (C.c_int, [vp, C.c_int]),
+        "nc_decode_trace": (C.c_int, [vp, vp, i32]),
+        "nc_decode_trace_entries": (i32, [C.POINTER(NcConfig)]),
     }
     for name, (res, args) in sig.items():
         f = getattr(lib, name)
@@ -203,6 +207,23 @@ def nc_prefill_last(model, tokens, B, T, logits_last, argmax_out, cache, stream=
 def nc_decode_step(model, tokens, B, pos, logits, argmax_out, cache, stream=None):
     _check(load().nc_decode_step(model, _ptr(tokens), B, pos, _ptr(logits), _ptr(argmax_out),
                                  cache, _stream(stream)), "nc_decode_step")
+
+
+NC_DECODE_AUTO, NC_DECODE_PERSISTENT, NC_DECODE_KERNELS = 0, 1, 2
+
+
+def nc_model_set_decode_path(model, path):
+    _check(load().nc_model_set_decode_path(model, path), "nc_model_set_decode_path")
+
+
+def nc_decode_trace(model, buf):
+    """buf: device uint64 (torch int64) tensor, or None to switch tracing off."""
+    _check(load().nc_decode_trace(model, _ptr(buf), 0 if buf is None else buf.numel()),
+           "nc_decode_trace")
+
+
+def nc_decode_trace_entries(cfg):
+    return load().nc_decode_trace_entries(C.byref(cfg))
 
 
 def nc_generate_host(model, prompt, B, T, steps, out_tokens, cache, stream=None):

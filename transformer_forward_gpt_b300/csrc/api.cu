@@ -10,6 +10,7 @@
 #include <vector>
 
 #include "common.cuh"
+#include "decode_fused.h"
 #include "nc_internal.h"
 #include "tc.h"
 
@@ -105,6 +106,25 @@ struct nc_model {
   size_t attn_scratch_bytes = 0;
   nc::TcModel* tc = nullptr;    // tensor-core state (16-bit models)
   void* wcopy = nullptr;        // weights converted to adt (when it differs from cfg.dtype)
+  // persistent decode step (16-bit path), set up on first use
+  int decode_path = NC_DECODE_AUTO;
+  int sms = 0;
+  nc::dec::Layout dlay{};
+  uint8_t* dpack = nullptr;     // weights in mma-fragment order
+  void* dws = nullptr;          // its scratch
+  float* d_qkv = nullptr;
+  float* d_hacc = nullptr;
+  float* d_ss = nullptr;
+  void* d_xnf = nullptr;
+  unsigned int* d_cnt = nullptr;
+  unsigned long long* d_amkey = nullptr;
+  unsigned int* d_amcnt = nullptr;
+  unsigned long long* d_bar = nullptr;
+  float* d_part = nullptr;      // partial softmax states (grown on demand)
+  size_t d_part_bytes = 0;
+  unsigned long long bar_base = 0;
+  unsigned long long* dec_trace = nullptr;   // caller's buffer (nc_decode_trace)
+  int32_t dec_trace_cap = 0;
   // measurement
   bool prof = false;
   std::vector<ProfRec> recs;
@@ -152,6 +172,8 @@ struct nc_kv_cache {
   bool owns = false;
   int32_t batch = 0, t_max = 0, len = 0;
   size_t layer_elems = 0;  // batch * Hkv * t_max * hd
+  bool maps = false;       // TMA views of K and V for the persistent decode step
+  CUtensorMap tmk, tmv;
 };
 
 extern "C" {
@@ -217,6 +239,9 @@ void nc_model_destroy(nc_model* m) {
   }
   for (auto e : m->event_pool) cudaEventDestroy(e);
   cudaFree(m->wcopy);
+  cudaFree(m->dpack);
+  cudaFree(m->dws);
+  cudaFree(m->d_part);
   cudaFree(m->ws);
   cudaFree(m->cos_tab);
   cudaFree(m->sin_tab);
@@ -480,8 +505,13 @@ nc_status run_blocks(nc_model* m, nc_kv_cache* c, int B, int rows_per_seq, int p
       nc::launch_attention_decode(m->q, dst.k_cache, dst.v_cache, m->att, B, H, Hkv, pos0 + 1,
                                   c->t_max, hd, dt, m->attn_scratch, s);
     } else if (tc) {
-      nc_status st = nc::tc_attention_prefill(m->q, dst.k_cache, dst.v_cache, m->att, B, H, Hkv,
-                                              rows_per_seq, c->t_max, dt, s);
+      const int64_t one_layer = (int64_t)c->batch * Hkv * c->t_max * hd;
+      nc_status st = nc::tc_attention_prefill_tc(m->q, dst.k_cache, dst.v_cache, m->att, B, H,
+                                                 Hkv, rows_per_seq, c->t_max, 1, one_layer, 0, dt,
+                                                 m->status, s);
+      if (st != NC_OK)   // descriptors could not be built: the mma.sync kernel needs none
+        st = nc::tc_attention_prefill(m->q, dst.k_cache, dst.v_cache, m->att, B, H, Hkv,
+                                      rows_per_seq, c->t_max, dt, s);
       if (st != NC_OK) return st;
     } else {
       nc::launch_attention_prefill_simt(m->q, dst.k_cache, dst.v_cache, m->att, B, H, Hkv,
@@ -562,6 +592,160 @@ nc_status prefill_common(nc_model* m, const int32_t* tokens, int32_t B, int32_t 
   return NC_OK;
 }
 
+
+// ------------------------------------------------ persistent decode step
+bool decode_fused_applies(const nc_model* m) {
+  const nc_config& c = m->cfg;
+  return m->adt != NC_F32 &&
+         nc::dec::supported(c.d_model, c.n_head, c.n_kv_head, c.d_mlp, c.head_dim) &&
+         c.vocab % 4 == 0;
+}
+
+nc_status decode_fused_init(nc_model* m, cudaStream_t s) {
+  if (m->dpack) return NC_OK;
+  const nc_config& c = m->cfg;
+  int dev = 0;
+  NC_CUDA(cudaGetDevice(&dev));
+  NC_CUDA(cudaDeviceGetAttribute(&m->sms, cudaDevAttrMultiProcessorCount, dev));
+  int coop = 0;
+  NC_CUDA(cudaDeviceGetAttribute(&coop, cudaDevAttrCooperativeLaunch, dev));
+  NC_CHECK(coop, NC_ERR_UNSUPPORTED, "device has no cooperative launch");
+  m->dlay = nc::dec::layout_of(c.n_layer, c.d_model, c.n_head, c.n_kv_head, c.d_mlp, c.vocab);
+  const int K = nc::dec::kMaxTok;
+  size_t off = 0;
+  auto carve = [&](size_t bytes) {
+    size_t o = off;
+    off = round_up(off + bytes, 256);
+    return o;
+  };
+  const size_t o_qkv = carve((size_t)2 * K * m->dlay.nqkv_pad * 4),
+               o_h = carve((size_t)K * c.d_mlp * 4), o_ss = carve((size_t)2 * c.n_layer * K * 4),
+               o_xnf = carve((size_t)c.d_model * 64), o_cnt = carve((size_t)K * c.n_kv_head * 4),
+               o_key = carve((size_t)K * 8), o_amc = carve((size_t)K * 4), o_bar = carve(8);
+  if (cudaMalloc(&m->dws, off) != cudaSuccess) {
+    cudaGetLastError();
+    m->dws = nullptr;
+    set_err("decode scratch allocation of %zu bytes failed", off);
+    return NC_ERR_OOM;
+  }
+  NC_CUDA(cudaMemset(m->dws, 0, off));
+  char* b = static_cast<char*>(m->dws);
+  m->d_qkv = reinterpret_cast<float*>(b + o_qkv);
+  m->d_hacc = reinterpret_cast<float*>(b + o_h);
+  m->d_ss = reinterpret_cast<float*>(b + o_ss);
+  m->d_xnf = b + o_xnf;
+  m->d_cnt = reinterpret_cast<unsigned int*>(b + o_cnt);
+  m->d_amkey = reinterpret_cast<unsigned long long*>(b + o_key);
+  m->d_amcnt = reinterpret_cast<unsigned int*>(b + o_amc);
+  m->d_bar = reinterpret_cast<unsigned long long*>(b + o_bar);
+  m->bar_base = 0;
+  uint8_t* pack = nullptr;
+  if (cudaMalloc(&pack, (size_t)m->dlay.total_bytes) != cudaSuccess) {
+    cudaGetLastError();
+    set_err("packed decode weights: allocation of %lld bytes failed",
+            (long long)m->dlay.total_bytes);
+    return NC_ERR_OOM;
+  }
+  nc::dec::PackSrc src{c.n_layer, c.d_model, c.n_head, c.n_kv_head, c.d_mlp, c.vocab,
+                       m->wq.data(), m->wk.data(), m->wv.data(), m->wo.data(),
+                       m->w_fc.data(), m->w_proj.data(), m->lm_head};
+  nc_status st = nc::dec::pack_weights(src, m->adt == NC_F16, pack, s);
+  if (st != NC_OK) {
+    cudaFree(pack);
+    set_err("packing the decode weights failed");
+    return st;
+  }
+  m->dpack = pack;
+  return NC_OK;
+}
+
+nc_status decode_fused(nc_model* m, const int32_t* tokens, int32_t B, int32_t pos, float* logits,
+                       int32_t* argmax_out, nc_kv_cache* c, cudaStream_t s) {
+  nc_status st = decode_fused_init(m, s);
+  if (st != NC_OK) return st;
+  const nc_config& cfg = m->cfg;
+  const bool f16 = m->adt == NC_F16;
+  if (!c->maps) {
+    const uint64_t rows = (uint64_t)cfg.n_layer * c->batch * cfg.n_kv_head * c->t_max;
+    NC_CHECK(nc::dec::make_cache_map(&c->tmk, c->k, rows, f16) &&
+                 nc::dec::make_cache_map(&c->tmv, c->v, rows, f16),
+             NC_ERR_CUDA, "TMA descriptors of the KV cache could not be built");
+    c->maps = true;
+  }
+  const int G = cfg.n_head / cfg.n_kv_head;
+  ProfScope ps(m, NC_K_DECODE_STEP, s);
+  for (int b0 = 0; b0 < B; b0 += nc::dec::kMaxTok) {
+    const int Bc = std::min(nc::dec::kMaxTok, B - b0);
+    nc::dec::Params p{};
+    p.B = Bc;
+    p.b_off = b0;
+    p.pos = pos;
+    p.cache_batch = c->batch;
+    p.t_max = c->t_max;
+    p.L = cfg.n_layer;
+    p.d = cfg.d_model;
+    p.H = cfg.n_head;
+    p.Hkv = cfg.n_kv_head;
+    p.F = cfg.d_mlp;
+    p.V = cfg.vocab;
+    p.vpad = m->dlay.vpad;
+    p.nqkv = m->dlay.nqkv;
+    p.nqkv_pad = m->dlay.nqkv_pad;
+    p.attn_slots = nc::dec::attn_slots_needed(Bc, cfg.n_kv_head, pos, m->sms);
+    p.eps = cfg.rms_eps;
+    p.scale_log2 = (float)(1.4426950408889634 / sqrt((double)cfg.head_dim));
+    p.layer_bytes = m->dlay.layer_bytes;
+    p.off_o = m->dlay.off_o;
+    p.off_fc = m->dlay.off_fc;
+    p.off_proj = m->dlay.off_proj;
+    p.tokens = tokens + b0;
+    p.argmax_out = argmax_out ? argmax_out + b0 : nullptr;
+    p.wte = m->wte;
+    p.wpack = m->dpack;
+    p.cos_tab = m->cos_tab;
+    p.sin_tab = m->sin_tab;
+    p.k_cache = c->k;
+    p.v_cache = c->v;
+    p.x = m->x;
+    p.qkv_acc = m->d_qkv;
+    p.hacc = m->d_hacc;
+    p.ss = m->d_ss;
+    p.att = m->att;
+    p.xnf = m->d_xnf;
+    p.logits = (logits ? logits : m->logits_tmp) + (size_t)b0 * cfg.vocab;
+    p.attn_count = m->d_cnt;
+    p.argmax_key = m->d_amkey;
+    p.argmax_count = m->d_amcnt;
+    p.bar_counter = m->d_bar;
+    p.bar_base = m->bar_base;
+    p.status = m->status;
+    p.abort = m->status + 1;
+    p.trace = (b0 == 0 && m->dec_trace &&
+               m->dec_trace_cap >= 2 * nc::dec::barriers_per_step(cfg.n_layer) + 2)
+                  ? m->dec_trace
+                  : nullptr;
+    const size_t part = (size_t)Bc * cfg.n_kv_head * p.attn_slots * G * (cfg.head_dim + 2) * 4;
+    if (part > m->d_part_bytes) {
+      // grows on the first calls of a larger shape only (the free waits for the device)
+      cudaFree(m->d_part);
+      m->d_part = nullptr;
+      m->d_part_bytes = 0;
+      const size_t want = part * 2;
+      if (cudaMalloc(&m->d_part, want) != cudaSuccess) {
+        cudaGetLastError();
+        m->d_part = nullptr;
+        set_err("decode attention scratch of %zu bytes failed", want);
+        return NC_ERR_OOM;
+      }
+      m->d_part_bytes = want;
+    }
+    p.attn_part = m->d_part;
+    st = nc::dec::launch_step(c->tmk, c->tmv, p, f16, cfg.dtype, m->sms, s);
+    if (st != NC_OK) return st;
+    m->bar_base += (unsigned long long)nc::dec::barriers_per_step(cfg.n_layer) * m->sms;
+  }
+  return NC_OK;
+}
 }  // namespace
 
 extern "C" {
@@ -613,6 +797,14 @@ nc_status nc_decode_step(nc_model* m, const int32_t* tokens, int32_t B, int32_t 
   NC_CHECK(pos >= 1, NC_ERR_INVALID_ARG, "decode needs a prefilled cache (pos >= 1)");
   NC_CHECK(pos + 1 <= c->t_max, NC_ERR_INVALID_ARG, "cache full (t_max %d)", c->t_max);
   cudaStream_t s = static_cast<cudaStream_t>(stream);
+  const bool fused_ok = decode_fused_applies(m);
+  NC_CHECK(fused_ok || m->decode_path != NC_DECODE_PERSISTENT, NC_ERR_UNSUPPORTED,
+           "the persistent decode step does not support this shape");
+  if (fused_ok && m->decode_path != NC_DECODE_KERNELS) {
+    nc_status st = decode_fused(m, tokens, B, pos, logits, argmax_out, c, s);
+    if (st == NC_OK) c->len = pos + 1;
+    return st;
+  }
   {
     ProfScope ps(m, NC_K_EMBED, s);
     nc::launch_embed_norm(tokens, m->wte, m->cfg.dtype, m->x, m->xn, m->adt, B, m->cfg.d_model,
@@ -652,6 +844,26 @@ nc_status nc_generate_host(nc_model* m, const int32_t* prompt, int32_t B, int32_
   NC_CUDA(cudaMemcpyAsync(out_tokens, m->gen_dev, sizeof(int32_t) * B * (steps + 1),
                           cudaMemcpyDeviceToHost, s));
   NC_CUDA(cudaStreamSynchronize(s));
+  return NC_OK;
+}
+
+nc_status nc_decode_trace(nc_model* m, uint64_t* dev_buf, int32_t capacity) {
+  NC_CHECK(m, NC_ERR_INVALID_ARG, "model is NULL");
+  NC_CHECK(!dev_buf || capacity > 0, NC_ERR_INVALID_ARG, "capacity must be positive");
+  m->dec_trace = reinterpret_cast<unsigned long long*>(dev_buf);
+  m->dec_trace_cap = dev_buf ? capacity : 0;
+  return NC_OK;
+}
+
+int32_t nc_decode_trace_entries(const nc_config* cfg) {
+  return cfg ? 2 * nc::dec::barriers_per_step(cfg->n_layer) + 2 : 0;
+}
+
+nc_status nc_model_set_decode_path(nc_model* m, nc_decode_path path) {
+  NC_CHECK(m, NC_ERR_INVALID_ARG, "model is NULL");
+  NC_CHECK(path == NC_DECODE_AUTO || path == NC_DECODE_PERSISTENT || path == NC_DECODE_KERNELS,
+           NC_ERR_INVALID_ARG, "unknown decode path %d", (int)path);
+  m->decode_path = path;
   return NC_OK;
 }
 
@@ -695,6 +907,10 @@ nc_status nc_model_check(nc_model* m, void* stream) {
   NC_CUDA(cudaMemcpy(&word, m->status, 4, cudaMemcpyDeviceToHost));
   NC_CUDA(cudaMemset(m->status, 0, 4));
   if (word & nc::ST_TIMEOUT) {
+    // a persistent step gave up: clear its abort word and barrier counter
+    NC_CUDA(cudaMemset(m->status + 1, 0, 4));
+    if (m->d_bar) NC_CUDA(cudaMemset(m->d_bar, 0, 8));
+    m->bar_base = 0;
     set_err("a kernel's bounded wait timed out (status 0x%x)", word);
     return NC_ERR_DEVICE_TIMEOUT;
   }
@@ -744,6 +960,10 @@ nc_status nc_op_attention_prefill(const void* q, const void* k, const void* v, v
   cudaStream_t s = static_cast<cudaStream_t>(stream);
   if (dtype == NC_BF16 || dtype == NC_F16) {
     NC_CHECK(hd == 128, NC_ERR_UNSUPPORTED, "16-bit attention needs head_dim 128");
+    const int64_t one_layer = (int64_t)B * Hkv * t_max * hd;
+    nc_status st = nc::tc_attention_prefill_tc(q, k, v, o, B, H, Hkv, T, t_max, 1, one_layer, 0,
+                                               dtype, nullptr, s);
+    if (st == NC_OK) return NC_OK;
     return nc::tc_attention_prefill(q, k, v, o, B, H, Hkv, T, t_max, dtype, s);
   }
   NC_CHECK(dtype == NC_F32, NC_ERR_INVALID_ARG, "bad dtype");

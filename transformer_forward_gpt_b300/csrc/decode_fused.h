@@ -1,0 +1,79 @@
+// Host interface of the persistent single-launch decode step (decode_fused.cu).
+#pragma once
+#include <cuda.h>
+#include <stdint.h>
+
+#include "nc_internal.h"
+
+namespace nc {
+namespace dec {
+
+constexpr int kMaxTok = 32;   // sequences per launch (larger batches run in chunks)
+
+// Byte layout of the packed decode weights: per layer [QKV | O | FC | PROJ],
+// then the LM head; each matrix in 8 KB units of 128 rows x 32 columns.
+struct Layout {
+  int nqkv, nqkv_pad, vpad;
+  int64_t off_o, off_fc, off_proj, layer_bytes, total_bytes;
+};
+
+struct PackSrc {
+  int L, d, H, Hkv, F, V;
+  const void* const* wq;
+  const void* const* wk;
+  const void* const* wv;
+  const void* const* wo;
+  const void* const* wfc;
+  const void* const* wproj;
+  const void* lm;
+};
+
+struct Params {
+  int B, b_off, pos, cache_batch, t_max;
+  int L, d, H, Hkv, F, V, vpad, nqkv, nqkv_pad;
+  int stages, act_bytes, attn_slots;
+  float eps, scale_log2;
+  int64_t layer_bytes, off_o, off_fc, off_proj;
+  const int32_t* tokens;      // [B]
+  int32_t* argmax_out;        // [B] or null
+  const void* wte;            // [V, d] in the model's weight type
+  const uint8_t* wpack;
+  const float* cos_tab;
+  const float* sin_tab;
+  void* k_cache;              // K of layer 0 (all layers follow), 16-bit
+  void* v_cache;
+  float* x;                   // [kMaxTok, d] residual
+  float* qkv_acc;             // [2][kMaxTok][nqkv_pad]
+  float* hacc;                // [kMaxTok][F]
+  float* ss;                  // [2 L][kMaxTok]
+  void* att;                  // [kMaxTok][H*128] 16-bit
+  void* xnf;                  // final-norm fragments [d/16][NT][32] x 8 bytes
+  float* logits;              // [B][V]
+  float* attn_part;           // partial softmax states
+  unsigned int* attn_count;   // [kMaxTok * Hkv]
+  unsigned long long* argmax_key;   // [kMaxTok]
+  unsigned int* argmax_count;       // [kMaxTok]
+  unsigned long long* bar_counter;  // grid barrier arrivals (monotonic)
+  unsigned long long bar_base;      // its value when this launch starts
+  uint32_t* status;
+  uint32_t* abort;
+  // optional: %globaltimer of CTA 0 at start, at each grid barrier (arrival,
+  // exit) and at the end: 2 * barriers + 2 entries
+  unsigned long long* trace;
+};
+
+Layout layout_of(int L, int d, int H, int Hkv, int F, int V);
+int64_t packed_bytes(int N, int K);
+bool supported(int d, int H, int Hkv, int F, int hd);
+nc_status pack_weights(const PackSrc& src, bool half, uint8_t* out, cudaStream_t s);
+int attn_slots_needed(int B, int Hkv, int pos, int P);
+// TMA view of a KV array (all layers) as [rows, 128] 16-bit values.
+bool make_cache_map(CUtensorMap* map, void* base, uint64_t rows, bool half);
+// Grid barriers one launch passes (its arrivals are that times the grid size).
+inline int barriers_per_step(int L) { return 5 * L + 3; }
+// Enqueues one step for p.B <= kMaxTok sequences on `sms` CTAs (cooperative launch).
+nc_status launch_step(const CUtensorMap& tk, const CUtensorMap& tv, Params p, bool half,
+                      nc_dtype wdt, int sms, cudaStream_t s);
+
+}  // namespace dec
+}  // namespace nc

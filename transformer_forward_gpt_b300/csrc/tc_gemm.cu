@@ -56,7 +56,9 @@ struct TileCfg {
   static constexpr int kBoxRowsB = BN < 128 ? BN : 128;
   static constexpr int kTmemCols = (2 * BN <= 32) ? 32 : (2 * BN <= 64) ? 64 : (2 * BN <= 128) ? 128
                                    : (2 * BN <= 256) ? 256 : 512;
-  static constexpr size_t kSmemBytes = (size_t)kStages * kStageBytes + 1024 + 256;
+  static constexpr int kEpiStride = 36;   // floats per staged row (16-byte aligned, conflict-free)
+  static constexpr int kEpiBytes = 4 * 32 * kEpiStride * 4;
+  static constexpr size_t kSmemBytes = (size_t)kStages * kStageBytes + 1024 + 256 + kEpiBytes;
 };
 
 __device__ __forceinline__ const CUtensorMap* pick_map(const CUtensorMap* m0, const CUtensorMap* m1,
@@ -77,52 +79,79 @@ __device__ __forceinline__ const CUtensorMap* pick_map(const CUtensorMap* m0, co
 // ----------------------------------------------------------------- epilogues
 // Each thread holds row `row` of the tile; taddr points at its TMEM lane and
 // the accumulator's first column. tcgen05.ld is warp-collective, so every lane
-// runs the loads and only the stores are predicated on the row being valid.
+// runs the loads. A thread-per-row store would touch 32 rows per warp
+// instruction, so each 32-column chunk goes through the warp's staging area
+// (32 rows x kEpiStride floats) and is written row by row: 8 lanes cover the
+// 128 bytes of one fp32 row chunk (4 lanes the 64 bytes of a 16-bit one).
 template <int BN, class T16>
-__device__ __forceinline__ void epi_store_rows(const GemmArgs& p, uint32_t taddr, int row, int nb,
-                                               int mode) {
-  const bool valid = row < p.M;
+__device__ __forceinline__ void epi_store_rows(const GemmArgs& p, uint32_t taddr, float* stage,
+                                               int row0, int nb, int mode) {
+  constexpr int S = TileCfg<BN>::kEpiStride;
+  const int lane = threadIdx.x % 32;
 #pragma unroll 1
   for (int c = 0; c < BN / 32; ++c) {
     float v[32];
     tmem_ld32_sync(taddr + c * 32, v);
     const int n0 = nb * BN + c * 32;
-    if (!valid || n0 >= p.N) continue;
-    if (mode == EPI_F32) {
-      float* dst = p.out_f32 + (int64_t)row * p.ldo + n0;
+    if (n0 >= p.N) continue;   // uniform across the warp
+    if (mode == EPI_RELU2) {
 #pragma unroll
-      for (int i = 0; i < 8; ++i)
-        if (n0 + 4 * i < p.N)
-          st_global_cs_v4(dst + 4 * i, make_uint4(__float_as_uint(v[4 * i]), __float_as_uint(v[4 * i + 1]),
-                                                  __float_as_uint(v[4 * i + 2]), __float_as_uint(v[4 * i + 3])));
-    } else if (mode == EPI_RESID) {
-      float* dst = p.out_f32 + (int64_t)row * p.ldo + n0;
-#pragma unroll
-      for (int i = 0; i < 8; ++i)
-        if (n0 + 4 * i < p.N) {
-          float4 x = *reinterpret_cast<float4*>(dst + 4 * i);
-          x.x += v[4 * i];
-          x.y += v[4 * i + 1];
-          x.z += v[4 * i + 2];
-          x.w += v[4 * i + 3];
-          *reinterpret_cast<float4*>(dst + 4 * i) = x;
-        }
-    } else {  // EPI_RELU2
-      T16* dst = reinterpret_cast<T16*>(p.out_16) + (int64_t)row * p.ldo + n0;
-#pragma unroll
-      for (int i = 0; i < 4; ++i)
-        if (n0 + 8 * i < p.N) {
-          float a[8];
-#pragma unroll
-          for (int j = 0; j < 8; ++j) {
-            const float r = fmaxf(v[8 * i + j], 0.f);
-            a[j] = r * r;
-          }
-          *reinterpret_cast<uint4*>(dst + 8 * i) =
-              make_uint4(pack2<T16>(a[0], a[1]), pack2<T16>(a[2], a[3]), pack2<T16>(a[4], a[5]),
-                         pack2<T16>(a[6], a[7]));
-        }
+      for (int j = 0; j < 32; ++j) {
+        const float r = fmaxf(v[j], 0.f);
+        v[j] = r * r;
+      }
     }
+#pragma unroll
+    for (int i = 0; i < 8; ++i)
+      *reinterpret_cast<float4*>(stage + lane * S + 4 * i) =
+          make_float4(v[4 * i], v[4 * i + 1], v[4 * i + 2], v[4 * i + 3]);
+    __syncwarp();
+    if (mode == EPI_RELU2) {
+      // 4 lanes per row (8 values each), 8 rows per pass
+#pragma unroll
+      for (int it = 0; it < 4; ++it) {
+        const int r = it * 8 + lane / 4, cc = (lane % 4) * 8;
+        const int grow = row0 + r, gcol = n0 + cc;
+        if (grow < p.M && gcol < p.N) {
+          const float4 a = *reinterpret_cast<const float4*>(stage + r * S + cc);
+          const float4 b = *reinterpret_cast<const float4*>(stage + r * S + cc + 4);
+          T16* dst = reinterpret_cast<T16*>(p.out_16) + (int64_t)grow * p.ldo + gcol;
+          *reinterpret_cast<uint4*>(dst) = make_uint4(pack2<T16>(a.x, a.y), pack2<T16>(a.z, a.w),
+                                                      pack2<T16>(b.x, b.y), pack2<T16>(b.z, b.w));
+        }
+      }
+    } else {
+      // 8 lanes per row (4 values each), 4 rows per pass. The residual rows are
+      // all loaded before any store so that the eight loads overlap.
+      const int cc = (lane % 8) * 4, gcol = n0 + cc;
+      float4 x[8];
+      if (mode == EPI_RESID) {
+#pragma unroll
+        for (int it = 0; it < 8; ++it) {
+          const int grow = row0 + it * 4 + lane / 8;
+          x[it] = (grow < p.M && gcol < p.N)
+                      ? __ldcg(reinterpret_cast<const float4*>(p.out_f32 + (int64_t)grow * p.ldo + gcol))
+                      : make_float4(0.f, 0.f, 0.f, 0.f);
+        }
+      }
+#pragma unroll
+      for (int it = 0; it < 8; ++it) {
+        const int r = it * 4 + lane / 8;
+        const int grow = row0 + r;
+        if (grow < p.M && gcol < p.N) {
+          const float4 a = *reinterpret_cast<const float4*>(stage + r * S + cc);
+          float* dst = p.out_f32 + (int64_t)grow * p.ldo + gcol;
+          if (mode == EPI_RESID) {
+            *reinterpret_cast<float4*>(dst) =
+                make_float4(x[it].x + a.x, x[it].y + a.y, x[it].z + a.z, x[it].w + a.w);
+          } else {
+            st_global_cs_v4(dst, make_uint4(__float_as_uint(a.x), __float_as_uint(a.y),
+                                            __float_as_uint(a.z), __float_as_uint(a.w)));
+          }
+        }
+      }
+    }
+    __syncwarp();
   }
 }
 
@@ -243,6 +272,7 @@ __global__ void __launch_bounds__(192, 1)
   uint64_t* tempty = tfull + 2;  // [2] accumulator drained by the epilogue
   uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(tempty + 2);
   volatile int* abort_flag = reinterpret_cast<volatile int*>(tmem_slot + 1);
+  float* epi_stage = reinterpret_cast<float*>(smem + S * C::kStageBytes + 256);
 
   const int warp = threadIdx.x / 32, lane = threadIdx.x % 32;
   if (threadIdx.x == 0) {
@@ -387,7 +417,8 @@ __global__ void __launch_bounds__(192, 1)
       else if (EPI == EPI_SWAP)
         epi_swap<BN>(p, taddr, row, nb, ks);
       else
-        epi_store_rows<BN, T16>(p, taddr, row, nb, EPI);
+        epi_store_rows<BN, T16>(p, taddr, epi_stage + quarter * 32 * C::kEpiStride,
+                                mb * 128 + quarter * 32, nb, EPI);
       tc_fence_before();
       __syncwarp();
       if (lane == 0) mbar_arrive(&tempty[acc]);
