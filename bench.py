@@ -254,6 +254,21 @@ def run_ours(args):
     clocks = clk.summary()
 
     if profiling_aid:
+        # not a bench line: a plain summary for profiling runs
+        if rank == 0:
+            K = args.steps
+            msg = f"profiling aid: prefill {pre_ms / K:.3f} ms/step (B{Bp}xT{Tp})"
+            if args.phase != "prefill":
+                msg += f", decode {dec_ms / K / steps * 1e3:.1f} us/token-step (B{Bd})"
+            print(msg, flush=True)
+            for m, name in ((mp, "prefill"), (md, "decode")):
+                if m is None:
+                    continue
+                nc.nc_profile_begin(m.handle)
+                (prefill_phase if name == "prefill" else decode_phase)()
+                prof = nc.nc_profile_end(m.handle, stream)
+                print("  " + name + ": " + ", ".join(f"{k} {v[0]:.3f} ms" for k, v in prof.items()
+                                                     if v[1]), flush=True)
         return
     # per-kernel-class device time: one more step with the library's event pairs on
     nc.nc_profile_begin(mp.handle)

@@ -720,11 +720,12 @@ nc_status decode_fused(nc_model* m, const int32_t* tokens, int32_t B, int32_t po
     p.bar_base = m->bar_base;
     p.status = m->status;
     p.abort = m->status + 1;
-    p.trace = (b0 == 0 && m->dec_trace &&
-               m->dec_trace_cap >= 2 * nc::dec::barriers_per_step(cfg.n_layer) + 2)
+    p.nbar = nc::dec::barriers_per_step(cfg.n_layer);
+    p.trace = (b0 == 0 && m->dec_trace && m->dec_trace_cap >= nc::dec::trace_entries(cfg.n_layer))
                   ? m->dec_trace
                   : nullptr;
-    const size_t part = (size_t)Bc * cfg.n_kv_head * p.attn_slots * G * (cfg.head_dim + 2) * 4;
+    p.rec_stride = (G * (cfg.head_dim + 2) + 3) / 4 * 4;
+    const size_t part = (size_t)Bc * cfg.n_kv_head * p.attn_slots * p.rec_stride * 4;
     if (part > m->d_part_bytes) {
       // grows on the first calls of a larger shape only (the free waits for the device)
       cudaFree(m->d_part);
@@ -856,7 +857,7 @@ nc_status nc_decode_trace(nc_model* m, uint64_t* dev_buf, int32_t capacity) {
 }
 
 int32_t nc_decode_trace_entries(const nc_config* cfg) {
-  return cfg ? 2 * nc::dec::barriers_per_step(cfg->n_layer) + 2 : 0;
+  return cfg ? nc::dec::trace_entries(cfg->n_layer) : 0;
 }
 
 nc_status nc_model_set_decode_path(nc_model* m, nc_decode_path path) {

@@ -16,11 +16,17 @@
 // on almost every tile; the final O / l is the same either way. Scores of tile
 // j+1 are computed while the softmax of tile j runs.
 #include <math.h>
+#include <stdlib.h>
 
 #include "common.cuh"
 #include "tc.h"
 
 namespace nc {
+
+nc_status attn2_launch(const CUtensorMap& mq, const CUtensorMap& mk, const CUtensorMap& mv,
+                       void* o, int B, int H, int Hkv, int T, bool half, uint32_t* status,
+                       cudaStream_t s);
+
 namespace {
 
 constexpr int kHd = 128;
@@ -100,14 +106,16 @@ __global__ void __launch_bounds__(192, 1)
                                              ~uintptr_t(1023));
   uint64_t* bars = reinterpret_cast<uint64_t*>(smem + kOffBar);
   uint64_t* q_full = bars;          // 1
-  uint64_t* kv_full = bars + 1;     // 2
-  uint64_t* kv_empty = bars + 3;    // 2
-  uint64_t* s_full = bars + 5;      // 2
-  uint64_t* s_free = bars + 7;      // 2 (4 softmax warps)
-  uint64_t* p_full = bars + 9;      // 1 (4 softmax warps)
-  uint64_t* o_done = bars + 10;     // 1 (one commit per P V)
-  uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(bars + 12);
-  volatile int* abort_flag = reinterpret_cast<volatile int*>(bars + 13);
+  uint64_t* k_full = bars + 1;      // 2
+  uint64_t* k_empty = bars + 3;     // 2 (freed once S of the tile is done)
+  uint64_t* v_full = bars + 5;      // 2
+  uint64_t* v_empty = bars + 7;     // 2 (freed once P V of the tile is done)
+  uint64_t* s_full = bars + 9;      // 2
+  uint64_t* s_free = bars + 11;     // 2 (4 softmax warps)
+  uint64_t* p_full = bars + 13;     // 1 (4 softmax warps)
+  uint64_t* o_done = bars + 14;     // 1 (one commit per P V)
+  uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(bars + 16);
+  volatile int* abort_flag = reinterpret_cast<volatile int*>(bars + 17);
 
   // heaviest query tiles first
   const int per_qt = a.B * a.H;
@@ -121,8 +129,10 @@ __global__ void __launch_bounds__(192, 1)
   if (threadIdx.x == 0) {
     mbar_init(q_full, 1);
     for (int i = 0; i < 2; ++i) {
-      mbar_init(&kv_full[i], 1);
-      mbar_init(&kv_empty[i], 1);
+      mbar_init(&k_full[i], 1);
+      mbar_init(&k_empty[i], 1);
+      mbar_init(&v_full[i], 1);
+      mbar_init(&v_empty[i], 1);
       mbar_init(&s_full[i], 1);
       mbar_init(&s_free[i], 4);
     }
@@ -151,25 +161,35 @@ __global__ void __launch_bounds__(192, 1)
       tma_load_3d(smem + kOffQ + kHalf, &tmQ, q_full, 64, qt * kBq, bh);
       const int bg = b * a.Hkv + g;
       int issued = 0;
+      int issued_k = 0, issued_v = 0;
       for (int j = 0; j < n_kt; ++j) {
         const int st = j & 1;
-        if (!mbar_wait(&kv_empty[st], ((j >> 1) & 1) ^ 1, a.status)) {
+        const uint32_t par = ((j >> 1) & 1) ^ 1;
+        if (!mbar_wait(&k_empty[st], par, a.status)) {
           *abort_flag = 1;
           break;
         }
-        mbar_arrive_expect_tx(&kv_full[st], 2 * kTile);
         uint8_t* kd = smem + kOffK + st * kTile;
+        mbar_arrive_expect_tx(&k_full[st], kTile);
+        tma_load_4d(kd, &tmK, &k_full[st], 0, j * kBk, bg, layer);
+        tma_load_4d(kd + kHalf, &tmK, &k_full[st], 64, j * kBk, bg, layer);
+        ++issued_k;
+        if (!mbar_wait(&v_empty[st], par, a.status)) {
+          *abort_flag = 1;
+          break;
+        }
         uint8_t* vd = smem + kOffV + st * kTile;
-        tma_load_4d(kd, &tmK, &kv_full[st], 0, j * kBk, bg, layer);
-        tma_load_4d(kd + kHalf, &tmK, &kv_full[st], 64, j * kBk, bg, layer);
-        tma_load_4d(vd, &tmV, &kv_full[st], 0, j * kBk, bg, layer);
-        tma_load_4d(vd + kHalf, &tmV, &kv_full[st], 64, j * kBk, bg, layer);
-        ++issued;
+        mbar_arrive_expect_tx(&v_full[st], kTile);
+        tma_load_4d(vd, &tmV, &v_full[st], 0, j * kBk, bg, layer);
+        tma_load_4d(vd + kHalf, &tmV, &v_full[st], 64, j * kBk, bg, layer);
+        ++issued_v;
       }
       // copies in flight must land before shared memory is released
       mbar_wait(q_full, 0, a.status);
-      for (int j = (issued > 2 ? issued - 2 : 0); j < issued; ++j)
-        mbar_wait(&kv_full[j & 1], (j >> 1) & 1, a.status);
+      for (int j = (issued_k > 2 ? issued_k - 2 : 0); j < issued_k; ++j)
+        mbar_wait(&k_full[j & 1], (j >> 1) & 1, a.status);
+      for (int j = (issued_v > 2 ? issued_v - 2 : 0); j < issued_v; ++j)
+        mbar_wait(&v_full[j & 1], (j >> 1) & 1, a.status);
     }
   } else if (warp == 1) {
     if (lane == 0) {
@@ -180,7 +200,9 @@ __global__ void __launch_bounds__(192, 1)
       bool ok = mbar_wait(q_full, 0, a.status);
       auto pv = [&](int jj) -> bool {
         // O (+)= P V_jj once the softmax has written P_jj
-        if (!mbar_wait(p_full, jj & 1, a.status)) return false;
+        if (!mbar_wait(p_full, jj & 1, a.status) ||
+            !mbar_wait(&v_full[jj & 1], (jj >> 1) & 1, a.status))
+          return false;
         tc_fence_after();
         const uint32_t sV = smem_u32(smem + kOffV + (jj & 1) * kTile);
 #pragma unroll
@@ -191,12 +213,12 @@ __global__ void __launch_bounds__(192, 1)
           mma_f16kind_ss(tmem + kColO, da, db, kIdO, (jj > 0 || kk > 0) ? 1u : 0u);
         }
         mma_commit(o_done);
-        mma_commit(&kv_empty[jj & 1]);
+        mma_commit(&v_empty[jj & 1]);
         return true;
       };
       for (int j = 0; j < n_kt && ok; ++j) {
         const int st = j & 1;
-        if (!mbar_wait(&kv_full[st], (j >> 1) & 1, a.status) ||
+        if (!mbar_wait(&k_full[st], (j >> 1) & 1, a.status) ||
             !mbar_wait(&s_free[st], ((j >> 1) & 1) ^ 1, a.status)) {
           ok = false;
           break;
@@ -210,6 +232,7 @@ __global__ void __launch_bounds__(192, 1)
           mma_f16kind_ss(tmem + kColS0 + st * 128, da, db, kIdS, kk > 0 ? 1u : 0u);
         }
         mma_commit(&s_full[st]);
+        mma_commit(&k_empty[st]);
         if (j >= 1 && !pv(j - 1)) {
           ok = false;
           break;
@@ -232,39 +255,34 @@ __global__ void __launch_bounds__(192, 1)
       ok = __all_sync(0xffffffffu, mbar_wait(&s_full[st], (j >> 1) & 1, a.status));
       if (!ok) break;
       tc_fence_after();
-      float s[128];
-#pragma unroll
-      for (int c = 0; c < 4; ++c) {
-        float v[32];
-        tmem_ld32_sync(tmem + lane_base + kColS0 + st * 128 + c * 32, v);
-#pragma unroll
-        for (int i = 0; i < 32; ++i) s[c * 32 + i] = v[i];
-      }
-      tc_fence_before();
-      __syncwarp();
-      if (lane == 0) mbar_arrive(&s_free[st]);
-      // scale, causal mask on the diagonal tile, row max
-      float mx = -INFINITY;
+      // the score row in one 128-column TMEM load; scale, causal mask, row max
+      const uint32_t s_col = tmem + lane_base + kColS0 + st * 128;
       const bool diag = j == qt;
+      const int kmax = qpos - j * kBk;   // keys i > kmax are masked on the diagonal tile
+      float sv[128];
+      tmem_ld128_sync(s_col, sv);
+      float mx = -INFINITY;
 #pragma unroll
       for (int i = 0; i < 128; ++i) {
-        float v = s[i] * a.scale_log2;
-        if (diag && j * kBk + i > qpos) v = -INFINITY;
-        s[i] = v;
-        mx = fmaxf(mx, v);
+        sv[i] = (diag && i > kmax) ? -INFINITY : sv[i] * a.scale_log2;
+        mx = fmaxf(mx, sv[i]);
       }
       // raise the reference only when the max outgrows it by 2^8
       const bool raise = mx > m_ref + 8.f;
       const float m_new = raise ? mx : m_ref;
       const float corr = raise ? exp2f(m_ref - m_new) : 1.f;   // 0 on the first tile
+      // p = 2^(s - m) packed to 16 bits in registers, row sum
       float psum = 0.f;
       uint32_t pk[64];
 #pragma unroll
       for (int i = 0; i < 64; ++i) {
-        const float p0 = exp2f(s[2 * i] - m_new), p1 = exp2f(s[2 * i + 1] - m_new);
+        const float p0 = exp2f(sv[2 * i] - m_new), p1 = exp2f(sv[2 * i + 1] - m_new);
         psum += p0 + p1;
         pk[i] = pack2<T16>(p0, p1);
       }
+      tc_fence_before();
+      __syncwarp();
+      if (lane == 0) mbar_arrive(&s_free[st]);
       l_sum = l_sum * corr + psum;
       m_ref = m_new;
       // P V of the previous tile must be done before P is overwritten or O touched
@@ -374,6 +392,16 @@ bool make_rows_map(CUtensorMap* map, const void* base, bool half, int rank, uint
 // Status word of calls made without a model (bounded-wait timeouts).
 __device__ uint32_t g_attn_status;
 
+// The two-query-tile kernel (attn_tc2.cu) when NC_ATTN_V2=1 (measurement).
+bool use_attn_v2() {
+  static int v = -1;
+  if (v < 0) {
+    const char* e = getenv("NC_ATTN_V2");
+    v = (e && e[0] == '1') ? 1 : 0;
+  }
+  return v == 1;
+}
+
 }  // namespace
 
 // q [B, H, T, 128]; K/V of layer `layer` at k + layer * layer_stride elements,
@@ -391,6 +419,12 @@ nc_status tc_attention_prefill_tc(const void* q, const void* k, const void* v, v
       !make_rows_map(&mv, v, half, 4, T, (uint64_t)B * Hkv, kv_rows_bytes, n_layers,
                      (uint64_t)layer_stride * 2))
     return NC_ERR_CUDA;
+  if (use_attn_v2()) {
+    if (!status && cudaGetSymbolAddress(reinterpret_cast<void**>(&status), g_attn_status) != cudaSuccess)
+      return NC_ERR_CUDA;
+    // the two-tile kernel reads K/V of one layer (layer coordinate 0)
+    if (n_layers == 1) return attn2_launch(mq, mk, mv, o, B, H, Hkv, T, half, status, s);
+  }
   AttnArgs a;
   a.B = B;
   a.H = H;

@@ -168,6 +168,7 @@ struct Shared {
   float* xpose;        // per-warp 16 x 32 transpose tiles
   uint8_t* sq;         // Q tile (16 x 128, swizzled)
   uint16_t* kvnew;     // new K row, new V row (16-bit)
+  float* ss_s;         // [kMaxTok] per-token partial sums of squares
   volatile int* flag;  // [0] abort seen, [1] last-arriver flag, [2] barrier ok
 };
 
@@ -177,6 +178,18 @@ __device__ __forceinline__ bool aborted(const Params& p) {
 __device__ __forceinline__ void raise_abort(const Params& p) {
   atomicOr(p.status, ST_TIMEOUT);
   atomicExch(p.abort, 1u);
+}
+
+// Trace mark m (0..3) of the phase that ends at grid barrier k: CTA 0, first
+// consumer thread, only while a trace buffer is set.
+__device__ __forceinline__ void trace_mark(const Params& p, int k, int m) {
+  if (p.trace && blockIdx.x == 0 && threadIdx.x == 32)
+    p.trace[2 * p.nbar + 2 + 5 * (k - 1) + m] = global_timer_ns();
+}
+// Producer mark: when CTA 0's producer starts issuing the loads of the phase
+// that ends at grid barrier k.
+__device__ __forceinline__ void trace_producer(const Params& p, int k) {
+  if (p.trace && blockIdx.x == 0) p.trace[2 * p.nbar + 2 + 5 * (k - 1) + 4] = global_timer_ns();
 }
 
 // Bounded wait on a ring barrier; false on timeout or abort.
@@ -361,16 +374,21 @@ __device__ void producer(const Params& p, Shared& sh, const CUtensorMap* tk, con
   Ring& r = sh.ring;
   const uint64_t pol = l2_policy_evict_first();
   bool ok = true;
-  int issued = 0;
   for (int l = 0; l < p.L && ok; ++l) {
+    const int k = 2 + 5 * l;   // grid barrier that ends this layer's QKV phase
+    trace_producer(p, k);
     produce_gemv(p, r, gemv_of(p, l, PH_QKV), pol, ok);
+    trace_producer(p, k + 1);
     produce_attn(p, r, tk, tv, l, pol, ok);
+    trace_producer(p, k + 2);
     produce_gemv(p, r, gemv_of(p, l, PH_O), pol, ok);
+    trace_producer(p, k + 3);
     produce_gemv(p, r, gemv_of(p, l, PH_FC), pol, ok);
+    trace_producer(p, k + 4);
     produce_gemv(p, r, gemv_of(p, l, PH_PROJ), pol, ok);
   }
+  trace_producer(p, 5 * p.L + 3);
   if (ok) produce_gemv(p, r, gemv_lm(p), pol, ok);
-  (void)issued;
   if (!ok) {
     // Let every copy already issued land before the CTA's shared memory goes
     // away: the latest fill of each stage completes its full barrier's phase.
@@ -390,21 +408,41 @@ __device__ void producer(const Params& p, Shared& sh, const CUtensorMap* tk, con
 // memory as mma B fragments: entry ((ks - ks0) * NT + nt) * 32 + lane holds the
 // two 32-bit registers of lane `lane` for tokens 8nt..8nt+7.
 template <int NT, class T16>
-__device__ void stage_act(const Params& p, const Shared& sh, const Gemv& g, int ks0, int ks1) {
-  // Each thread converts up to 8 entries per pass and issues all of their loads
-  // before the first use, so a pass costs one L2 round trip, not eight.
-  constexpr int kBatch = 8;
+__device__ void stage_act(const Params& p, const Shared& sh, const Gemv& g, int ks0, int ks1,
+                          int ss_c0, int ss_c1, int ks0b = 0, int ks1b = 0) {
+  // Entry i of the window holds lane (i % 32)'s B fragment of token tile
+  // (i / 32) % NT. A thread handles entries tid, tid + 256, ...; as NT divides 8,
+  // all of them belong to one token: tok = (warp % NT) * 8 + lane / 4. Each pass
+  // issues all of a thread's loads before their first use (one L2 round trip).
+  // For ACT_X32 the squares of the columns in [ss_c0, ss_c1) are summed in a
+  // register and added to g.ss_out; for ACT_H32 the token's norm scale is read
+  // once before the loads.
+  constexpr int kBatch = 12;
   uint2* dst = reinterpret_cast<uint2*>(sh.act);
   const int tid = threadIdx.x - 32;
-  const int n = (ks1 - ks0) * NT * 32;
+  const int lane = tid & 31;
+  const int tok = ((tid >> 5) % NT) * 8 + (lane >> 2);
+  const bool tok_ok = tok < p.B;
+  // entries of k steps [ks0, ks1) come first, then those of [ks0b, ks1b)
+  const int lenA = ks1 - ks0;
+  const int n = (lenA + (ks1b - ks0b)) * NT * 32;
+  auto ks_of = [&](int i) {
+    const int e = (i >> 5) / NT;
+    return e < lenA ? ks0 + e : ks0b + (e - lenA);
+  };
+  const bool want_ss = g.act_kind == ACT_X32 && g.ss_out && ss_c0 < ss_c1;
+  // the token's norm scale (ACT_H32) is loaded here and used after the first
+  // batch of loads is in flight
+  const float ss_tok = (g.act_kind == ACT_H32 && tok_ok) ? __ldcg(g.ss_in + tok) : 0.f;
+  float ssum = 0.f;
   for (int i0 = tid; i0 < n; i0 += 256 * kBatch) {
     if (g.act_kind == ACT_FRAG) {
-      const uint2* src = reinterpret_cast<const uint2*>(g.act) + (int64_t)ks0 * NT * 32;
+      const uint2* src = reinterpret_cast<const uint2*>(g.act);
       uint2 v[kBatch];
 #pragma unroll
       for (int u = 0; u < kBatch; ++u) {
         const int i = i0 + u * 256;
-        if (i < n) v[u] = __ldcg(src + i);
+        if (i < n) v[u] = __ldcg(src + ((int64_t)ks_of(i) * NT + ((i >> 5) % NT)) * 32 + (i & 31));
       }
 #pragma unroll
       for (int u = 0; u < kBatch; ++u) {
@@ -413,66 +451,63 @@ __device__ void stage_act(const Params& p, const Shared& sh, const Gemv& g, int 
       }
       continue;
     }
-    float2 a[kBatch], b[kBatch];
-    uint2 w[kBatch];
-    float sc[kBatch];
+    if (g.act_kind == ACT_A16) {
+      uint2 w[kBatch];
 #pragma unroll
-    for (int u = 0; u < kBatch; ++u) {
-      const int i = i0 + u * 256;
-      const int ln = i & 31;
-      const int nt = (i >> 5) % NT;
-      const int ks = ks0 + (i >> 5) / NT;
-      const int tok = nt * 8 + (ln >> 2);
-      const int kc = ks * 16 + 2 * (ln & 3);
-      a[u] = b[u] = make_float2(0.f, 0.f);
-      w[u] = make_uint2(0u, 0u);
-      sc[u] = 1.f;
-      if (i < n && tok < p.B) {
-        if (g.act_kind == ACT_A16) {
+      for (int u = 0; u < kBatch; ++u) {
+        const int i = i0 + u * 256;
+        const int kc = ks_of(i) * 16 + 2 * (lane & 3);
+        w[u] = make_uint2(0u, 0u);
+        if (i < n && tok_ok) {
           const uint32_t* src = reinterpret_cast<const uint32_t*>(
               static_cast<const T16*>(g.act) + (int64_t)tok * g.act_ld + kc);
           w[u].x = __ldcg(src);
           w[u].y = __ldcg(src + 4);
-        } else {
-          const float* src = static_cast<const float*>(g.act) + (int64_t)tok * g.act_ld + kc;
-          a[u] = __ldcg(reinterpret_cast<const float2*>(src));
-          b[u] = __ldcg(reinterpret_cast<const float2*>(src + 8));
-          if (g.act_kind == ACT_H32) sc[u] = __ldcg(g.ss_in + tok);
         }
       }
+#pragma unroll
+      for (int u = 0; u < kBatch; ++u)
+        if (i0 + u * 256 < n) dst[i0 + u * 256] = w[u];
+      continue;
     }
+    float4 v[kBatch];   // x[tok, kc], x[tok, kc + 1], x[tok, kc + 8], x[tok, kc + 9]
+#pragma unroll
+    for (int u = 0; u < kBatch; ++u) {
+      const int i = i0 + u * 256;
+      const int kc = ks_of(i) * 16 + 2 * (lane & 3);
+      v[u] = make_float4(0.f, 0.f, 0.f, 0.f);
+      if (i < n && tok_ok) {
+        const float* src = static_cast<const float*>(g.act) + (int64_t)tok * g.act_ld + kc;
+        const float2 a = __ldcg(reinterpret_cast<const float2*>(src));
+        const float2 b = __ldcg(reinterpret_cast<const float2*>(src + 8));
+        v[u] = make_float4(a.x, a.y, b.x, b.y);
+      }
+    }
+    const float rscale = rsqrtf(ss_tok / (float)p.d + p.eps);
 #pragma unroll
     for (int u = 0; u < kBatch; ++u) {
       const int i = i0 + u * 256;
       if (i >= n) continue;
-      if (g.act_kind != ACT_A16) {
-        if (g.act_kind == ACT_H32) {
-          const float r = rsqrtf(sc[u] / (float)p.d + p.eps);
-          float v0 = fmaxf(a[u].x * r, 0.f), v1 = fmaxf(a[u].y * r, 0.f);
-          float v2 = fmaxf(b[u].x * r, 0.f), v3 = fmaxf(b[u].y * r, 0.f);
-          a[u] = make_float2(v0 * v0, v1 * v1);
-          b[u] = make_float2(v2 * v2, v3 * v3);
-        }
-        w[u].x = pack2<T16>(a[u].x, a[u].y);
-        w[u].y = pack2<T16>(b[u].x, b[u].y);
+      float4 x = v[u];
+      if (want_ss && (i >> 5) / NT < lenA) {   // columns of the first range only
+        const int kc = ks_of(i) * 16 + 2 * (lane & 3);
+        if (kc >= ss_c0 && kc < ss_c1) ssum += x.x * x.x + x.y * x.y + x.z * x.z + x.w * x.w;
       }
-      dst[i] = w[u];
+      if (g.act_kind == ACT_H32) {
+        x.x = fmaxf(x.x * rscale, 0.f);
+        x.y = fmaxf(x.y * rscale, 0.f);
+        x.z = fmaxf(x.z * rscale, 0.f);
+        x.w = fmaxf(x.w * rscale, 0.f);
+        x = make_float4(x.x * x.x, x.y * x.y, x.z * x.z, x.w * x.w);
+      }
+      dst[i] = make_uint2(pack2<T16>(x.x, x.y), pack2<T16>(x.z, x.w));
     }
   }
-}
-
-// Adds sum_k x[tok, k]^2 over columns [c0, c1) into ss[tok] (warp per token).
-__device__ void add_sumsq(const Params& p, const float* x, int ld, int c0, int c1, float* ss) {
-  const int warp = threadIdx.x / 32 - 1, lane = threadIdx.x % 32;
-  for (int tok = warp; tok < p.B; tok += kCons) {
-    const float* row = x + (int64_t)tok * ld;
-    float s = 0.f;
-    for (int c = c0 + lane * 4; c < c1; c += 128) {
-      const float4 v = __ldcg(reinterpret_cast<const float4*>(row + c));
-      s += v.x * v.x + v.y * v.y + v.z * v.z + v.w * v.w;
-    }
-    s = warp_sum(s);
-    if (lane == 0) atomicAdd(ss + tok, s);
+  if (want_ss) {
+    // the four lanes of a quad hold the same token
+    ssum += __shfl_xor_sync(0xffffffffu, ssum, 1);
+    ssum += __shfl_xor_sync(0xffffffffu, ssum, 2);
+    if ((lane & 3) == 0 && tok_ok && ssum != 0.f) atomicAdd(g.ss_out + tok, ssum);
   }
 }
 
@@ -512,31 +547,54 @@ __device__ __forceinline__ void flush_rows(const Params& p, const Shared& sh, co
 }
 
 template <int NT, class T16>
-__device__ bool consume_gemv(const Params& p, Shared& sh, const Gemv& g) {
+__device__ bool consume_gemv(const Params& p, Shared& sh, const Gemv& g, int k) {
   const int warp = threadIdx.x / 32 - 1, lane = threadIdx.x % 32;
   Ring& r = sh.ring;
   int64_t u0, u1;
   const int64_t units = (int64_t)g.groups * g.kpairs;
   share(units, blockIdx.x, gridDim.x, u0, u1);
   if (u0 >= u1) return true;
-  // sum of squares of x over the columns of row group 0 this CTA covers
+  // The sum of squares of x over the columns of row group 0 this CTA covers is
+  // taken while staging that run (runs in row group 0 only start this CTA's range).
+  int ss_c0 = 0, ss_c1 = 0;
   if (g.ss_out && u0 < g.kpairs) {
-    const int c0 = (int)u0 * kUnitCols, c1 = (int)std::min<int64_t>(u1, g.kpairs) * kUnitCols;
-    add_sumsq(p, static_cast<const float*>(g.act), g.act_ld, c0, c1, g.ss_out);
+    ss_c0 = (int)u0 * kUnitCols;
+    ss_c1 = (int)std::min<int64_t>(u1, g.kpairs) * kUnitCols;
   }
-  // activation window [win0, win1) in k16 steps, staged on demand
+  // activation window [win0, win1) in k16 steps, staged on demand. A share of
+  // exactly two runs (the end of one row group, the start of the next) that fits
+  // is staged in one pass: run 1's k steps, then run 2's at offset `off2`.
   int win0 = 0, win1 = 0;
+  int two_b0 = -1, two_off = 0;   // run 2's first k step and its offset, if both staged
   const int cap = sh.act_ksteps;
+  {
+    const int kpa = (int)(u0 % g.kpairs);
+    const int64_t n1 = g.kpairs - kpa;   // units of run 1
+    const int64_t n2 = (u1 - u0) - n1;   // units of run 2
+    if (n1 > 0 && n2 > 0 && n2 <= g.kpairs && 2 * (n1 + n2) <= cap) {
+      bar_consumers();
+      trace_mark(p, k, 3);
+      win0 = 2 * kpa;
+      win1 = 2 * g.kpairs;
+      two_b0 = 0;
+      two_off = 2 * (int)n1;
+      stage_act<NT, T16>(p, sh, g, win0, win1, ss_c0, ss_c1, 0, 2 * (int)n2);
+      bar_consumers();
+      trace_mark(p, k, 0);
+    }
+  }
   int64_t u = u0;
   while (u < u1) {
     const int grp = (int)(u / g.kpairs);
     const int kp0 = (int)(u % g.kpairs);
     const int kp1 = (int)std::min<int64_t>(g.kpairs, kp0 + (u1 - u));
-    if (2 * kp0 < win0 || 2 * kp1 > win1) {
+    const bool second = two_b0 >= 0 && u > u0;   // run 2 of a two-run share
+    if (!second && (2 * kp0 < win0 || 2 * kp1 > win1)) {
       // Every warp is done with the old window (all warps walk the same units).
       // A later row group needs the same columns again: stage the whole K once
       // if it fits, else this run's columns.
       bar_consumers();
+      trace_mark(p, k, 3);
       if (u1 - u > g.kpairs && 2 * g.kpairs <= cap) {
         win0 = 0;
         win1 = 2 * g.kpairs;
@@ -544,39 +602,52 @@ __device__ bool consume_gemv(const Params& p, Shared& sh, const Gemv& g) {
         win0 = 2 * kp0;
         win1 = std::min(2 * kp1, win0 + cap);
       }
-      stage_act<NT, T16>(p, sh, g, win0, win1);
+      stage_act<NT, T16>(p, sh, g, win0, win1, ss_c0, ss_c1);
       bar_consumers();
+      trace_mark(p, k, 0);
     }
-    float acc[NT][4];
+    // two accumulator sets (even / odd k16 step) halve the mma dependency chain
+    float acc[NT][4], acc2[NT][4];
 #pragma unroll
-    for (int nt = 0; nt < NT; ++nt) acc[nt][0] = acc[nt][1] = acc[nt][2] = acc[nt][3] = 0.f;
+    for (int nt = 0; nt < NT; ++nt)
+#pragma unroll
+      for (int e = 0; e < 4; ++e) acc[nt][e] = acc2[nt][e] = 0.f;
     for (int kp = kp0; kp < kp1; ++kp) {
       const int ks = 2 * kp;
-      if (ks + 2 > win1) {   // run longer than the window: slide it
+      if (!second && ks + 2 > win1) {   // run longer than the window: slide it
         bar_consumers();
         win0 = ks;
         win1 = std::min(2 * kp1, win0 + cap);
-        stage_act<NT, T16>(p, sh, g, win0, win1);
+        stage_act<NT, T16>(p, sh, g, win0, win1, ss_c0, ss_c1);
         bar_consumers();
       }
       if (!ring_wait(&r.full[r.stage], r.parity, p)) return false;
       const uint8_t* st = r.base + (size_t)r.stage * kStage;
       const uint2* bf = reinterpret_cast<const uint2*>(sh.act);
-#pragma unroll
-      for (int kk = 0; kk < 2; ++kk) {
-        const uint4 a = *reinterpret_cast<const uint4*>(st + kk * 4096 + warp * 512 + lane * 16);
-        const int ksl = ks + kk - win0;
+      {
+        const uint4 a0 = *reinterpret_cast<const uint4*>(st + warp * 512 + lane * 16);
+        const uint4 a1 = *reinterpret_cast<const uint4*>(st + 4096 + warp * 512 + lane * 16);
+        const int ksl = second ? two_off + ks - two_b0 : ks - win0;
 #pragma unroll
         for (int nt = 0; nt < NT; ++nt) {
-          const uint2 b = bf[(ksl * NT + nt) * 32 + lane];
-          mma16816<T16>(acc[nt], a.x, a.y, a.z, a.w, b.x, b.y);
+          const uint2 b0 = bf[(ksl * NT + nt) * 32 + lane];
+          const uint2 b1 = bf[((ksl + 1) * NT + nt) * 32 + lane];
+          mma16816<T16>(acc[nt], a0.x, a0.y, a0.z, a0.w, b0.x, b0.y);
+          mma16816<T16>(acc2[nt], a1.x, a1.y, a1.z, a1.w, b1.x, b1.y);
         }
       }
       __syncwarp();
       if (lane == 0) mbar_arrive(&r.empty[r.stage]);
       r.advance();
     }
+    trace_mark(p, k, 1);
+#pragma unroll
+    for (int nt = 0; nt < NT; ++nt)
+#pragma unroll
+      for (int e = 0; e < 4; ++e) acc[nt][e] += acc2[nt][e];
     flush_rows<NT>(p, sh, g, grp * kUnitRows + warp * 16, acc);
+    trace_mark(p, k, 2);
+    if (grp == 0) ss_c0 = ss_c1 = 0;   // the columns are counted once
     u += kp1 - kp0;
   }
   return true;
@@ -614,7 +685,7 @@ __device__ __forceinline__ void st16(uint8_t* tile, int r, int col, float v) {
 }
 
 template <class T16>
-__device__ bool consume_attn(const Params& p, Shared& sh, int l) {
+__device__ bool consume_attn(const Params& p, Shared& sh, int l, int k) {
   const int warp = threadIdx.x / 32 - 1, lane = threadIdx.x % 32;
   const int tid = threadIdx.x - 32;
   const int gq = lane >> 2, tq = lane & 3;
@@ -636,55 +707,79 @@ __device__ bool consume_attn(const Params& p, Shared& sh, int l) {
     const int j0 = (int)(f % T16n);
     const int j1 = (int)std::min<int64_t>(T16n, j0 + (f1 - f));
     const int b = bg / p.Hkv, g = bg % p.Hkv;
-    const float rb = rsqrtf(__ldcg(ss_l + b) / (float)p.d + p.eps);
+    const float ssb = __ldcg(ss_l + b);   // used after the q/k/v loads are issued
     const float* accb = acc_l + (int64_t)b * p.nqkv_pad;
-    // ---- Q tile of the group's query heads (rows >= G zero), new k / v row
-    for (int hh = warp; hh < 16; hh += kCons) {
-      if (hh < G) {
-        float o[4];
-        rope_norm(p, accb + (g * G + hh) * kHd, rb, o);
-#pragma unroll
-        for (int jj = 0; jj < 4; ++jj) st16<T16>(sh.sq, hh, lane + 32 * jj, o[jj]);
-      } else {
-#pragma unroll
-        for (int jj = 0; jj < 4; ++jj) st16<T16>(sh.sq, hh, lane + 32 * jj, 0.f);
-      }
-    }
+    // ---- Q tile of the group's query heads (rows >= G zero) and, in the CTA that
+    // holds position pos, the new k / v row. Warp w prepares query rows w and w + 8;
+    // warps 0 and 1 also the new k and v. All loads are issued before any use.
     const bool has_last = j1 == T16n;
-    if (has_last) {
-      const int64_t crow = (((int64_t)l * p.cache_batch + p.b_off + b) * p.Hkv + g) * p.t_max + p.pos;
-      if (warp == 0) {
+    {
+      const int nrow = (has_last && warp < 2) ? 3 : 2;
+      float av[3][4];
+      const float* cs = p.cos_tab + (int64_t)p.pos * (kHd / 2);
+      const float* sn = p.sin_tab + (int64_t)p.pos * (kHd / 2);
+      float cv[2], sv[2];
+#pragma unroll
+      for (int jj = 0; jj < 2; ++jj) {
+        cv[jj] = cs[lane + 32 * jj];
+        sv[jj] = sn[lane + 32 * jj];
+      }
+#pragma unroll
+      for (int rr = 0; rr < 3; ++rr) {
+        const int hh = warp + 8 * rr;
+        const float* src = nullptr;
+        if (rr < 2 && hh < G) src = accb + (g * G + hh) * kHd;
+        if (rr == 2 && nrow == 3) src = accb + qd + (warp == 0 ? g * kHd : kvd + g * kHd);
+#pragma unroll
+        for (int jj = 0; jj < 4; ++jj) av[rr][jj] = src ? __ldcg(src + lane + 32 * jj) : 0.f;
+      }
+      const float rb = rsqrtf(ssb / (float)p.d + p.eps);
+#pragma unroll
+      for (int rr = 0; rr < 3; ++rr)
+#pragma unroll
+        for (int jj = 0; jj < 4; ++jj) av[rr][jj] *= rb;
+#pragma unroll
+      for (int rr = 0; rr < 3; ++rr) {
+        if (rr == 2 && nrow < 3) break;
+        const bool is_v = rr == 2 && warp == 1;
         float o[4];
-        rope_norm(p, accb + qd + g * kHd, rb, o);
-        T16* kc = static_cast<T16*>(p.k_cache) + crow * kHd;
+        if (is_v) {
 #pragma unroll
-        for (int jj = 0; jj < 4; ++jj) {
-          const T16 v = from_f32<T16>(o[jj]);
-          kc[lane + 32 * jj] = v;
-          reinterpret_cast<T16*>(sh.kvnew)[lane + 32 * jj] = v;
+          for (int jj = 0; jj < 4; ++jj) o[jj] = av[rr][jj];
+        } else {
+          float sq = 0.f;
+#pragma unroll
+          for (int jj = 0; jj < 4; ++jj) sq += av[rr][jj] * av[rr][jj];
+          sq = warp_sum(sq);
+          const float rn = rsqrtf(sq * (1.f / kHd) + p.eps);
+#pragma unroll
+          for (int jj = 0; jj < 2; ++jj) {
+            const float lo = av[rr][jj], hi = av[rr][jj + 2];
+            o[jj] = (lo * cv[jj] - hi * sv[jj]) * rn;
+            o[jj + 2] = (lo * sv[jj] + hi * cv[jj]) * rn;
+          }
         }
-      } else if (warp == 1) {
-        T16* vc = static_cast<T16*>(p.v_cache) + crow * kHd;
+        if (rr < 2) {
 #pragma unroll
-        for (int jj = 0; jj < 4; ++jj) {
-          const T16 v = from_f32<T16>(__ldcg(accb + qd + kvd + g * kHd + lane + 32 * jj) * rb);
-          vc[lane + 32 * jj] = v;
-          reinterpret_cast<T16*>(sh.kvnew)[kHd + lane + 32 * jj] = v;
+          for (int jj = 0; jj < 4; ++jj) st16<T16>(sh.sq, warp + 8 * rr, lane + 32 * jj, o[jj]);
+        } else {
+          const int64_t crow =
+              (((int64_t)l * p.cache_batch + p.b_off + b) * p.Hkv + g) * p.t_max + p.pos;
+          T16* dstc = static_cast<T16*>(is_v ? p.v_cache : p.k_cache) + crow * kHd;
+#pragma unroll
+          for (int jj = 0; jj < 4; ++jj) {
+            const T16 v = from_f32<T16>(o[jj]);
+            dstc[lane + 32 * jj] = v;
+            reinterpret_cast<T16*>(sh.kvnew)[(is_v ? kHd : 0) + lane + 32 * jj] = v;
+          }
         }
       }
     }
     bar_consumers();
-    // ---- Q fragments (A operand) for the 8 k16 steps of head_dim
-    uint32_t qa[8][4];
-    {
-      const uint32_t sq = smem_u32(sh.sq);
-      const int row = (lane & 7) + ((lane >> 3) & 1) * 8;
-#pragma unroll
-      for (int ks = 0; ks < 8; ++ks) {
-        const int c16 = 2 * ks + (lane >> 4);
-        ldsm_x4(sq + sw_off(row, c16), qa[ks]);
-      }
-    }
+    trace_mark(p, k, 0);
+    // ---- Q fragments (A operand) are read from shared memory per k16 step
+    const uint32_t sq_base = smem_u32(sh.sq);
+    const int q_row = (lane & 7) + ((lane >> 3) & 1) * 8;
     float m_r[2] = {-INFINITY, -INFINITY}, l_r[2] = {0.f, 0.f};
     float o[16][4];
 #pragma unroll
@@ -716,10 +811,11 @@ __device__ bool consume_attn(const Params& p, Shared& sh, int l) {
           const int key = (lane & 7) + ((lane >> 4) << 3);
 #pragma unroll
           for (int ks = 0; ks < 8; ++ks) {
-            uint32_t kb[4];
+            uint32_t kb[4], qa[4];
+            ldsm_x4(sq_base + sw_off(q_row, 2 * ks + (lane >> 4)), qa);
             ldsm_x4(sK + sw_off(key, 2 * ks + ((lane >> 3) & 1)), kb);
-            mma16816<T16>(s[0], qa[ks][0], qa[ks][1], qa[ks][2], qa[ks][3], kb[0], kb[1]);
-            mma16816<T16>(s[1], qa[ks][0], qa[ks][1], qa[ks][2], qa[ks][3], kb[2], kb[3]);
+            mma16816<T16>(s[0], qa[0], qa[1], qa[2], qa[3], kb[0], kb[1]);
+            mma16816<T16>(s[1], qa[0], qa[1], qa[2], qa[3], kb[2], kb[3]);
           }
         }
         // mask keys past pos, online softmax in the log2 domain
@@ -780,6 +876,7 @@ __device__ bool consume_attn(const Params& p, Shared& sh, int l) {
       if (lane == 0) mbar_arrive(&r.empty[r.stage]);
       r.advance();
     }
+    trace_mark(p, k, 1);
     // ---- merge the warps' states: row sums over the quad, then through smem
 #pragma unroll
     for (int h = 0; h < 2; ++h) {
@@ -807,7 +904,7 @@ __device__ bool consume_attn(const Params& p, Shared& sh, int l) {
     const int c_first = owner_of(total, (int64_t)bg * T16n, gridDim.x);
     const int c_last = owner_of(total, (int64_t)bg * T16n + T16n - 1, gridDim.x);
     const int slot = blockIdx.x - c_first;
-    float* rec = p.attn_part + ((int64_t)bg * p.attn_slots + slot) * G * (kHd + 2);
+    float* rec = p.attn_part + ((int64_t)bg * p.attn_slots + slot) * p.rec_stride;
     for (int e = tid; e < G * (kHd + 2); e += 256) {
       const int h = e / (kHd + 2), i = e % (kHd + 2);
       float M = -INFINITY;
@@ -827,6 +924,7 @@ __device__ bool consume_attn(const Params& p, Shared& sh, int l) {
     }
     __threadfence();
     bar_consumers();
+    trace_mark(p, k, 2);
     if (tid == 0) {
       const unsigned int n = atomicAdd(p.attn_count + bg, 1u);
       sh.flag[1] = (n == (unsigned)(c_last - c_first)) ? 1 : 0;
@@ -835,20 +933,38 @@ __device__ bool consume_attn(const Params& p, Shared& sh, int l) {
     bar_consumers();
     if (sh.flag[1]) {
       // last CTA of (b, g): log-sum-exp merge of every slot -> att[b, heads of g].
-      // Scales exp2(m_s - M) / L per (slot, head) go to shared memory first.
+      // The records are contiguous: read them into shared memory in one batched
+      // pass, then merge from there.
       const int ns = c_last - c_first + 1;
-      const float* base = p.attn_part + (int64_t)bg * p.attn_slots * G * (kHd + 2);
-      float* scl = reinterpret_cast<float*>(sh.act);   // [ns][G]; the merge area is free again
+      const float* base = p.attn_part + (int64_t)bg * p.attn_slots * p.rec_stride;
+      // (a long context over few sequences can give more slots than shared memory
+      // holds: then the records are read from global memory directly)
+      const int scl_floats = (ns * G + 3) / 4 * 4;   // keeps the records 16-byte aligned
+      const bool in_smem = ((int64_t)ns * p.rec_stride + scl_floats) * 4 <= p.act_bytes;
+      float* scl = reinterpret_cast<float*>(sh.act);          // [ns][G]: exp2(m_s - M) / L
+      float* recs_s = scl + scl_floats;
+      auto rec_at = [&](int idx) { return in_smem ? recs_s[idx] : __ldcg(base + idx); };
+      const int n4 = in_smem ? ns * p.rec_stride / 4 : 0;
+      for (int i0 = tid; i0 < n4; i0 += 256 * 8) {
+        float4 v[8];
+#pragma unroll
+        for (int u = 0; u < 8; ++u)
+          if (i0 + u * 256 < n4) v[u] = __ldcg(reinterpret_cast<const float4*>(base) + i0 + u * 256);
+#pragma unroll
+        for (int u = 0; u < 8; ++u)
+          if (i0 + u * 256 < n4) reinterpret_cast<float4*>(recs_s)[i0 + u * 256] = v[u];
+      }
+      bar_consumers();
       if (tid < G) {
         const int h = tid;
         float M = -INFINITY;
-        for (int s2 = 0; s2 < ns; ++s2) M = fmaxf(M, __ldcg(base + (s2 * G + h) * (kHd + 2)));
+        for (int s2 = 0; s2 < ns; ++s2) M = fmaxf(M, rec_at(s2 * p.rec_stride + h * (kHd + 2)));
         float L = 0.f;
         for (int s2 = 0; s2 < ns; ++s2) {
-          const float* rr = base + (s2 * G + h) * (kHd + 2);
-          const float e = exp2f(__ldcg(rr) - M);
+          const int rr = s2 * p.rec_stride + h * (kHd + 2);
+          const float e = exp2f(rec_at(rr) - M);
           scl[s2 * G + h] = e;
-          L += e * __ldcg(rr + 1);
+          L += e * rec_at(rr + 1);
         }
         const float inv = 1.f / L;
         for (int s2 = 0; s2 < ns; ++s2) scl[s2 * G + h] *= inv;
@@ -857,20 +973,14 @@ __device__ bool consume_attn(const Params& p, Shared& sh, int l) {
       for (int e = tid; e < G * kHd; e += 256) {
         const int h = e / kHd, i = e % kHd;
         float O = 0.f;
-        int s2 = 0;
-        for (; s2 + 4 <= ns; s2 += 4) {
-          float v[4];
-#pragma unroll
-          for (int u = 0; u < 4; ++u) v[u] = __ldcg(base + ((s2 + u) * G + h) * (kHd + 2) + 2 + i);
-#pragma unroll
-          for (int u = 0; u < 4; ++u) O += scl[(s2 + u) * G + h] * v[u];
-        }
-        for (; s2 < ns; ++s2) O += scl[s2 * G + h] * __ldcg(base + (s2 * G + h) * (kHd + 2) + 2 + i);
+        for (int s2 = 0; s2 < ns; ++s2)
+          O += scl[s2 * G + h] * rec_at(s2 * p.rec_stride + h * (kHd + 2) + 2 + i);
         static_cast<T16*>(p.att)[(int64_t)b * qd + (g * G + h) * kHd + i] = from_f32<T16>(O);
       }
       if (tid == 0) p.attn_count[bg] = 0u;
     }
     bar_consumers();
+    trace_mark(p, k, 3);
     f += j1 - j0;
   }
   return true;
@@ -953,9 +1063,23 @@ __device__ void phase_argmax(const Params& p, const Shared& sh) {
     const int b = t / nch, ch = t % nch;
     const float* row = p.logits + (int64_t)b * p.V;
     uint64_t best = 0;
-    for (int i = ch * kChunk + tid; i < min(p.V, (ch + 1) * kChunk); i += 256) {
-      const uint64_t k = argmax_key(__ldcg(row + i), i);
-      best = k > best ? k : best;
+    // thread: 8 consecutive logits (two 16-byte loads issued together)
+    const int i0 = ch * kChunk + tid * 8;
+    const int lim = min(p.V, (ch + 1) * kChunk);
+    if (i0 + 8 <= lim) {
+      const float4 a = __ldcg(reinterpret_cast<const float4*>(row + i0));
+      const float4 c = __ldcg(reinterpret_cast<const float4*>(row + i0 + 4));
+      const float v[8] = {a.x, a.y, a.z, a.w, c.x, c.y, c.z, c.w};
+#pragma unroll
+      for (int u = 0; u < 8; ++u) {
+        const uint64_t k = argmax_key(v[u], i0 + u);
+        best = k > best ? k : best;
+      }
+    } else {
+      for (int i = i0; i < lim; ++i) {
+        const uint64_t k = argmax_key(__ldcg(row + i), i);
+        best = k > best ? k : best;
+      }
     }
 #pragma unroll
     for (int o = 16; o > 0; o >>= 1) {
@@ -1004,6 +1128,8 @@ __global__ void __launch_bounds__(kThreads, 1)
   q += 4096;
   sh.kvnew = reinterpret_cast<uint16_t*>(q);
   q += 512;
+  sh.ss_s = reinterpret_cast<float*>(q);
+  q += 128;
   sh.ring.full = reinterpret_cast<uint64_t*>(q);
   sh.ring.empty = sh.ring.full + p.stages;
   sh.flag = reinterpret_cast<volatile int*>(sh.ring.empty + p.stages);
@@ -1050,22 +1176,22 @@ __global__ void __launch_bounds__(kThreads, 1)
   if (!grid_barrier(p, sh, ++nbar)) return;
   for (int l = 0; l < p.L; ++l) {
     zero_f32(p.hacc, (int64_t)p.B * p.F);
-    if (!consume_gemv<NT, T16>(p, sh, gemv_of(p, l, PH_QKV))) return;
+    if (!consume_gemv<NT, T16>(p, sh, gemv_of(p, l, PH_QKV), nbar + 1)) return;
     if (!grid_barrier(p, sh, ++nbar)) return;
     if (l + 1 < p.L) zero_f32(p.qkv_acc + (int64_t)((l + 1) & 1) * kMaxTok * p.nqkv_pad,
                               (int64_t)p.B * p.nqkv_pad);
-    if (!consume_attn<T16>(p, sh, l)) return;
+    if (!consume_attn<T16>(p, sh, l, nbar + 1)) return;
     if (!grid_barrier(p, sh, ++nbar)) return;
-    if (!consume_gemv<NT, T16>(p, sh, gemv_of(p, l, PH_O))) return;
+    if (!consume_gemv<NT, T16>(p, sh, gemv_of(p, l, PH_O), nbar + 1)) return;
     if (!grid_barrier(p, sh, ++nbar)) return;
-    if (!consume_gemv<NT, T16>(p, sh, gemv_of(p, l, PH_FC))) return;
+    if (!consume_gemv<NT, T16>(p, sh, gemv_of(p, l, PH_FC), nbar + 1)) return;
     if (!grid_barrier(p, sh, ++nbar)) return;
-    if (!consume_gemv<NT, T16>(p, sh, gemv_of(p, l, PH_PROJ))) return;
+    if (!consume_gemv<NT, T16>(p, sh, gemv_of(p, l, PH_PROJ), nbar + 1)) return;
     if (!grid_barrier(p, sh, ++nbar)) return;
   }
   phase_final_norm<NT, T16>(p);
   if (!grid_barrier(p, sh, ++nbar)) return;
-  if (!consume_gemv<NT, T16>(p, sh, gemv_lm(p))) return;
+  if (!consume_gemv<NT, T16>(p, sh, gemv_lm(p), nbar + 1)) return;
   if (!grid_barrier(p, sh, ++nbar)) return;
   phase_argmax(p, sh);
   if (p.trace && blockIdx.x == 0 && threadIdx.x == 32)
@@ -1180,7 +1306,7 @@ size_t smem_bytes(int nt, int d, int* stages, int* act_bytes) {
   const int ksteps = d / 16;
   int act = std::max(nt * 256 * ksteps, kMergeBytes);
   act = (act + 1023) / 1024 * 1024;
-  const int fixed = 1024 /*align*/ + kXposeBytes + 4096 + 512 + 64;
+  const int fixed = 1024 /*align*/ + kXposeBytes + 4096 + 512 + 128 + 64;
   const int limit = 232448 - 1024;   // dynamic part; static shared memory is small
   int st = (limit - fixed - act) / (kStage + 16);
   if (st > 24) st = 24;

@@ -32,6 +32,7 @@ struct Params {
   int B, b_off, pos, cache_batch, t_max;
   int L, d, H, Hkv, F, V, vpad, nqkv, nqkv_pad;
   int stages, act_bytes, attn_slots;
+  int rec_stride;             // floats per partial record: G*(128+2) rounded up to 4
   float eps, scale_log2;
   int64_t layer_bytes, off_o, off_fc, off_proj;
   const int32_t* tokens;      // [B]
@@ -58,8 +59,9 @@ struct Params {
   uint32_t* status;
   uint32_t* abort;
   // optional: %globaltimer of CTA 0 at start, at each grid barrier (arrival,
-  // exit) and at the end: 2 * barriers + 2 entries
+  // exit) and at the end (2 * nbar + 2 entries), then 4 marks inside each phase
   unsigned long long* trace;
+  int nbar;                   // grid barriers of this launch
 };
 
 Layout layout_of(int L, int d, int H, int Hkv, int F, int V);
@@ -71,6 +73,8 @@ int attn_slots_needed(int B, int Hkv, int pos, int P);
 bool make_cache_map(CUtensorMap* map, void* base, uint64_t rows, bool half);
 // Grid barriers one launch passes (its arrivals are that times the grid size).
 inline int barriers_per_step(int L) { return 5 * L + 3; }
+// Entries of a full trace (barrier times plus 5 marks per phase).
+inline int trace_entries(int L) { return 7 * barriers_per_step(L) + 2; }
 // Enqueues one step for p.B <= kMaxTok sequences on `sms` CTAs (cooperative launch).
 nc_status launch_step(const CUtensorMap& tk, const CUtensorMap& tv, Params p, bool half,
                       nc_dtype wdt, int sms, cudaStream_t s);

@@ -20,6 +20,7 @@
 //     writes transposed fp32 partial sums [split][token][feature] that a
 //     finishing kernel reduces (or, unsplit, the logits directly).
 #include <limits.h>
+#include <stdlib.h>
 
 #include <algorithm>
 #include <vector>
@@ -45,6 +46,60 @@ struct GemmArgs {
   RowMap rm;               // EPI_QKV
   QkvDst qkv;
   uint32_t* status;
+  int stream_k;            // 1: CTAs take equal contiguous ranges of (tile, k block)
+};
+
+// Work schedule shared by the three roles of a CTA: a sequence of segments
+// (m block, n block, k blocks [kb0, kb1), split index for EPI_SWAP).
+//   persistent: whole tiles (or K splits) u = first, first + step, ...
+//   stream-K:   the CTA's contiguous share of all (tile, k block) pairs, so
+//               every CTA does the same number of k blocks; a tile cut between
+//               CTAs is finished by more than one of them (EPI_RESID adds).
+struct Seg {
+  int mb, nb, kb0, kb1, ks;
+};
+struct Sched {
+  int64_t pos, end;   // stream-K position / end, or persistent unit / units
+  int step, num_mu, rank, mc;
+  bool sk;
+  __device__ __forceinline__ void init(const GemmArgs& p, int mc_, int rank_) {
+    mc = mc_;
+    rank = rank_;
+    num_mu = (p.num_m_blk + mc - 1) / mc;
+    sk = p.stream_k != 0;
+    if (sk) {
+      const int64_t total = (int64_t)p.num_m_blk * p.num_n_blk * p.num_k_blk;
+      pos = total * blockIdx.x / gridDim.x;
+      end = total * (blockIdx.x + 1) / gridDim.x;
+      step = 0;
+    } else {
+      pos = blockIdx.x / mc;
+      end = (int64_t)num_mu * p.num_n_blk * p.k_splits;
+      step = gridDim.x / mc;
+    }
+  }
+  __device__ __forceinline__ bool next(const GemmArgs& p, Seg& g) {
+    if (pos >= end) return false;
+    if (sk) {
+      const int64_t t = pos / p.num_k_blk;
+      g.kb0 = (int)(pos % p.num_k_blk);
+      { const int64_t e = g.kb0 + (end - pos); g.kb1 = (int)(e < p.num_k_blk ? e : p.num_k_blk); }
+      g.mb = (int)(t % p.num_m_blk);
+      g.nb = (int)(t / p.num_m_blk);
+      g.ks = 0;
+      pos += g.kb1 - g.kb0;
+    } else {
+      const int u = (int)pos;
+      g.mb = (u % num_mu) * mc + rank;
+      const int rest = u / num_mu;
+      g.nb = rest % p.num_n_blk;
+      g.ks = rest / p.num_n_blk;
+      g.kb0 = g.ks * p.k_per_split;
+      g.kb1 = min(p.num_k_blk, g.kb0 + p.k_per_split);
+      pos += step;
+    }
+    return true;
+  }
 };
 
 template <int BN>
@@ -121,19 +176,10 @@ __device__ __forceinline__ void epi_store_rows(const GemmArgs& p, uint32_t taddr
         }
       }
     } else {
-      // 8 lanes per row (4 values each), 4 rows per pass. The residual rows are
-      // all loaded before any store so that the eight loads overlap.
+      // 8 lanes per row (4 values each), 4 rows per pass. The residual add is a
+      // vector reduction into x: no load, and a tile split between CTAs
+      // (stream-K) adds each part.
       const int cc = (lane % 8) * 4, gcol = n0 + cc;
-      float4 x[8];
-      if (mode == EPI_RESID) {
-#pragma unroll
-        for (int it = 0; it < 8; ++it) {
-          const int grow = row0 + it * 4 + lane / 8;
-          x[it] = (grow < p.M && gcol < p.N)
-                      ? __ldcg(reinterpret_cast<const float4*>(p.out_f32 + (int64_t)grow * p.ldo + gcol))
-                      : make_float4(0.f, 0.f, 0.f, 0.f);
-        }
-      }
 #pragma unroll
       for (int it = 0; it < 8; ++it) {
         const int r = it * 4 + lane / 8;
@@ -142,8 +188,7 @@ __device__ __forceinline__ void epi_store_rows(const GemmArgs& p, uint32_t taddr
           const float4 a = *reinterpret_cast<const float4*>(stage + r * S + cc);
           float* dst = p.out_f32 + (int64_t)grow * p.ldo + gcol;
           if (mode == EPI_RESID) {
-            *reinterpret_cast<float4*>(dst) =
-                make_float4(x[it].x + a.x, x[it].y + a.y, x[it].z + a.z, x[it].w + a.w);
+            red_add_f32x4(dst, a);
           } else {
             st_global_cs_v4(dst, make_uint4(__float_as_uint(a.x), __float_as_uint(a.y),
                                             __float_as_uint(a.z), __float_as_uint(a.w)));
@@ -255,7 +300,11 @@ __device__ __forceinline__ void epi_swap(const GemmArgs& p, uint32_t taddr, int 
 }
 
 // --------------------------------------------------------------------- kernel
-template <int BN, int EPI, class T16>
+// MC = 2: CTAs run in clusters of two that take adjacent 128-row blocks of A
+// and the same B tile; each CTA loads half of the B tile and multicasts it to
+// both, so B is read from L2 once per pair. A stage is refilled only when both
+// CTAs' MMAs have released it (the empty barriers count both commits).
+template <int BN, int EPI, class T16, int MC>
 __global__ void __launch_bounds__(192, 1)
     gemm_tc_kernel(const __grid_constant__ CUtensorMap tmA0, const __grid_constant__ CUtensorMap tmA1,
                    const __grid_constant__ CUtensorMap tmA2, const __grid_constant__ CUtensorMap tmB0,
@@ -278,7 +327,7 @@ __global__ void __launch_bounds__(192, 1)
   if (threadIdx.x == 0) {
     for (int s = 0; s < S; ++s) {
       mbar_init(&full[s], 1);
-      mbar_init(&empty[s], 1);
+      mbar_init(&empty[s], MC);
     }
     for (int b = 0; b < 2; ++b) {
       mbar_init(&tfull[b], 1);
@@ -297,23 +346,23 @@ __global__ void __launch_bounds__(192, 1)
   }
   tc_fence_before();
   __syncthreads();
+  if (MC > 1) cluster_sync_all();   // the peer's barriers exist before any multicast
   tc_fence_after();
   const uint32_t tmem_base = *tmem_slot;
-  const int units = p.num_m_blk * p.num_n_blk * p.k_splits;
+  // work segments; a cluster walks the same sequence
+  const int rank = MC > 1 ? (int)cluster_ctarank() : 0;
 
   if (warp == 0) {
     if (lane == 0) {
       // ------------------------------------------------------------ producer
       int stage = 0, issued = 0;
       uint32_t phase = 0;
-      for (int u = blockIdx.x; u < units && !*abort_flag; u += gridDim.x) {
-        const int mb = u % p.num_m_blk;
-        const int rest = u / p.num_m_blk;
-        const int nb = rest % p.num_n_blk;
-        const int ks = rest / p.num_n_blk;
-        const int kb0 = ks * p.k_per_split;
-        const int kb1 = min(p.num_k_blk, kb0 + p.k_per_split);
-        for (int kb = kb0; kb < kb1; ++kb) {
+      Sched sc;
+      sc.init(p, MC, rank);
+      Seg sg;
+      while (!*abort_flag && sc.next(p, sg)) {
+        const int mb = sg.mb, nb = sg.nb;
+        for (int kb = sg.kb0; kb < sg.kb1; ++kb) {
           if (!mbar_wait(&empty[stage], phase ^ 1, p.status)) {
             *abort_flag = 1;
             break;
@@ -324,11 +373,23 @@ __global__ void __launch_bounds__(192, 1)
           int local;
           const CUtensorMap* ma = pick_map(&tmA0, &tmA1, &tmA2, mb * 128, p.a_split0, p.a_split1, local);
           tma_load_2d(sa, ma, &full[stage], kb * 64, local);
+          if (MC > 1) {
+            // this CTA's share of the B tile, to both CTAs of the pair
 #pragma unroll
-          for (int h = 0; h < BN / C::kBoxRowsB; ++h) {
-            const CUtensorMap* mb_ = pick_map(&tmB0, &tmB1, &tmB2, nb * BN + h * C::kBoxRowsB,
-                                              p.b_split0, p.b_split1, local);
-            tma_load_2d(sb + h * C::kBoxRowsB * 128, mb_, &full[stage], kb * 64, local);
+            for (int h = rank * (BN / C::kBoxRowsB / MC); h < (rank + 1) * (BN / C::kBoxRowsB / MC);
+                 ++h) {
+              const CUtensorMap* mb_ = pick_map(&tmB0, &tmB1, &tmB2, nb * BN + h * C::kBoxRowsB,
+                                                p.b_split0, p.b_split1, local);
+              tma_load_2d_mc(sb + h * C::kBoxRowsB * 128, mb_, &full[stage], kb * 64, local,
+                             (uint16_t)((1u << MC) - 1));
+            }
+          } else {
+#pragma unroll
+            for (int h = 0; h < BN / C::kBoxRowsB; ++h) {
+              const CUtensorMap* mb_ = pick_map(&tmB0, &tmB1, &tmB2, nb * BN + h * C::kBoxRowsB,
+                                                p.b_split0, p.b_split1, local);
+              tma_load_2d(sb + h * C::kBoxRowsB * 128, mb_, &full[stage], kb * 64, local);
+            }
           }
           if (++stage == S) {
             stage = 0;
@@ -354,10 +415,11 @@ __global__ void __launch_bounds__(192, 1)
       uint32_t phase = 0;
       int acc = 0;
       uint32_t acc_phase = 0;
-      for (int u = blockIdx.x; u < units && !*abort_flag; u += gridDim.x) {
-        const int ks = (u / p.num_m_blk) / p.num_n_blk;
-        const int kb0 = ks * p.k_per_split;
-        const int kb1 = min(p.num_k_blk, kb0 + p.k_per_split);
+      Sched sc;
+      sc.init(p, MC, rank);
+      Seg sg;
+      while (!*abort_flag && sc.next(p, sg)) {
+        const int kb0 = sg.kb0, kb1 = sg.kb1;
         if (!mbar_wait(&tempty[acc], acc_phase ^ 1, p.status)) {
           *abort_flag = 1;
           break;
@@ -379,7 +441,10 @@ __global__ void __launch_bounds__(192, 1)
             mma_f16kind_ss(d_tmem, sdesc_kmajor_sw128(a_addr + k * 32),
                         sdesc_kmajor_sw128(b_addr + k * 32), kIdesc, (kb > kb0 || k > 0) ? 1u : 0u);
           }
-          mma_commit(&empty[stage]);
+          if (MC > 1)
+            mma_commit_mc(&empty[stage], (uint16_t)((1u << MC) - 1));
+          else
+            mma_commit(&empty[stage]);
           if (++stage == S) {
             stage = 0;
             phase ^= 1;
@@ -398,11 +463,11 @@ __global__ void __launch_bounds__(192, 1)
     const int quarter = warp % 4;
     int acc = 0;
     uint32_t acc_phase = 0;
-    for (int u = blockIdx.x; u < units; u += gridDim.x) {
-      const int mb = u % p.num_m_blk;
-      const int rest = u / p.num_m_blk;
-      const int nb = rest % p.num_n_blk;
-      const int ks = rest / p.num_n_blk;
+    Sched sc;
+    sc.init(p, MC, rank);
+    Seg sg;
+    while (sc.next(p, sg)) {
+      const int mb = sg.mb, nb = sg.nb, ks = sg.ks;
       const bool ok = __all_sync(0xffffffffu, mbar_wait(&tfull[acc], acc_phase, p.status));
       if (!ok) {
         *abort_flag = 1;
@@ -434,6 +499,9 @@ __global__ void __launch_bounds__(192, 1)
     tc_fence_after();
     tmem_dealloc(tmem_base, C::kTmemCols);
   }
+  // the peer may still multicast into this CTA's shared memory or arrive on its
+  // barriers until it is done too
+  if (MC > 1) cluster_sync_all();
 }
 
 
@@ -501,12 +569,57 @@ static int sm_count_now() {
   return n;
 }
 
+// Tile-mode GEMMs with 256-wide N tiles run in clusters of two that share the
+// B tile through TMA multicast when NC_GEMM_MC=1 is set in the environment.
+static bool use_multicast() {
+  static int v = -1;
+  if (v < 0) {
+    const char* e = getenv("NC_GEMM_MC");
+    v = (e && e[0] == '1') ? 1 : 0;
+  }
+  return v == 1;
+}
+
 template <int BN, int EPI, class T16>
 static nc_status launch_gemm(const CUtensorMap& a0, const CUtensorMap& a1, const CUtensorMap& a2,
                              const CUtensorMap& b0, const CUtensorMap& b1, const CUtensorMap& b2,
                              const GemmArgs& args, int sm_count, cudaStream_t s) {
   using C = TileCfg<BN>;
-  auto kern = gemm_tc_kernel<BN, EPI, T16>;
+  if constexpr (BN == 256 && EPI != EPI_SWAP) {
+    if (use_multicast() && !args.stream_k) {
+      auto kern = gemm_tc_kernel<BN, EPI, T16, 2>;
+      static int max_pairs = -1;
+      cudaLaunchConfig_t cfg = {};
+      cudaLaunchAttribute at[1];
+      at[0].id = cudaLaunchAttributeClusterDimension;
+      at[0].val.clusterDim.x = 2;
+      at[0].val.clusterDim.y = 1;
+      at[0].val.clusterDim.z = 1;
+      cfg.blockDim = dim3(192);
+      cfg.dynamicSmemBytes = C::kSmemBytes;
+      cfg.attrs = at;
+      cfg.numAttrs = 1;
+      if (max_pairs < 0) {
+        max_pairs = 0;
+        if (cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                 (int)C::kSmemBytes) == cudaSuccess) {
+          cfg.gridDim = dim3(2 * (sm_count / 2));
+          int n = 0;
+          if (cudaOccupancyMaxActiveClusters(&n, kern, &cfg) == cudaSuccess) max_pairs = n;
+        }
+        cudaGetLastError();
+      }
+      if (max_pairs > 0) {
+        const int pair_units = (args.num_m_blk + 1) / 2 * args.num_n_blk * args.k_splits;
+        cfg.gridDim = dim3(2 * std::min(pair_units, max_pairs));
+        cfg.stream = s;
+        const cudaError_t e = cudaLaunchKernelEx(&cfg, kern, a0, a1, a2, b0, b1, b2, args);
+        count_launches(1);
+        return e == cudaSuccess ? NC_OK : NC_ERR_CUDA;
+      }
+    }
+  }
+  auto kern = gemm_tc_kernel<BN, EPI, T16, 1>;
   static bool configured = false;
   if (!configured) {
     if (cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize,
@@ -515,7 +628,7 @@ static nc_status launch_gemm(const CUtensorMap& a0, const CUtensorMap& a1, const
     configured = true;
   }
   const int units = args.num_m_blk * args.num_n_blk * args.k_splits;
-  const int grid = std::min(units, sm_count);
+  const int grid = args.stream_k ? sm_count : std::min(units, sm_count);
   kern<<<grid, 192, C::kSmemBytes, s>>>(a0, a1, a2, b0, b1, b2, args);
   count_launches(1);
   return cudaGetLastError() == cudaSuccess ? NC_OK : NC_ERR_CUDA;
@@ -536,14 +649,23 @@ static GemmArgs base_args(int M, int N, int K, int BN, uint32_t* status) {
   return a;
 }
 
-// tile mode: N tile 128 or 256, whichever wastes less of the last wave
+// tile mode: N tile 128 or 256. A 128 x 128 x 16 MMA reads 8 KB of shared
+// memory every 64 cycles (the full 128 B/clock of an SM), a 128 x 256 x 16 one
+// 12 KB every 128 cycles, so 256 wins unless 128 wastes clearly less of the last
+// wave. NC_GEMM_BN=128|256 in the environment forces one (measurement).
 static int pick_bn(int M, int N, int sm_count) {
+  static int forced = -1;
+  if (forced < 0) {
+    const char* e = getenv("NC_GEMM_BN");
+    forced = e ? atoi(e) : 0;
+  }
+  if (forced == 128 || forced == 256) return forced;
   const int mb = (M + 127) / 128;
   auto cost = [&](int bn) {
     const int units = mb * ((N + bn - 1) / bn);
     return (int64_t)((units + sm_count - 1) / sm_count) * bn;
   };
-  return cost(256) < cost(128) ? 256 : 128;
+  return cost(128) * 4 < cost(256) * 3 ? 128 : 256;
 }
 
 template <int EPI, class T16>
@@ -642,6 +764,7 @@ static nc_status out_proj_impl(TcModel* t, int l, int64_t M, float* x, float* pa
   GemmArgs args = base_args((int)M, d, qd, BN, t->status);
   args.out_f32 = x;
   args.ldo = d;
+  args.stream_k = 1;
   return tile_gemm<EPI_RESID, T16>(a, w.wo, w.wo, w.wo, args, BN, t->sm_count, s);
 }
 
@@ -686,6 +809,7 @@ static nc_status proj_impl(TcModel* t, int l, int64_t M, float* x, float* part, 
   GemmArgs args = base_args((int)M, d, F, BN, t->status);
   args.out_f32 = x;
   args.ldo = d;
+  args.stream_k = 1;
   return tile_gemm<EPI_RESID, T16>(a, w.wproj, w.wproj, w.wproj, args, BN, t->sm_count, s);
 }
 
