@@ -336,11 +336,13 @@ def run_ours(args):
                    "l2": "inputs larger than L2 (no flush)"},
         "prefill": {"value": round(value, 1), "unit": "tok/s", "ms": round(pre_ms / K, 3),
                     "tflops": round(pre_tflops, 1), "algorithmic_tflop": round((g_flops + a_flops) / 1e12, 3),
-                    "frac_of_measured_peak": round(pre_tflops / bf16_peak, 4),
+                    "frac_of_peak": round(pre_tflops / bf16_peak, 4),
+                    "peak": bf16_peak, "peak_source": f"{peak_src} bf16",
                     "frac_of_nominal_peak": round(pre_tflops / NOMINAL["bf16_tflops"], 4)},
         "decode": {"value": round(dec_value, 1), "unit": "tok/s", "ms_per_token_step": round(dec_ms / K / steps, 4),
                    "gbs": round(dec_gbs, 1), "algorithmic_mb_per_step": round(dec_bytes / steps / 1e6, 1),
-                   "frac_of_measured_peak": round(dec_gbs / peaks["hbm_gbs"], 4),
+                   "frac_of_peak": round(dec_gbs / peaks["hbm_gbs"], 4),
+                   "peak": peaks["hbm_gbs"], "peak_source": f"{peak_src} HBM copy",
                    "frac_of_nominal_peak": round(dec_gbs / NOMINAL["hbm_gbs"], 4),
                    "e2e": e2e["decode"]},
         "roofline": roof,
@@ -355,6 +357,32 @@ def run_ours(args):
     print(json.dumps(line), flush=True)
 
 
+def recorded_traffic(kind):
+    """Per-launch DRAM traffic (read + write) of a kernel class from its committed ncu
+    summary under profiles/, or None if there is none or the kernel's source has
+    changed since the counters were taken (the summary records a source hash)."""
+    import hashlib
+    files = {"decode_step": "decode_step_d20_mqa_B32_dram.md"}
+    if kind not in files:
+        return None
+    path = os.path.join(ROOT, "profiles", files[kind])
+    if not os.path.exists(path):
+        return None
+    fields = {}
+    for line in open(path):
+        if ":" in line and not line.startswith(("|", "#", " ")):
+            k, _, v = line.partition(":")
+            fields[k.strip()] = v.strip()
+    try:
+        src = os.path.join(ROOT, fields["kernel_source"])
+        h = hashlib.sha256(open(src, "rb").read()).hexdigest()[:16]
+        if h != fields["kernel_source_sha256_16"]:
+            return None
+        return int(fields["traffic_bytes_per_launch_mean_ctx"])
+    except (KeyError, OSError, ValueError):
+        return None
+
+
 def decode_kind_roofline(shape, B, ctxs, kind, ms, n, peaks, peak_src):
     d, H, Hkv, hd, F, L, V = (shape.d_model, shape.n_head, shape.n_kv_head, shape.head_dim,
                               shape.d_mlp, shape.n_layer, shape.vocab)
@@ -366,7 +394,8 @@ def decode_kind_roofline(shape, B, ctxs, kind, ms, n, peaks, peak_src):
     total = per.get(kind, 0) * steps
     achieved = total / n / (ms / n / 1e3) / 1e9 if total else 0.0
     return {"bound": "hbm", "achieved": round(achieved, 1), "peak": peaks["hbm_gbs"],
-            "unit": "GB/s", "frac": round(achieved / peaks["hbm_gbs"], 4), "traffic": None,
+            "unit": "GB/s", "frac": round(achieved / peaks["hbm_gbs"], 4),
+            "traffic": recorded_traffic(kind), "algorithmic_bytes_per_launch": total / n if n else 0,
             "peak_source": f"{peak_src} HBM copy", "launch_ms": ms / n}
 
 
