@@ -98,3 +98,42 @@ def test_paths_agree(cuda_device):
 def test_many_steps_keep_barrier_state(cuda_device):
     """Forty steps in a row: the grid barrier counter carries over between launches."""
     _run(_small(synth.D20_MQA, n_layer=1, vocab=512), 3, 16, 40)
+
+
+def test_phase_trace_is_ordered(cuda_device):
+    """nc_decode_trace: barrier arrivals and exits of CTA 0 are in time order, the
+    producer marks precede the phases they load for, and a too-small buffer is
+    left untouched."""
+    import torch
+    shape = _small(synth.D20_MQA, n_layer=2, vocab=512)
+    W = synth.make_weights(shape)
+    B, T0 = 4, 40
+    model = nc.Model(W, max_seq=T0 + 2, max_batch=B)
+    nc.nc_model_set_decode_path(model.handle, nc.NC_DECODE_PERSISTENT)
+    cache = model.cache(B, T0 + 2)
+    toks = torch.from_numpy(synth.make_tokens(shape, B, T0 + 1)).cuda()
+    am = torch.empty(B, dtype=torch.int32, device="cuda")
+    nc.nc_prefill_last(model.handle, toks[:, :T0].contiguous(), B, T0, None, am, cache.handle)
+    n = nc.nc_decode_trace_entries(model.cfg)
+    nbar = 5 * shape.n_layer + 3
+    assert n >= 2 * nbar + 2
+    small = torch.full((n - 1,), -7, dtype=torch.int64, device="cuda")
+    nc.nc_decode_trace(model.handle, small)
+    nc.nc_decode_step(model.handle, toks[:, T0].contiguous(), B, T0, None, am, cache.handle)
+    torch.cuda.synchronize()
+    assert bool((small == -7).all()), "a buffer below the required size must not be written"
+    buf = torch.zeros(n, dtype=torch.int64, device="cuda")
+    nc.nc_decode_trace(model.handle, buf)
+    nc.nc_kv_cache_set_length(cache.handle, T0)
+    nc.nc_decode_step(model.handle, toks[:, T0].contiguous(), B, T0, None, am, cache.handle)
+    torch.cuda.synchronize()
+    nc.nc_decode_trace(model.handle, None)
+    t = buf.cpu().numpy()
+    main = t[: 2 * nbar + 2]
+    assert (np.diff(main) >= 0).all(), "barrier timestamps must be non-decreasing"
+    assert main[-1] > main[0]
+    marks = t[2 * nbar + 2:].reshape(-1, 6)
+    for k in range(2, nbar):   # producer started each streamed phase before it ended
+        if marks[k - 1, 4]:
+            assert marks[k - 1, 4] <= main[2 * k - 1]
+    assert nc.nc_model_check(model.handle) == nc.NC_OK

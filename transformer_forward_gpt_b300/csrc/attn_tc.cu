@@ -261,12 +261,17 @@ __global__ void __launch_bounds__(192, 1)
       const int kmax = qpos - j * kBk;   // keys i > kmax are masked on the diagonal tile
       float sv[128];
       tmem_ld128_sync(s_col, sv);
+      if (diag) {
+#pragma unroll
+        for (int i = 0; i < 128; ++i)
+          if (i > kmax) sv[i] = -INFINITY;
+      }
+      // max of the raw scores; the scale (> 0) is applied to the max and folded
+      // into the exponent's FMA below
       float mx = -INFINITY;
 #pragma unroll
-      for (int i = 0; i < 128; ++i) {
-        sv[i] = (diag && i > kmax) ? -INFINITY : sv[i] * a.scale_log2;
-        mx = fmaxf(mx, sv[i]);
-      }
+      for (int i = 0; i < 128; ++i) mx = fmaxf(mx, sv[i]);
+      mx *= a.scale_log2;
       // raise the reference only when the max outgrows it by 2^8
       const bool raise = mx > m_ref + 8.f;
       const float m_new = raise ? mx : m_ref;
@@ -276,7 +281,8 @@ __global__ void __launch_bounds__(192, 1)
       uint32_t pk[64];
 #pragma unroll
       for (int i = 0; i < 64; ++i) {
-        const float p0 = exp2f(sv[2 * i] - m_new), p1 = exp2f(sv[2 * i + 1] - m_new);
+        const float p0 = ex2_approx(fmaf(sv[2 * i], a.scale_log2, -m_new));
+        const float p1 = ex2_approx(fmaf(sv[2 * i + 1], a.scale_log2, -m_new));
         psum += p0 + p1;
         pk[i] = pack2<T16>(p0, p1);
       }

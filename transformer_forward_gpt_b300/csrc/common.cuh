@@ -63,6 +63,13 @@ template <class T> struct Fmt16;
 template <> struct Fmt16<bf16> { static constexpr uint32_t code = 1; };
 template <> struct Fmt16<f16> { static constexpr uint32_t code = 0; };
 
+// 2^x with the hardware's approximate exp2 (flush-to-zero; 2^-inf = 0).
+__device__ __forceinline__ float ex2_approx(float x) {
+  float y;
+  asm("ex2.approx.ftz.f32 %0, %1;" : "=f"(y) : "f"(x));
+  return y;
+}
+
 __device__ __forceinline__ float warp_sum(float v) {
 #pragma unroll
   for (int o = 16; o > 0; o >>= 1) v += __shfl_xor_sync(0xffffffffu, v, o);
