@@ -168,7 +168,7 @@ __global__ void __launch_bounds__(128) attn_decode_mma_kernel(
     for (int r = 0; r < 2; ++r) {
       mx[r] = fmaxf(mx[r], __shfl_xor_sync(0xffffffffu, mx[r], 1));
       mx[r] = fmaxf(mx[r], __shfl_xor_sync(0xffffffffu, mx[r], 2));
-      corr[r] = mx[r] == -INFINITY ? 1.f : exp2f((m_run[r] - mx[r]) * scale_log2);
+      corr[r] = mx[r] == -INFINITY ? 1.f : ex2_approx((m_run[r] - mx[r]) * scale_log2);
     }
     uint32_t a[4];
     {
@@ -178,7 +178,7 @@ __global__ void __launch_bounds__(128) attn_decode_mma_kernel(
 #pragma unroll
         for (int e = 0; e < 4; ++e) {
           const float m = mx[e / 2];
-          p[n][e] = m == -INFINITY ? 0.f : exp2f((s[n][e] - m) * scale_log2);
+          p[n][e] = m == -INFINITY ? 0.f : ex2_approx((s[n][e] - m) * scale_log2);
           rs[e / 2] += p[n][e];
         }
       a[0] = pack2<T16>(p[0][0], p[0][1]);
@@ -239,7 +239,7 @@ __global__ void __launch_bounds__(128) attn_decode_mma_kernel(
     float sc[4], L = 0.f;
 #pragma unroll
     for (int w = 0; w < 4; ++w) {
-      sc[w] = wm[w * 16 + r] == -INFINITY ? 0.f : exp2f((wm[w * 16 + r] - M) * scale_log2);
+      sc[w] = wm[w * 16 + r] == -INFINITY ? 0.f : ex2_approx((wm[w * 16 + r] - M) * scale_log2);
       L += sc[w] * wl[w * 16 + r];
     }
     float* rec = scratch + (((int64_t)b * H + g * G + r) * n_split + split) * (kHd + 2);

@@ -285,8 +285,8 @@ __global__ void __launch_bounds__(320, 1)
 #pragma unroll
         for (int i = 0; i < 16; ++i) {
           const int i0 = c * 32 + 2 * i;
-          const float p0 = (diag && i0 > kmax) ? 0.f : exp2f(v[2 * i] * a.scale_log2 - m_new);
-          const float p1 = (diag && i0 + 1 > kmax) ? 0.f : exp2f(v[2 * i + 1] * a.scale_log2 - m_new);
+          const float p0 = (diag && i0 > kmax) ? 0.f : ex2_approx(fmaf(v[2 * i], a.scale_log2, -m_new));
+          const float p1 = (diag && i0 + 1 > kmax) ? 0.f : ex2_approx(fmaf(v[2 * i + 1], a.scale_log2, -m_new));
           psum += p0 + p1;
           pk[c * 16 + i] = pack2<T16>(p0, p1);
         }

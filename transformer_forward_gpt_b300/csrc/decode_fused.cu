@@ -184,12 +184,13 @@ __device__ __forceinline__ void raise_abort(const Params& p) {
 // consumer thread, only while a trace buffer is set.
 __device__ __forceinline__ void trace_mark(const Params& p, int k, int m) {
   if (p.trace && blockIdx.x == 0 && threadIdx.x == 32)
-    p.trace[2 * p.nbar + 2 + 5 * (k - 1) + m] = global_timer_ns();
+    p.trace[2 * p.nbar + 2 + 6 * (k - 1) + m] = global_timer_ns();
 }
+
 // Producer mark: when CTA 0's producer starts issuing the loads of the phase
 // that ends at grid barrier k.
 __device__ __forceinline__ void trace_producer(const Params& p, int k) {
-  if (p.trace && blockIdx.x == 0) p.trace[2 * p.nbar + 2 + 5 * (k - 1) + 4] = global_timer_ns();
+  if (p.trace && blockIdx.x == 0) p.trace[2 * p.nbar + 2 + 6 * (k - 1) + 4] = global_timer_ns();
 }
 
 // Bounded wait on a ring barrier; false on timeout or abort.
@@ -417,7 +418,7 @@ __device__ void stage_act(const Params& p, const Shared& sh, const Gemv& g, int 
   // For ACT_X32 the squares of the columns in [ss_c0, ss_c1) are summed in a
   // register and added to g.ss_out; for ACT_H32 the token's norm scale is read
   // once before the loads.
-  constexpr int kBatch = 12;
+  constexpr int kBatch = 8;
   uint2* dst = reinterpret_cast<uint2*>(sh.act);
   const int tid = threadIdx.x - 32;
   const int lane = tid & 31;
@@ -606,12 +607,11 @@ __device__ bool consume_gemv(const Params& p, Shared& sh, const Gemv& g, int k) 
       bar_consumers();
       trace_mark(p, k, 0);
     }
-    // two accumulator sets (even / odd k16 step) halve the mma dependency chain
-    float acc[NT][4], acc2[NT][4];
+    float acc[NT][4];
 #pragma unroll
     for (int nt = 0; nt < NT; ++nt)
 #pragma unroll
-      for (int e = 0; e < 4; ++e) acc[nt][e] = acc2[nt][e] = 0.f;
+      for (int e = 0; e < 4; ++e) acc[nt][e] = 0.f;
     for (int kp = kp0; kp < kp1; ++kp) {
       const int ks = 2 * kp;
       if (!second && ks + 2 > win1) {   // run longer than the window: slide it
@@ -633,7 +633,7 @@ __device__ bool consume_gemv(const Params& p, Shared& sh, const Gemv& g, int k) 
           const uint2 b0 = bf[(ksl * NT + nt) * 32 + lane];
           const uint2 b1 = bf[((ksl + 1) * NT + nt) * 32 + lane];
           mma16816<T16>(acc[nt], a0.x, a0.y, a0.z, a0.w, b0.x, b0.y);
-          mma16816<T16>(acc2[nt], a1.x, a1.y, a1.z, a1.w, b1.x, b1.y);
+          mma16816<T16>(acc[nt], a1.x, a1.y, a1.z, a1.w, b1.x, b1.y);
         }
       }
       __syncwarp();
@@ -641,10 +641,6 @@ __device__ bool consume_gemv(const Params& p, Shared& sh, const Gemv& g, int k) 
       r.advance();
     }
     trace_mark(p, k, 1);
-#pragma unroll
-    for (int nt = 0; nt < NT; ++nt)
-#pragma unroll
-      for (int e = 0; e < 4; ++e) acc[nt][e] += acc2[nt][e];
     flush_rows<NT>(p, sh, g, grp * kUnitRows + warp * 16, acc);
     trace_mark(p, k, 2);
     if (grp == 0) ss_c0 = ss_c1 = 0;   // the columns are counted once
@@ -836,7 +832,7 @@ __device__ bool consume_attn(const Params& p, Shared& sh, int l, int k) {
           mx[h] = fmaxf(mx[h], __shfl_xor_sync(0xffffffffu, mx[h], 1));
           mx[h] = fmaxf(mx[h], __shfl_xor_sync(0xffffffffu, mx[h], 2));
           const float mn = fmaxf(m_r[h], mx[h]);
-          alpha[h] = exp2f(m_r[h] - mn);
+          alpha[h] = ex2_approx(m_r[h] - mn);
           m_r[h] = mn;
           l_r[h] *= alpha[h];
         }
@@ -845,7 +841,7 @@ __device__ bool consume_attn(const Params& p, Shared& sh, int l, int k) {
         for (int nt = 0; nt < 2; ++nt)
 #pragma unroll
           for (int e = 0; e < 4; ++e) {
-            pr[nt][e] = exp2f(s[nt][e] - m_r[e >> 1]);
+            pr[nt][e] = ex2_approx(s[nt][e] - m_r[e >> 1]);
             l_r[e >> 1] += pr[nt][e];
           }
 #pragma unroll
@@ -916,7 +912,7 @@ __device__ bool consume_attn(const Params& p, Shared& sh, int l, int k) {
       } else {
         for (int w = 0; w < kCons; ++w) {
           const float* base = reinterpret_cast<float*>(sh.act) + w * (16 * kMergeStride + 32);
-          const float sc = exp2f(base[h] - M);
+          const float sc = ex2_approx(base[h] - M);
           v += sc * (i == 1 ? base[16 + h] : base[32 + h * kMergeStride + (i - 2)]);
         }
       }
@@ -962,7 +958,7 @@ __device__ bool consume_attn(const Params& p, Shared& sh, int l, int k) {
         float L = 0.f;
         for (int s2 = 0; s2 < ns; ++s2) {
           const int rr = s2 * p.rec_stride + h * (kHd + 2);
-          const float e = exp2f(rec_at(rr) - M);
+          const float e = ex2_approx(rec_at(rr) - M);
           scl[s2 * G + h] = e;
           L += e * rec_at(rr + 1);
         }

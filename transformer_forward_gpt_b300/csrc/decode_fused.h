@@ -73,8 +73,8 @@ int attn_slots_needed(int B, int Hkv, int pos, int P);
 bool make_cache_map(CUtensorMap* map, void* base, uint64_t rows, bool half);
 // Grid barriers one launch passes (its arrivals are that times the grid size).
 inline int barriers_per_step(int L) { return 5 * L + 3; }
-// Entries of a full trace (barrier times plus 5 marks per phase).
-inline int trace_entries(int L) { return 7 * barriers_per_step(L) + 2; }
+// Entries of a full trace (barrier times plus 6 marks per phase).
+inline int trace_entries(int L) { return 8 * barriers_per_step(L) + 2; }
 // Enqueues one step for p.B <= kMaxTok sequences on `sms` CTAs (cooperative launch).
 nc_status launch_step(const CUtensorMap& tk, const CUtensorMap& tv, Params p, bool half,
                       nc_dtype wdt, int sms, cudaStream_t s);

@@ -233,15 +233,14 @@ __device__ __forceinline__ void epi_qkv(const GemmArgs& p, uint32_t taddr, int r
       }
       continue;
     }
+    // the head's 128 values in one TMEM load; mean square over the un-rotated values
+    float hv[128];
+    tmem_ld128_sync(base, hv);
     float ss = 0.f;
-#pragma unroll 1
-    for (int c = 0; c < 4; ++c) {
-      float v[32];
-      tmem_ld32_sync(base + c * 32, v);
 #pragma unroll
-      for (int i = 0; i < 32; ++i) ss = fmaf(v[i], v[i], ss);
-    }
+    for (int i = 0; i < 128; ++i) ss = fmaf(hv[i], hv[i], ss);
     const float r = rsqrtf(ss * (1.f / 128.f) + q.eps);
+    if (!valid) continue;
     T16* out;
     if (j < q.H)
       out = reinterpret_cast<T16*>(q.q) +
@@ -250,30 +249,28 @@ __device__ __forceinline__ void epi_qkv(const GemmArgs& p, uint32_t taddr, int r
       out = reinterpret_cast<T16*>(q.k_cache) + (((int64_t)b * q.Hkv + (j - q.H)) * q.t_max + t) * 128;
     const float* cs = q.cos_tab + (int64_t)t * 64;
     const float* sn = q.sin_tab + (int64_t)t * 64;
-#pragma unroll 1
-    for (int c = 0; c < 2; ++c) {
-      float lo[32], hi[32];
-      tmem_ld32_sync(base + c * 32, lo);
-      tmem_ld32_sync(base + 64 + c * 32, hi);
-      if (!valid) continue;
+    // pairs (i, i + 64) in four blocks of 16, each rotated, scaled and stored at once
 #pragma unroll
-      for (int i = 0; i < 8; ++i) {
-        const float4 c4 = *reinterpret_cast<const float4*>(cs + c * 32 + 4 * i);
-        const float4 s4 = *reinterpret_cast<const float4*>(sn + c * 32 + 4 * i);
+    for (int c = 0; c < 4; ++c) {
+      float lo[16], hi[16];
+#pragma unroll
+      for (int i4 = 0; i4 < 4; ++i4) {
+        const float4 c4 = *reinterpret_cast<const float4*>(cs + 16 * c + 4 * i4);
+        const float4 s4 = *reinterpret_cast<const float4*>(sn + 16 * c + 4 * i4);
         const float cc[4] = {c4.x, c4.y, c4.z, c4.w}, ssn[4] = {s4.x, s4.y, s4.z, s4.w};
 #pragma unroll
         for (int u = 0; u < 4; ++u) {
-          const float a = lo[4 * i + u], h = hi[4 * i + u];
-          lo[4 * i + u] = (a * cc[u] - h * ssn[u]) * r;
-          hi[4 * i + u] = (a * ssn[u] + h * cc[u]) * r;
+          const float a = hv[16 * c + 4 * i4 + u], h = hv[64 + 16 * c + 4 * i4 + u];
+          lo[4 * i4 + u] = (a * cc[u] - h * ssn[u]) * r;
+          hi[4 * i4 + u] = (a * ssn[u] + h * cc[u]) * r;
         }
       }
 #pragma unroll
-      for (int i = 0; i < 4; ++i) {
-        *reinterpret_cast<uint4*>(out + c * 32 + 8 * i) = make_uint4(
+      for (int i = 0; i < 2; ++i) {
+        *reinterpret_cast<uint4*>(out + 16 * c + 8 * i) = make_uint4(
             pack2<T16>(lo[8 * i], lo[8 * i + 1]), pack2<T16>(lo[8 * i + 2], lo[8 * i + 3]),
             pack2<T16>(lo[8 * i + 4], lo[8 * i + 5]), pack2<T16>(lo[8 * i + 6], lo[8 * i + 7]));
-        *reinterpret_cast<uint4*>(out + 64 + c * 32 + 8 * i) = make_uint4(
+        *reinterpret_cast<uint4*>(out + 64 + 16 * c + 8 * i) = make_uint4(
             pack2<T16>(hi[8 * i], hi[8 * i + 1]), pack2<T16>(hi[8 * i + 2], hi[8 * i + 3]),
             pack2<T16>(hi[8 * i + 4], hi[8 * i + 5]), pack2<T16>(hi[8 * i + 6], hi[8 * i + 7]));
       }
