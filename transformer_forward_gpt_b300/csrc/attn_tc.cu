@@ -1,15 +1,18 @@
 // Causal flash attention for prefill on tcgen05 (head_dim 128, 16-bit Q/K/V,
 // fp32 softmax and accumulation in TMEM), with grouped-query head sharing.
 //
-// CTA = 128 queries of one (sequence, query head); 192 threads:
+// CTA = 128 queries of one (sequence, query head); 320 threads:
 //   warp 0      TMA: the Q tile once, then K and V tiles of 128 keys into a
 //               two-stage ring (keys at or past T read as zeros)
 //   warp 1      TMEM owner; one thread issues S = Q K^T (M = N = K = 128) into
 //               one of two TMEM score buffers, and O += P V (P from shared
 //               memory, V as an MN-major operand) into the TMEM output
-//   warps 2..5  softmax: thread = query row = TMEM lane. Reads its score row,
-//               masks keys past the query on the diagonal tile, exponentiates
-//               in the log2 domain and writes P (16-bit) to shared memory.
+//   warps 2..9  softmax: warps w and w + 4 share the TMEM lane quarter w % 4
+//               (thread = query row) and split the row's 128 key columns in two
+//               halves; the pair exchanges row maxima through shared memory.
+//               A thread masks keys past the query on the diagonal tile,
+//               exponentiates in the log2 domain and writes its half of the P
+//               row (16-bit) to shared memory.
 // The running max used as the exponent's reference is only raised when a row's
 // max grows by more than 8 (log2 units): then that row of O is rescaled in TMEM.
 // Otherwise p <= 2^8 and the reference stays, which keeps O in TMEM untouched
@@ -41,7 +44,9 @@ constexpr int kOffK = kTile;
 constexpr int kOffV = 3 * kTile;
 constexpr int kOffP = 5 * kTile;
 constexpr int kOffBar = 6 * kTile;
-constexpr size_t kSmem = 6 * kTile + 256 + 1024;
+constexpr int kOffX = 6 * kTile + 256;        // [2 parity][128 rows][2 halves] row maxima
+constexpr int kOffL = kOffX + 2048;           // [128 rows][2 halves] final row sums
+constexpr size_t kSmem = 6 * kTile + 256 + 3072 + 1024;
 
 // TMEM columns: S[0] 0..127, S[1] 128..255, O 256..383
 constexpr uint32_t kColS0 = 0, kColO = 256, kTmemCols = 512;
@@ -98,7 +103,7 @@ struct AttnArgs {
 };
 
 template <class T16>
-__global__ void __launch_bounds__(192, 1)
+__global__ void __launch_bounds__(320, 1)
     attn_prefill_tc_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_constant__ CUtensorMap tmK,
                            const __grid_constant__ CUtensorMap tmV, const AttnArgs a, int layer) {
   extern __shared__ uint8_t smem_raw[];
@@ -116,6 +121,9 @@ __global__ void __launch_bounds__(192, 1)
   uint64_t* o_done = bars + 14;     // 1 (one commit per P V)
   uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(bars + 16);
   volatile int* abort_flag = reinterpret_cast<volatile int*>(bars + 17);
+  // [quarter][3]: the two softmax warps of a lane quarter exchange row maxima
+  // (slots 0, 1 by tile parity) and the final row sums (slot 2); 2 arrivals each
+  uint64_t* xbar = bars + 18;
 
   // heaviest query tiles first
   const int per_qt = a.B * a.H;
@@ -134,10 +142,11 @@ __global__ void __launch_bounds__(192, 1)
       mbar_init(&v_full[i], 1);
       mbar_init(&v_empty[i], 1);
       mbar_init(&s_full[i], 1);
-      mbar_init(&s_free[i], 4);
+      mbar_init(&s_free[i], 8);
     }
-    mbar_init(p_full, 4);
+    mbar_init(p_full, 8);
     mbar_init(o_done, 1);
+    for (int i = 0; i < 12; ++i) mbar_init(&xbar[i], 2);
     *abort_flag = 0;
     fence_mbar_init();
   }
@@ -244,10 +253,14 @@ __global__ void __launch_bounds__(192, 1)
   } else {
     // -------------------------------------------------------------- softmax
     const int quarter = warp % 4;
+    const int half = (warp - 2) / 4;          // key / output columns [64 half, 64 half + 64)
     const int row = quarter * 32 + lane;      // query row within the tile = TMEM lane
     const int qpos = qt * kBq + row;
     const uint32_t lane_base = (uint32_t)(quarter * 32) << 16;
     uint8_t* sP = smem + kOffP;
+    float* xch = reinterpret_cast<float*>(smem + kOffX);
+    float* xl = reinterpret_cast<float*>(smem + kOffL);
+    uint64_t* qbar = xbar + 3 * quarter;      // this quarter's exchange barriers
     float m_ref = -INFINITY, l_sum = 0.f;
     bool ok = true;
     for (int j = 0; j < n_kt; ++j) {
@@ -255,32 +268,37 @@ __global__ void __launch_bounds__(192, 1)
       ok = __all_sync(0xffffffffu, mbar_wait(&s_full[st], (j >> 1) & 1, a.status));
       if (!ok) break;
       tc_fence_after();
-      // the score row in one 128-column TMEM load; scale, causal mask, row max
-      const uint32_t s_col = tmem + lane_base + kColS0 + st * 128;
+      // this half of the score row in one 64-column TMEM load; causal mask
+      const uint32_t s_col = tmem + lane_base + kColS0 + st * 128 + 64 * half;
       const bool diag = j == qt;
-      const int kmax = qpos - j * kBk;   // keys i > kmax are masked on the diagonal tile
-      float sv[128];
-      tmem_ld128_sync(s_col, sv);
+      const int kmax = qpos - j * kBk - 64 * half;   // keys i > kmax are masked (diagonal)
+      float sv[64];
+      tmem_ld64_sync(s_col, sv);
       if (diag) {
 #pragma unroll
-        for (int i = 0; i < 128; ++i)
+        for (int i = 0; i < 64; ++i)
           if (i > kmax) sv[i] = -INFINITY;
       }
-      // max of the raw scores; the scale (> 0) is applied to the max and folded
-      // into the exponent's FMA below
+      // row max over both halves (raw scores; the scale > 0 is applied to the max
+      // and folded into the exponent's FMA), exchanged through shared memory
       float mx = -INFINITY;
 #pragma unroll
-      for (int i = 0; i < 128; ++i) mx = fmaxf(mx, sv[i]);
-      mx *= a.scale_log2;
+      for (int i = 0; i < 64; ++i) mx = fmaxf(mx, sv[i]);
+      xch[(st * 128 + row) * 2 + half] = mx;
+      __syncwarp();
+      if (lane == 0) mbar_arrive(&qbar[st]);
+      ok = __all_sync(0xffffffffu, mbar_wait(&qbar[st], (j >> 1) & 1, a.status));
+      if (!ok) break;
+      mx = fmaxf(mx, xch[(st * 128 + row) * 2 + (half ^ 1)]) * a.scale_log2;
       // raise the reference only when the max outgrows it by 2^8
       const bool raise = mx > m_ref + 8.f;
       const float m_new = raise ? mx : m_ref;
-      const float corr = raise ? exp2f(m_ref - m_new) : 1.f;   // 0 on the first tile
-      // p = 2^(s - m) packed to 16 bits in registers, row sum
+      const float corr = raise ? ex2_approx(m_ref - m_new) : 1.f;   // 0 on the first tile
+      // p = 2^(s - m) packed to 16 bits in registers, this half's row sum
       float psum = 0.f;
-      uint32_t pk[64];
+      uint32_t pk[32];
 #pragma unroll
-      for (int i = 0; i < 64; ++i) {
+      for (int i = 0; i < 32; ++i) {
         const float p0 = ex2_approx(fmaf(sv[2 * i], a.scale_log2, -m_new));
         const float p1 = ex2_approx(fmaf(sv[2 * i + 1], a.scale_log2, -m_new));
         psum += p0 + p1;
@@ -296,21 +314,22 @@ __global__ void __launch_bounds__(192, 1)
         ok = __all_sync(0xffffffffu, mbar_wait(o_done, (j - 1) & 1, a.status));
         if (!ok) break;
         tc_fence_after();
-        if (__any_sync(0xffffffffu, raise)) {
+        if (__any_sync(0xffffffffu, raise)) {   // this half of the O row
 #pragma unroll 1
-          for (int c = 0; c < 4; ++c) {
+          for (int c = 0; c < 2; ++c) {
             float v[32];
-            tmem_ld32_sync(tmem + lane_base + kColO + c * 32, v);
+            const uint32_t oc = tmem + lane_base + kColO + 64 * half + c * 32;
+            tmem_ld32_sync(oc, v);
 #pragma unroll
             for (int i = 0; i < 32; ++i) v[i] *= corr;
-            tmem_st32_sync(tmem + lane_base + kColO + c * 32, v);
+            tmem_st32_sync(oc, v);
           }
         }
       }
-      // P row -> shared memory (K-major, 128-byte swizzle)
+      // this half of the P row -> shared memory (K-major, 128-byte swizzle)
 #pragma unroll
-      for (int c = 0; c < 16; ++c)
-        *reinterpret_cast<uint4*>(sP + tile_off(row, c)) =
+      for (int c = 0; c < 8; ++c)
+        *reinterpret_cast<uint4*>(sP + tile_off(row, 8 * half + c)) =
             make_uint4(pk[4 * c], pk[4 * c + 1], pk[4 * c + 2], pk[4 * c + 3]);
       fence_proxy_async_smem();
       tc_fence_before();
@@ -318,21 +337,29 @@ __global__ void __launch_bounds__(192, 1)
       if (lane == 0) mbar_arrive(p_full);
     }
     if (ok) ok = __all_sync(0xffffffffu, mbar_wait(o_done, (n_kt - 1) & 1, a.status));
+    // the row sum is the two halves' sums (same reference max)
+    if (ok) {
+      xl[row * 2 + half] = l_sum;
+      __syncwarp();
+      if (lane == 0) mbar_arrive(&qbar[2]);
+      ok = __all_sync(0xffffffffu, mbar_wait(&qbar[2], 0, a.status));
+      if (ok) l_sum += xl[row * 2 + (half ^ 1)];
+    }
     if (ok) {
       tc_fence_after();
-      // O / l -> out[b, qpos, h*128 ..]; staged through this warp's 32 rows of the
-      // (now idle) P buffer (256-byte rows, 16-byte chunks XOR-swizzled by row) so
-      // that each row's 256 bytes go out in one pass
+      // O / l for output columns [64 half, 64 half + 64) -> out[b, qpos, h*128 ..];
+      // staged through this warp's 4 KB of the (idle) P buffer (128-byte rows,
+      // 16-byte chunks XOR-swizzled by row), then 8 lanes per row
       const float inv = 1.f / l_sum;
-      uint8_t* stage = sP + quarter * 32 * 256;
+      uint8_t* stage = sP + (warp - 2) * 32 * 128;
 #pragma unroll 1
-      for (int c = 0; c < 4; ++c) {
+      for (int c = 0; c < 2; ++c) {
         float v[32];
-        tmem_ld32_sync(tmem + lane_base + kColO + c * 32, v);
+        tmem_ld32_sync(tmem + lane_base + kColO + 64 * half + c * 32, v);
 #pragma unroll
         for (int i = 0; i < 4; ++i) {
           const int chunk = c * 4 + i;
-          *reinterpret_cast<uint4*>(stage + lane * 256 + ((chunk ^ (lane & 15)) << 4)) =
+          *reinterpret_cast<uint4*>(stage + lane * 128 + ((chunk ^ (lane & 7)) << 4)) =
               make_uint4(pack2<T16>(v[8 * i] * inv, v[8 * i + 1] * inv),
                          pack2<T16>(v[8 * i + 2] * inv, v[8 * i + 3] * inv),
                          pack2<T16>(v[8 * i + 4] * inv, v[8 * i + 5] * inv),
@@ -342,12 +369,13 @@ __global__ void __launch_bounds__(192, 1)
       __syncwarp();
       T16* out = static_cast<T16*>(a.o);
 #pragma unroll 1
-      for (int it = 0; it < 16; ++it) {
-        const int r = it * 2 + lane / 16, cc = lane % 16;
+      for (int it = 0; it < 8; ++it) {
+        const int r = it * 4 + lane / 8, cc = lane % 8;
         const int t = qt * kBq + quarter * 32 + r;
         if (t < a.T)
-          *reinterpret_cast<uint4*>(out + ((int64_t)b * a.T + t) * (a.H * kHd) + h * kHd + cc * 8) =
-              *reinterpret_cast<const uint4*>(stage + r * 256 + ((cc ^ (r & 15)) << 4));
+          *reinterpret_cast<uint4*>(out + ((int64_t)b * a.T + t) * (a.H * kHd) + h * kHd +
+                                    64 * half + cc * 8) =
+              *reinterpret_cast<const uint4*>(stage + r * 128 + ((cc ^ (r & 7)) << 4));
       }
     } else {
       *abort_flag = 1;
@@ -451,7 +479,7 @@ nc_status tc_attention_prefill_tc(const void* q, const void* k, const void* v, v
         return NC_ERR_CUDA;
       cfg = true;
     }
-    attn_prefill_tc_kernel<f16><<<grid, 192, kSmem, s>>>(mq, mk, mv, a, layer);
+    attn_prefill_tc_kernel<f16><<<grid, 320, kSmem, s>>>(mq, mk, mv, a, layer);
   } else {
     static bool cfg = false;
     if (!cfg) {
@@ -460,7 +488,7 @@ nc_status tc_attention_prefill_tc(const void* q, const void* k, const void* v, v
         return NC_ERR_CUDA;
       cfg = true;
     }
-    attn_prefill_tc_kernel<bf16><<<grid, 192, kSmem, s>>>(mq, mk, mv, a, layer);
+    attn_prefill_tc_kernel<bf16><<<grid, 320, kSmem, s>>>(mq, mk, mv, a, layer);
   }
   count_launches(1);
   return cudaGetLastError() == cudaSuccess ? NC_OK : NC_ERR_CUDA;

@@ -145,6 +145,39 @@ __host__ __device__ __forceinline__ int owner_of(int64_t total, int64_t f, int P
   return total < P ? (int)f : (int)(((f + 1) * P - 1) / total);
 }
 
+// Attention work: tiles of 16 positions over (sequence, KV head) pairs bg. With no
+// more pairs than CTAs, every pair gets its own consecutive block of
+// floor or ceil(P / pairs) CTAs and each CTA one contiguous tile range of one pair
+// (one partial state per CTA); otherwise the flattened (pair, tile) space is
+// shared evenly. attn_work gives CTA c's flattened range [f0, f1) (f = bg * T16 +
+// tile); attn_group the CTAs holding tiles of pair bg: c_first, c_first + 1, ...
+// (ns of them).
+__host__ __device__ __forceinline__ void attn_work(int bhkv, int T16, int c, int P, int64_t& f0,
+                                                   int64_t& f1) {
+  if (bhkv <= P) {
+    const int bg = (int)(((int64_t)(c + 1) * bhkv - 1) / P);
+    const int cs = (int)((int64_t)bg * P / bhkv), ce = (int)((int64_t)(bg + 1) * P / bhkv);
+    int64_t j0, j1;
+    share(T16, c - cs, ce - cs, j0, j1);
+    f0 = (int64_t)bg * T16 + j0;
+    f1 = (int64_t)bg * T16 + j1;
+  } else {
+    share((int64_t)bhkv * T16, c, P, f0, f1);
+  }
+}
+__host__ __device__ __forceinline__ void attn_group(int bhkv, int T16, int bg, int P, int& c_first,
+                                                    int& ns) {
+  if (bhkv <= P) {
+    c_first = (int)((int64_t)bg * P / bhkv);
+    const int n = (int)((int64_t)(bg + 1) * P / bhkv) - c_first;
+    ns = n < T16 ? n : T16;
+  } else {
+    const int64_t total = (int64_t)bhkv * T16;
+    c_first = owner_of(total, (int64_t)bg * T16, P);
+    ns = owner_of(total, (int64_t)bg * T16 + T16 - 1, P) - c_first + 1;
+  }
+}
+
 // ------------------------------------------------------------------- state
 struct Ring {
   uint8_t* base;
@@ -349,9 +382,8 @@ __device__ void produce_gemv(const Params& p, Ring& r, const Gemv& g, uint64_t p
 __device__ void produce_attn(const Params& p, Ring& r, const CUtensorMap* tk, const CUtensorMap* tv,
                              int l, uint64_t pol, bool& ok) {
   const int T16 = attn_tiles(p);
-  const int64_t total = (int64_t)p.B * p.Hkv * T16;
   int64_t f0, f1;
-  share(total, blockIdx.x, gridDim.x, f0, f1);
+  attn_work(p.B * p.Hkv, T16, blockIdx.x, gridDim.x, f0, f1);
   for (int64_t f = f0; f < f1 && ok; ++f) {
     const int j = (int)(f % T16);
     const int bg = (int)(f / T16);
@@ -687,9 +719,8 @@ __device__ bool consume_attn(const Params& p, Shared& sh, int l, int k) {
   const int gq = lane >> 2, tq = lane & 3;
   Ring& r = sh.ring;
   const int T16n = attn_tiles(p);
-  const int64_t total = (int64_t)p.B * p.Hkv * T16n;
   int64_t f0, f1;
-  share(total, blockIdx.x, gridDim.x, f0, f1);
+  attn_work(p.B * p.Hkv, T16n, blockIdx.x, gridDim.x, f0, f1);
   const int G = p.H / p.Hkv;
   const int qd = p.H * kHd, kvd = p.Hkv * kHd;
   const float* acc_l = p.qkv_acc + (int64_t)(l & 1) * kMaxTok * p.nqkv_pad;
@@ -897,8 +928,9 @@ __device__ bool consume_attn(const Params& p, Shared& sh, int l, int k) {
     }
     bar_consumers();
     // partial record of this CTA for (b, g): per head [m, l, o[128]]
-    const int c_first = owner_of(total, (int64_t)bg * T16n, gridDim.x);
-    const int c_last = owner_of(total, (int64_t)bg * T16n + T16n - 1, gridDim.x);
+    int c_first, n_slots;
+    attn_group(p.B * p.Hkv, T16n, bg, gridDim.x, c_first, n_slots);
+    const int c_last = c_first + n_slots - 1;
     const int slot = blockIdx.x - c_first;
     float* rec = p.attn_part + ((int64_t)bg * p.attn_slots + slot) * p.rec_stride;
     for (int e = tid; e < G * (kHd + 2); e += 256) {
@@ -1289,11 +1321,11 @@ bool supported(int d, int H, int Hkv, int F, int hd) {
 // Largest number of partial-state slots any (sequence, KV head) gets.
 int attn_slots_needed(int B, int Hkv, int pos, int P) {
   const int T16 = (pos + 1 + 15) / 16;
-  const int64_t total = (int64_t)B * Hkv * T16;
   int best = 1;
   for (int bg = 0; bg < B * Hkv; ++bg) {
-    const int64_t fa = (int64_t)bg * T16, fb = fa + T16 - 1;
-    best = std::max(best, owner_of(total, fb, P) - owner_of(total, fa, P) + 1);
+    int c_first, ns;
+    attn_group(B * Hkv, T16, bg, P, c_first, ns);
+    best = std::max(best, ns);
   }
   return best;
 }
