@@ -86,6 +86,8 @@ struct nc_model {
   std::vector<const void*> wq, wk, wv, wo, w_fc, w_proj;
   float* cos_tab = nullptr;  // [max_seq, hd/2]
   float* sin_tab = nullptr;
+  float* cos_t = nullptr;    // [hd/2, max_seq]: consecutive positions adjacent
+  float* sin_t = nullptr;
   uint32_t* status = nullptr;
   // workspace
   void* ws = nullptr;
@@ -245,6 +247,8 @@ void nc_model_destroy(nc_model* m) {
   cudaFree(m->ws);
   cudaFree(m->cos_tab);
   cudaFree(m->sin_tab);
+  cudaFree(m->cos_t);
+  cudaFree(m->sin_t);
   cudaFree(m->status);
   cudaSetDevice(prev);
   delete m;
@@ -285,21 +289,28 @@ nc_status nc_model_create(const nc_config* cfg, const nc_weights* w, nc_model** 
   };
   // cos/sin tables: fp64 on the host, stored fp32 ("precomputed and kept in GPU memory")
   const int half = cfg->head_dim / 2, S = cfg->max_seq;
-  std::vector<float> c(size_t(S) * half), s(size_t(S) * half);
+  // The position-minor copies serve the prefill Q/K epilogue, where the 32 lanes
+  // of a warp hold 32 consecutive positions: one table entry for all of them is
+  // one 128-byte line instead of 32.
+  std::vector<float> c(size_t(S) * half), s(size_t(S) * half), ct(c.size()), snt(s.size());
   for (int t = 0; t < S; ++t)
     for (int i = 0; i < half; ++i) {
       const double theta = (double)t * pow((double)cfg->rope_base, -2.0 * i / cfg->head_dim);
-      c[size_t(t) * half + i] = (float)cos(theta);
-      s[size_t(t) * half + i] = (float)sin(theta);
+      c[size_t(t) * half + i] = ct[size_t(i) * S + t] = (float)cos(theta);
+      s[size_t(t) * half + i] = snt[size_t(i) * S + t] = (float)sin(theta);
     }
   if (cudaMalloc(&m->cos_tab, c.size() * 4) != cudaSuccess ||
       cudaMalloc(&m->sin_tab, s.size() * 4) != cudaSuccess ||
+      cudaMalloc(&m->cos_t, ct.size() * 4) != cudaSuccess ||
+      cudaMalloc(&m->sin_t, snt.size() * 4) != cudaSuccess ||
       cudaMalloc(&m->status, 256) != cudaSuccess) {
     set_err("allocation of tables failed");
     return fail(NC_ERR_OOM);
   }
   if (cudaMemcpy(m->cos_tab, c.data(), c.size() * 4, cudaMemcpyHostToDevice) != cudaSuccess ||
       cudaMemcpy(m->sin_tab, s.data(), s.size() * 4, cudaMemcpyHostToDevice) != cudaSuccess ||
+      cudaMemcpy(m->cos_t, ct.data(), ct.size() * 4, cudaMemcpyHostToDevice) != cudaSuccess ||
+      cudaMemcpy(m->sin_t, snt.data(), snt.size() * 4, cudaMemcpyHostToDevice) != cudaSuccess ||
       cudaMemset(m->status, 0, 256) != cudaSuccess) {
     set_err("upload of tables failed");
     return fail(NC_ERR_CUDA);
@@ -482,7 +493,8 @@ nc_status run_blocks(nc_model* m, nc_kv_cache* c, int B, int rows_per_seq, int p
   RowMap rm{rows_per_seq, pos0};
   for (int l = 0; l < cfg.n_layer; ++l) {
     QkvDst dst{m->q, layer_ptr(c->k, c->layer_elems, l, dt), layer_ptr(c->v, c->layer_elems, l, dt),
-               H, Hkv, hd, c->t_max, m->cos_tab, m->sin_tab, cfg.rms_eps};
+               H, Hkv, hd, c->t_max, m->cos_tab, m->sin_tab, cfg.rms_eps,
+               m->cos_t, m->sin_t, cfg.max_seq};
     // Q/K/V projections + RoPE + QK norm + cache write
     {
     ProfScope ps(m, NC_K_QKV, s);

@@ -30,6 +30,9 @@ struct QkvDst {
   const float* cos_tab;   // [max_seq, hd/2]
   const float* sin_tab;
   float eps;
+  const float* cos_t;     // the same tables position-minor: [hd/2, max_seq]
+  const float* sin_t;
+  int32_t tab_ld;         // max_seq
 };
 
 // ---- CUDA-core kernels (simt.cu)

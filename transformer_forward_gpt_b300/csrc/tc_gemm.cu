@@ -247,23 +247,21 @@ __device__ __forceinline__ void epi_qkv(const GemmArgs& p, uint32_t taddr, int r
             (((int64_t)b * q.H + j) * p.rm.rows_per_seq + (t - p.rm.pos0)) * 128;
     else
       out = reinterpret_cast<T16*>(q.k_cache) + (((int64_t)b * q.Hkv + (j - q.H)) * q.t_max + t) * 128;
-    const float* cs = q.cos_tab + (int64_t)t * 64;
-    const float* sn = q.sin_tab + (int64_t)t * 64;
+    // position-minor tables: entry i of position t at [i * ld + t], so the warp's
+    // 32 consecutive positions read one line per entry
+    const float* cs = q.cos_t + t;
+    const float* sn = q.sin_t + t;
+    const int64_t ld = q.tab_ld;
     // pairs (i, i + 64) in four blocks of 16, each rotated, scaled and stored at once
 #pragma unroll
     for (int c = 0; c < 4; ++c) {
       float lo[16], hi[16];
 #pragma unroll
-      for (int i4 = 0; i4 < 4; ++i4) {
-        const float4 c4 = *reinterpret_cast<const float4*>(cs + 16 * c + 4 * i4);
-        const float4 s4 = *reinterpret_cast<const float4*>(sn + 16 * c + 4 * i4);
-        const float cc[4] = {c4.x, c4.y, c4.z, c4.w}, ssn[4] = {s4.x, s4.y, s4.z, s4.w};
-#pragma unroll
-        for (int u = 0; u < 4; ++u) {
-          const float a = hv[16 * c + 4 * i4 + u], h = hv[64 + 16 * c + 4 * i4 + u];
-          lo[4 * i4 + u] = (a * cc[u] - h * ssn[u]) * r;
-          hi[4 * i4 + u] = (a * ssn[u] + h * cc[u]) * r;
-        }
+      for (int u = 0; u < 16; ++u) {
+        const float cc = __ldg(cs + (16 * c + u) * ld), sv = __ldg(sn + (16 * c + u) * ld);
+        const float a = hv[16 * c + u], h = hv[64 + 16 * c + u];
+        lo[u] = (a * cc - h * sv) * r;
+        hi[u] = (a * sv + h * cc) * r;
       }
 #pragma unroll
       for (int i = 0; i < 2; ++i) {
