@@ -83,10 +83,17 @@ def _attn_inputs(rng, B, H, Hkv, T, t_max, hd, dt):
     return q, k, v
 
 
-@pytest.mark.parametrize("B,H,Hkv,T,dt", [(2, 4, 2, 200, nc.NC_BF16), (1, 10, 1, 129, nc.NC_F16),
-                                          (3, 2, 2, 64, nc.NC_F16), (1, 3, 3, 1, nc.NC_F16),
-                                          (2, 13, 13, 300, nc.NC_F16), (2, 4, 4, 37, nc.NC_F32)])
-def test_attention_prefill(cuda_device, B, H, Hkv, T, dt):
+@pytest.mark.parametrize("B,H,Hkv,T,dt,qscale", [
+    (2, 4, 2, 200, nc.NC_BF16, 1.0), (1, 10, 1, 129, nc.NC_F16, 1.0),
+    (3, 2, 2, 64, nc.NC_F16, 1.0), (1, 3, 3, 1, nc.NC_F16, 1.0),
+    (2, 13, 13, 300, nc.NC_F16, 1.0), (2, 4, 4, 37, nc.NC_F32, 1.0),
+    # more (query tile, head) items than SMs: the persistent kernel runs several
+    # items per CTA, with ragged last query / key tiles
+    (2, 16, 4, 1037, nc.NC_F16, 1.0), (1, 40, 8, 777, nc.NC_BF16, 1.0),
+    # large scores: row maxima keep outgrowing the exponent's reference, so the
+    # output rows are rescaled in tensor memory many times
+    (1, 24, 2, 900, nc.NC_F16, 6.0)])
+def test_attention_prefill(cuda_device, B, H, Hkv, T, dt, qscale):
     """Bound: the output is rounded once (u |o|) and the probabilities are rounded
     to the operand format before P V (u max|v| at most); fp32 elsewhere."""
     import torch
@@ -94,6 +101,7 @@ def test_attention_prefill(cuda_device, B, H, Hkv, T, dt):
     t_max = T + 5
     rng = np.random.default_rng(T)
     q, k, v = _attn_inputs(rng, B, H, Hkv, T, t_max, hd, dt)
+    q *= qscale
     o = torch.empty(B, T, H * hd, device="cuda", dtype=q.dtype)
     nc.nc_op_attention_prefill(q, k, v, o, B, H, Hkv, T, t_max, hd, dt)
     torch.cuda.synchronize()

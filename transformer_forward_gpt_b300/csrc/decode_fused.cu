@@ -933,22 +933,37 @@ __device__ bool consume_attn(const Params& p, Shared& sh, int l, int k) {
     const int c_last = c_first + n_slots - 1;
     const int slot = blockIdx.x - c_first;
     float* rec = p.attn_part + ((int64_t)bg * p.attn_slots + slot) * p.rec_stride;
-    for (int e = tid; e < G * (kHd + 2); e += 256) {
-      const int h = e / (kHd + 2), i = e % (kHd + 2);
+    float* const mall = reinterpret_cast<float*>(sh.act);
+    constexpr int kWs = 16 * kMergeStride + 32;   // floats per warp's merge area
+    // one thread per head: the CTA's max M and sum L, and each warp's weight
+    // 2^(m_w - M), which replaces m_w in place (only this thread touches column h)
+    if (tid < G) {
+      const int h = tid;
+      float mwv[kCons];
       float M = -INFINITY;
-      for (int w = 0; w < kCons; ++w)
-        M = fmaxf(M, reinterpret_cast<float*>(sh.act)[w * (16 * kMergeStride + 32) + h]);
-      float v = 0.f;
-      if (i == 0) {
-        v = M;
-      } else {
-        for (int w = 0; w < kCons; ++w) {
-          const float* base = reinterpret_cast<float*>(sh.act) + w * (16 * kMergeStride + 32);
-          const float sc = ex2_approx(base[h] - M);
-          v += sc * (i == 1 ? base[16 + h] : base[32 + h * kMergeStride + (i - 2)]);
-        }
+#pragma unroll
+      for (int w = 0; w < kCons; ++w) {
+        mwv[w] = mall[w * kWs + h];
+        M = fmaxf(M, mwv[w]);
       }
-      rec[e] = v;
+      float L = 0.f;
+#pragma unroll
+      for (int w = 0; w < kCons; ++w) {
+        const float sc = ex2_approx(mwv[w] - M);
+        L = fmaf(sc, mall[w * kWs + 16 + h], L);
+        mall[w * kWs + h] = sc;
+      }
+      rec[h * (kHd + 2)] = M;
+      rec[h * (kHd + 2) + 1] = L;
+    }
+    bar_consumers();
+    for (int e = tid; e < G * kHd; e += 256) {
+      const int h = e / kHd, i = e % kHd;
+      float v = 0.f;
+#pragma unroll
+      for (int w = 0; w < kCons; ++w)
+        v = fmaf(mall[w * kWs + h], mall[w * kWs + 32 + h * kMergeStride + i], v);
+      rec[h * (kHd + 2) + 2 + i] = v;
     }
     __threadfence();
     bar_consumers();
