@@ -62,7 +62,8 @@ constexpr int kOffV = (1 + kKring) * kTile;
 constexpr int kOffBar = (1 + kKring + kVring) * kTile;
 constexpr int kOffX = kOffBar + 512;          // [2 parity][128 rows][2 halves] row maxima
 constexpr int kOffL = kOffX + 2048;           // [128 rows][2 halves] final row sums
-constexpr size_t kSmem = kOffL + 1024 + 1024; // + alignment slack of the base
+constexpr int kOffF = kOffL + 1024;           // [8 softmax warps] row-max flags (tile count)
+constexpr size_t kSmem = kOffF + 64 + 1024;   // + alignment slack of the base
 
 // TMEM columns: S/P buffers 0..383 (128 each), O 384..511
 constexpr uint32_t kColO = kSbuf * 128, kTmemCols = 512;
@@ -114,6 +115,33 @@ __device__ __forceinline__ void tmem_st32_sync(uint32_t taddr, const uint32_t (&
       "r"(v[0]), "r"(v[1]), "r"(v[2]), "r"(v[3]), "r"(v[4]), "r"(v[5]), "r"(v[6]), "r"(v[7]), "r"(v[8]), "r"(v[9]), "r"(v[10]), "r"(v[11]), "r"(v[12]), "r"(v[13]), "r"(v[14]), "r"(v[15]), "r"(v[16]), "r"(v[17]), "r"(v[18]), "r"(v[19]), "r"(v[20]), "r"(v[21]), "r"(v[22]), "r"(v[23]), "r"(v[24]), "r"(v[25]), "r"(v[26]), "r"(v[27]), "r"(v[28]), "r"(v[29]), "r"(v[30]), "r"(v[31])
       : "memory");
 }
+// Shared-memory word with release / acquire semantics at CTA scope.
+__device__ __forceinline__ void st_release_cta(uint32_t* p, uint32_t v) {
+  asm volatile("st.release.cta.shared::cta.u32 [%0], %1;" ::"r"(smem_u32(p)), "r"(v) : "memory");
+}
+__device__ __forceinline__ uint32_t ld_acquire_cta(const uint32_t* p) {
+  uint32_t v;
+  asm volatile("ld.acquire.cta.shared::cta.u32 %0, [%1];" : "=r"(v) : "r"(smem_u32(p)) : "memory");
+  return v;
+}
+// Waits until *flag >= target (a counter another warp of the CTA raises).
+// Bounded like every other wait: sets ST_TIMEOUT and returns false after kWaitLimitNs.
+__device__ __forceinline__ bool flag_wait(const uint32_t* flag, uint32_t target, uint32_t* status) {
+  if (ld_acquire_cta(flag) >= target) return true;
+  const uint64_t t0 = global_timer_ns();
+  while (true) {
+    // back off between polls: the partner warp shares this SM sub-partition
+    for (int i = 0; i < 32; ++i) {
+      __nanosleep(20);
+      if (ld_acquire_cta(flag) >= target) return true;
+    }
+    if (global_timer_ns() - t0 > kWaitLimitNs) {
+      atomicOr(status, ST_TIMEOUT);
+      return false;
+    }
+  }
+}
+
 struct AttnArgs {
   int B, H, Hkv, T, n_qt, n_items;
   float scale_log2;
@@ -161,8 +189,8 @@ __global__ void __launch_bounds__(kThreads, 1)
   // buffer), as parity waits require.
   uint64_t* o_done = bars + 18;
   uint64_t* o_free = bars + 21;     // 1: the item's O has been read out (8 softmax warps)
-  // [quarter][3]: the two softmax warps of a lane quarter exchange row maxima
-  // (slots 0, 1 by tile parity) and the final row sums (slot 2); 2 arrivals each
+  // [quarter][3]: the two softmax warps of a lane quarter exchange the final row
+  // sums through slot 2 (2 arrivals; slots 0 and 1 unused)
   uint64_t* xbar = bars + 22;       // 12
   uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(bars + 34);
   volatile int* abort_flag = reinterpret_cast<volatile int*>(bars + 35);
@@ -189,6 +217,7 @@ __global__ void __launch_bounds__(kThreads, 1)
     mbar_init(o_free, 8);
     for (int i = 0; i < 12; ++i) mbar_init(&xbar[i], 2);
     *abort_flag = 0;
+    for (int i = 0; i < 8; ++i) reinterpret_cast<uint32_t*>(smem + kOffF)[i] = 0u;
     fence_mbar_init();
   }
   if (warp == 1) {
@@ -211,7 +240,7 @@ __global__ void __launch_bounds__(kThreads, 1)
       bool ok = true;
       int n_items_here = 0;
       auto load_k = [&](int j, int bg) -> bool {
-        if (!mbar_wait(&k_empty[kp.slot()], kp.par() ^ 1u, a.status)) return false;
+        if (!mbar_wait_sleep(&k_empty[kp.slot()], kp.par() ^ 1u, a.status)) return false;
         uint8_t* d = smem + kOffK + kp.slot() * kTile;
         mbar_arrive_expect_tx(&k_full[kp.slot()], kTile);
         tma_load_4d(d, &tmK, &k_full[kp.slot()], 0, j * kBk, bg, layer);
@@ -220,7 +249,7 @@ __global__ void __launch_bounds__(kThreads, 1)
         return true;
       };
       auto load_v = [&](int j, int bg) -> bool {
-        if (!mbar_wait(&v_empty[vp.slot()], vp.par() ^ 1u, a.status)) return false;
+        if (!mbar_wait_sleep(&v_empty[vp.slot()], vp.par() ^ 1u, a.status)) return false;
         uint8_t* d = smem + kOffV + vp.slot() * kTile;
         mbar_arrive_expect_tx(&v_full[vp.slot()], kTile);
         tma_load_4d(d, &tmV, &v_full[vp.slot()], 0, j * kBk, bg, layer);
@@ -235,7 +264,7 @@ __global__ void __launch_bounds__(kThreads, 1)
         const int bg = (bh / a.H) * a.Hkv + (bh % a.H) / (a.H / a.Hkv);
         const int n = qt + 1;
         // Q of the previous item is no longer read once its last S is done
-        if (k > 0 && !mbar_wait(q_empty, (k - 1) & 1, a.status)) { ok = false; break; }
+        if (k > 0 && !mbar_wait_sleep(q_empty, (k - 1) & 1, a.status)) { ok = false; break; }
         mbar_arrive_expect_tx(q_full, kTile);
         tma_load_3d(smem + kOffQ, &tmQ, q_full, 0, qt * kBq, bh);
         tma_load_3d(smem + kOffQ + kHalf, &tmQ, q_full, 64, qt * kBq, bh);
@@ -250,11 +279,11 @@ __global__ void __launch_bounds__(kThreads, 1)
       }
       if (!ok) *abort_flag = 1;
       // copies in flight must land before shared memory is released
-      if (n_items_here > 0) mbar_wait(q_full, (n_items_here - 1) & 1, a.status);
+      if (n_items_here > 0) mbar_wait_sleep(q_full, (n_items_here - 1) & 1, a.status);
       for (uint32_t i = kp.i > kKring ? kp.i - kKring : 0; i < kp.i; ++i)
-        mbar_wait(&k_full[i % kKring], (i / kKring) & 1u, a.status);
+        mbar_wait_sleep(&k_full[i % kKring], (i / kKring) & 1u, a.status);
       for (uint32_t i = vp.i > kVring ? vp.i - kVring : 0; i < vp.i; ++i)
-        mbar_wait(&v_full[i % kVring], (i / kVring) & 1u, a.status);
+        mbar_wait_sleep(&v_full[i % kVring], (i / kVring) & 1u, a.status);
     }
   } else if (warp == 1) {
     if (lane == 0) {
@@ -268,14 +297,14 @@ __global__ void __launch_bounds__(kThreads, 1)
         const int item = item_of(k, c, G, a.n_items);
         if (item < 0 || *abort_flag) break;
         const int n = a.n_qt - item / per_qt;
-        if (!mbar_wait(q_full, k & 1, a.status)) { ok = false; break; }
+        if (!mbar_wait_sleep(q_full, k & 1, a.status)) { ok = false; break; }
         for (int j = 0; j < n; ++j) {
           const uint32_t gg = g + j;
           // the buffer's previous user is P V of tile gg - 3 (phase (gg-3)/3 of
           // its barrier; this thread waits on every phase of it in order)
           if ((gg >= kSbuf &&
-               !mbar_wait(&o_done[gg % kSbuf], ((gg - kSbuf) / kSbuf) & 1u, a.status)) ||
-              !mbar_wait(&k_full[kp.slot()], kp.par(), a.status)) {
+               !mbar_wait_sleep(&o_done[gg % kSbuf], ((gg - kSbuf) / kSbuf) & 1u, a.status)) ||
+              !mbar_wait_sleep(&k_full[kp.slot()], kp.par(), a.status)) {
             ok = false;
             break;
           }
@@ -313,9 +342,9 @@ __global__ void __launch_bounds__(kThreads, 1)
           const uint32_t gg = g + j;
           // P of the tile in TMEM; the first product of an item overwrites O, so
           // the previous item's O must have been read out
-          if (!mbar_wait(&p_full[gg % kSbuf], (gg / kSbuf) & 1u, a.status) ||
-              (j == 0 && k > 0 && !mbar_wait(o_free, (k - 1) & 1, a.status)) ||
-              !mbar_wait(&v_full[vp.slot()], vp.par(), a.status)) {
+          if (!mbar_wait_sleep(&p_full[gg % kSbuf], (gg / kSbuf) & 1u, a.status) ||
+              (j == 0 && k > 0 && !mbar_wait_sleep(o_free, (k - 1) & 1, a.status)) ||
+              !mbar_wait_sleep(&v_full[vp.slot()], vp.par(), a.status)) {
             ok = false;
             break;
           }
@@ -347,6 +376,11 @@ __global__ void __launch_bounds__(kThreads, 1)
     float* xch = reinterpret_cast<float*>(smem + kOffX);
     float* xl = reinterpret_cast<float*>(smem + kOffL);
     uint64_t* qbar = xbar + 3 * quarter;      // this quarter's exchange barriers
+    // row-max flags: warp w publishes the count of tiles whose maxima it has
+    // written; its partner (same lane quarter, other half) is warp w +- 4
+    uint32_t* flags = reinterpret_cast<uint32_t*>(smem + kOffF);
+    uint32_t* my_flag = flags + (warp - 2);
+    const uint32_t* partner_flag = flags + ((warp - 2) ^ 4);
     T16* out = static_cast<T16*>(a.o);
     uint32_t g = 0;
     bool ok = true;
@@ -375,30 +409,39 @@ __global__ void __launch_bounds__(kThreads, 1)
         }
         // row max over both halves (raw scores; the scale > 0 is applied to the max
         // and folded into the exponent's FMA), exchanged through shared memory
-        float mx = -INFINITY;
+        // (a tree: eight independent partial maxima, then three levels)
+        float m8[8];
 #pragma unroll
-        for (int i = 0; i < 64; ++i) mx = fmaxf(mx, sv[i]);
+        for (int u = 0; u < 8; ++u) m8[u] = sv[u];
+#pragma unroll
+        for (int i = 8; i < 64; ++i) m8[i & 7] = fmaxf(m8[i & 7], sv[i]);
+#pragma unroll
+        for (int w = 4; w >= 1; w >>= 1)
+#pragma unroll
+          for (int u = 0; u < w; ++u) m8[u] = fmaxf(m8[u], m8[u + w]);
+        float mx = m8[0];
         const int xp = gg & 1;
         xch[(xp * 128 + row) * 2 + half] = mx;
         __syncwarp();
-        if (lane == 0) mbar_arrive(&qbar[xp]);
-        ok = __all_sync(0xffffffffu, mbar_wait(&qbar[xp], (gg >> 1) & 1u, a.status));
+        if (lane == 0) st_release_cta(my_flag, gg + 1);
+        ok = __all_sync(0xffffffffu, flag_wait(partner_flag, gg + 1, a.status));
         if (!ok) break;
         mx = fmaxf(mx, xch[(xp * 128 + row) * 2 + (half ^ 1)]) * a.scale_log2;
         // raise the reference only when the max outgrows it by 2^8
         const bool raise = mx > m_ref + 8.f;
         const float m_new = raise ? mx : m_ref;
         const float corr = raise ? ex2_approx(m_ref - m_new) : 1.f;   // 0 on the first tile
-        // p = 2^(s - m) packed to 16 bits, this half's row sum
-        float psum = 0.f;
+        // p = 2^(s - m) packed to 16 bits, this half's row sum (four partial sums)
+        float ps4[4] = {0.f, 0.f, 0.f, 0.f};
         uint32_t pk[32];
 #pragma unroll
         for (int i = 0; i < 32; ++i) {
           const float p0 = ex2_approx(fmaf(sv[2 * i], a.scale_log2, -m_new));
           const float p1 = ex2_approx(fmaf(sv[2 * i + 1], a.scale_log2, -m_new));
-          psum += p0 + p1;
+          ps4[i & 3] += p0 + p1;
           pk[i] = pack2<T16>(p0, p1);
         }
+        const float psum = (ps4[0] + ps4[1]) + (ps4[2] + ps4[3]);
         l_sum = l_sum * corr + psum;
         m_ref = m_new;
         // a raised reference rescales this half of the O row, after P V of the
