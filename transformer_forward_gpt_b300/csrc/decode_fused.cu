@@ -436,6 +436,19 @@ __device__ void producer(const Params& p, Shared& sh, const CUtensorMap* tk, con
   }
 }
 
+// Asynchronous global -> shared copies of 4 or 8 bytes (cp.async, cached in L1 as
+// well: the copies of one staging pass are all in flight at once and hold no
+// registers). cp_async_wait_all makes this thread's copies visible to itself.
+__device__ __forceinline__ void cp_async4(void* dst, const void* src) {
+  asm volatile("cp.async.ca.shared.global [%0], [%1], 4;" ::"r"(smem_u32(dst)), "l"(src) : "memory");
+}
+__device__ __forceinline__ void cp_async8(void* dst, const void* src) {
+  asm volatile("cp.async.ca.shared.global [%0], [%1], 8;" ::"r"(smem_u32(dst)), "l"(src) : "memory");
+}
+__device__ __forceinline__ void cp_async_wait_all() {
+  asm volatile("cp.async.commit_group;\ncp.async.wait_all;\n" ::: "memory");
+}
+
 // =============================================================== consumers
 // Stages activation k16 steps [ks0, ks1) of the current phase into shared
 // memory as mma B fragments: entry ((ks - ks0) * NT + nt) * 32 + lane holds the
@@ -468,6 +481,63 @@ __device__ void stage_act(const Params& p, const Shared& sh, const Gemv& g, int 
   // batch of loads is in flight
   const float ss_tok = (g.act_kind == ACT_H32 && tok_ok) ? __ldcg(g.ss_in + tok) : 0.f;
   float ssum = 0.f;
+  // Asynchronous path, whenever the fp32 sources' landing zone (16 bytes per entry,
+  // after the 8-byte fragments) fits in the activation area: every copy of the
+  // pass is issued before the first is waited for (one L2 round trip, no
+  // registers held). 16-bit sources are copied straight into their fragments.
+  const bool f32src = g.act_kind == ACT_X32 || g.act_kind == ACT_H32;
+  if ((int64_t)n * (f32src ? 24 : 8) <= p.act_bytes) {
+    float4* land = reinterpret_cast<float4*>(sh.act + (size_t)n * 8);
+    for (int i = tid; i < n; i += 256) {
+      const int ks = ks_of(i);
+      if (g.act_kind == ACT_FRAG) {
+        cp_async8(dst + i, reinterpret_cast<const uint2*>(g.act) + ((int64_t)ks * NT + ((i >> 5) % NT)) * 32 + (i & 31));
+        continue;
+      }
+      if (!tok_ok) continue;
+      const int kc = ks * 16 + 2 * (lane & 3);
+      if (g.act_kind == ACT_A16) {
+        const T16* src = static_cast<const T16*>(g.act) + (int64_t)tok * g.act_ld + kc;
+        uint32_t* d = reinterpret_cast<uint32_t*>(dst + i);
+        cp_async4(d, src);
+        cp_async4(d + 1, src + 8);
+      } else {
+        const float* src = static_cast<const float*>(g.act) + (int64_t)tok * g.act_ld + kc;
+        float* d = reinterpret_cast<float*>(land + i);
+        cp_async8(d, src);
+        cp_async8(d + 2, src + 8);
+      }
+    }
+    cp_async_wait_all();
+    if (g.act_kind == ACT_FRAG) return;
+    if (g.act_kind == ACT_A16) {
+      if (!tok_ok)
+        for (int i = tid; i < n; i += 256) dst[i] = make_uint2(0u, 0u);
+      return;
+    }
+    const float rscale = rsqrtf(ss_tok / (float)p.d + p.eps);
+    for (int i = tid; i < n; i += 256) {
+      float4 x = tok_ok ? land[i] : make_float4(0.f, 0.f, 0.f, 0.f);
+      if (want_ss && (i >> 5) / NT < lenA) {   // columns of the first range only
+        const int kc = ks_of(i) * 16 + 2 * (lane & 3);
+        if (kc >= ss_c0 && kc < ss_c1) ssum += x.x * x.x + x.y * x.y + x.z * x.z + x.w * x.w;
+      }
+      if (g.act_kind == ACT_H32) {
+        x.x = fmaxf(x.x * rscale, 0.f);
+        x.y = fmaxf(x.y * rscale, 0.f);
+        x.z = fmaxf(x.z * rscale, 0.f);
+        x.w = fmaxf(x.w * rscale, 0.f);
+        x = make_float4(x.x * x.x, x.y * x.y, x.z * x.z, x.w * x.w);
+      }
+      dst[i] = make_uint2(pack2<T16>(x.x, x.y), pack2<T16>(x.z, x.w));
+    }
+    if (want_ss) {
+      ssum += __shfl_xor_sync(0xffffffffu, ssum, 1);
+      ssum += __shfl_xor_sync(0xffffffffu, ssum, 2);
+      if ((lane & 3) == 0 && tok_ok && ssum != 0.f) atomicAdd(g.ss_out + tok, ssum);
+    }
+    return;
+  }
   for (int i0 = tid; i0 < n; i0 += 256 * kBatch) {
     if (g.act_kind == ACT_FRAG) {
       const uint2* src = reinterpret_cast<const uint2*>(g.act);
