@@ -250,8 +250,9 @@ __device__ bool grid_barrier(const Params& p, const Shared& sh, int k) {
     bool ok = true;
     const bool tr = p.trace && blockIdx.x == 0;
     if (tr) p.trace[2 * k - 1] = global_timer_ns();
-    __threadfence();
-    atomicAdd(p.bar_counter, 1ull);
+    // release at GPU scope: this CTA's writes (ordered before this thread by the
+    // CTA barrier above) are visible to any CTA that acquires the count
+    asm volatile("red.release.gpu.global.add.u64 [%0], 1;" ::"l"(p.bar_counter) : "memory");
     const unsigned long long target = p.bar_base + (unsigned long long)k * gridDim.x;
     uint64_t t0 = 0;
     int it = 0;
@@ -1035,13 +1036,14 @@ __device__ bool consume_attn(const Params& p, Shared& sh, int l, int k) {
         v = fmaf(mall[w * kWs + h], mall[w * kWs + 32 + h * kMergeStride + i], v);
       rec[h * (kHd + 2) + 2 + i] = v;
     }
-    __threadfence();
     bar_consumers();
     trace_mark(p, k, 2);
     if (tid == 0) {
-      const unsigned int n = atomicAdd(p.attn_count + bg, 1u);
+      // acq_rel at GPU scope: releases this CTA's records (ordered before this
+      // thread by the CTA barrier); the last arriver acquires everyone's
+      unsigned int n;
+      asm volatile("atom.acq_rel.gpu.global.add.u32 %0, [%1], 1;" : "=r"(n) : "l"(p.attn_count + bg) : "memory");
       sh.flag[1] = (n == (unsigned)(c_last - c_first)) ? 1 : 0;
-      __threadfence();
     }
     bar_consumers();
     if (sh.flag[1]) {
