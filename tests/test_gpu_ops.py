@@ -59,10 +59,11 @@ def test_gemm_f32_simt(cuda_device):
 
 
 @pytest.mark.parametrize("dt", [nc.NC_F32, nc.NC_BF16, nc.NC_F16])
-def test_rmsnorm(cuda_device, dt):
+@pytest.mark.parametrize("M,d", [(77, 1280), (5, 4), (33, 772), (9, 2048), (7, 2052)])
+def test_rmsnorm(cuda_device, dt, M, d):
+    """Row widths from 4 to 2052, including ones that are not a multiple of 128."""
     import torch
     rng = np.random.default_rng(2)
-    M, d = 77, 1280
     x = torch.from_numpy(rng.standard_normal((M, d)).astype(np.float32) * 3).cuda()
     y = torch.empty(M, d, device="cuda", dtype=_torch_dt(dt))
     nc.nc_op_rmsnorm(x, y, dt, M, d, 1e-5)
