@@ -8,7 +8,7 @@ Shapes follow the nanochat-style GPT described on the pages (d_model = 64 x
 depth, head_dim 128, 4x ReLU^2 MLP, vocabulary 65,536) and the microgpt summary
 (vocabulary 27, width 16, one layer, four heads, block size 16).
 
-Recipe (also stated in the design doc):
+Recipe:
   * numpy ``default_rng(seed)`` (PCG64); every matrix W[rows, cols] is drawn as
     float32 standard normals times 1/sqrt(cols) (std = 1/sqrt(fan_in)).
   * bf16 workloads round each draw to bfloat16 (round to nearest even); the
