@@ -32,16 +32,11 @@
 #include <math.h>
 
 #include <algorithm>
-#include <stdlib.h>
 
 #include "common.cuh"
 #include "tc.h"
 
 namespace nc {
-
-nc_status attn2_launch(const CUtensorMap& mq, const CUtensorMap& mk, const CUtensorMap& mv,
-                       void* o, int B, int H, int Hkv, int T, bool half, uint32_t* status,
-                       cudaStream_t s);
 
 namespace {
 
@@ -551,16 +546,6 @@ bool make_rows_map(CUtensorMap* map, const void* base, bool half, int rank, uint
 // Status word of calls made without a model (bounded-wait timeouts).
 __device__ uint32_t g_attn_status;
 
-// The two-query-tile kernel (attn_tc2.cu) when NC_ATTN_V2=1 (measurement).
-bool use_attn_v2() {
-  static int v = -1;
-  if (v < 0) {
-    const char* e = getenv("NC_ATTN_V2");
-    v = (e && e[0] == '1') ? 1 : 0;
-  }
-  return v == 1;
-}
-
 }  // namespace
 
 // q [B, H, T, 128]; K/V of layer `layer` at k + layer * layer_stride elements,
@@ -578,12 +563,6 @@ nc_status tc_attention_prefill_tc(const void* q, const void* k, const void* v, v
       !make_rows_map(&mv, v, half, 4, T, (uint64_t)B * Hkv, kv_rows_bytes, n_layers,
                      (uint64_t)layer_stride * 2))
     return NC_ERR_CUDA;
-  if (use_attn_v2()) {
-    if (!status && cudaGetSymbolAddress(reinterpret_cast<void**>(&status), g_attn_status) != cudaSuccess)
-      return NC_ERR_CUDA;
-    // the two-tile kernel reads K/V of one layer (layer coordinate 0)
-    if (n_layers == 1) return attn2_launch(mq, mk, mv, o, B, H, Hkv, T, half, status, s);
-  }
   AttnArgs a;
   a.B = B;
   a.H = H;
