@@ -39,12 +39,26 @@ DECODE_STEPS = 128
 
 # ------------------------------------------------------------------- helpers
 def load_peaks():
+    """Measured peaks (hbm_gbs, bf16_tflops, bf16_tflops_sustained) if the file is
+    present and readable; a key it lacks, or a value that is not a positive number,
+    takes the fallback figure and the source says so."""
     path = os.path.join(ROOT, "MEASURED_PEAKS.json")
-    if os.path.exists(path):
+    if not os.path.exists(path):
+        return dict(PEAKS_FALLBACK), "fallback"
+    try:
         with open(path) as f:
             p = json.load(f)
-        return p, "measured"
-    return PEAKS_FALLBACK, "fallback"
+    except (OSError, ValueError):
+        return dict(PEAKS_FALLBACK), "fallback"
+    out, missing = {}, []
+    for k, v in PEAKS_FALLBACK.items():
+        x = p.get(k) if isinstance(p, dict) else None
+        if isinstance(x, (int, float)) and x > 0:
+            out[k] = float(x)
+        else:
+            out[k] = v
+            missing.append(k)
+    return out, ("measured" if not missing else "measured (fallback for " + ", ".join(missing) + ")")
 
 
 def dist_env():
