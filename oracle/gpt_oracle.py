@@ -244,3 +244,26 @@ def decode_step(cfg, wte, layers, lm_head, tokens, cache):
 def greedy_next(logits):
     """Index of the largest logit in each row; ties go to the lowest index."""
     return np.argmax(np.asarray(logits), axis=-1)
+
+
+def sample_temperature(logits, temperature, u):
+    """One draw per row from the softmax of logits / temperature, by inverse CDF.
+
+    Follows the Microgpt summary, section 推理（生成）: item 1 draws the next token
+    from the predicted distribution, item 2 divides by a temperature (lower values
+    sharpen the distribution, higher ones flatten it). The random number is an
+    input: u[b] in [0, 1) selects the smallest index k whose cumulative
+    probability exceeds u[b] (the last index if rounding leaves the total below
+    u[b]). A temperature <= 0 is the zero-temperature limit: the greedy index.
+    """
+    logits = np.asarray(logits, dtype=np.float64)
+    u = np.asarray(u, dtype=np.float64).reshape(-1)
+    if temperature <= 0:
+        return greedy_next(logits)
+    p = softmax_rows(logits / float(temperature))
+    cdf = np.cumsum(p, axis=-1)
+    out = np.empty(logits.shape[0], dtype=np.int64)
+    for b in range(logits.shape[0]):
+        k = int(np.searchsorted(cdf[b], u[b], side="right"))
+        out[b] = min(k, logits.shape[1] - 1)
+    return out

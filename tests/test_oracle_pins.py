@@ -267,3 +267,53 @@ def test_bf16_rounding_of_inputs():
     y = synth.bf16_bits_to_f32(synth.round_to_bf16_bits(x))
     assert y[0] == 1.0 and y[1] == 1.0 and y[2] == 1.0 + 2 ** -6 and y[3] == -2.5
     assert abs(y[4] - 1e-3) <= 1e-3 * 2 ** -8
+
+
+# ---------------------------------------------------------- temperature sampling
+# Microgpt summary, section 推理（生成）: draw from the predicted distribution;
+# the temperature sharpens (low) or flattens (high) it.
+
+def test_sampling_two_classes_closed_form():
+    """Two logits a, b: P(first) = 1 / (1 + e^((b - a) / T)), so u just below that
+    probability picks index 0 and u just above picks index 1."""
+    for a, b, T in [(0.3, -1.2, 0.7), (2.0, 2.5, 1.0), (-1.0, 3.0, 2.5)]:
+        p0 = 1.0 / (1.0 + math.exp((b - a) / T))
+        lo, hi = p0 * (1 - 1e-9), p0 * (1 + 1e-9)
+        ks = O.sample_temperature(np.array([[a, b], [a, b]]), T, np.array([lo, hi]))
+        assert ks.tolist() == [0, 1]
+
+
+def test_sampling_uniform_logits_picks_floor_u_times_v():
+    """Equal logits at any temperature: every index has probability 1/V, so u
+    selects floor(u V) (u placed mid-interval, away from the boundaries)."""
+    V = 97
+    j = np.arange(V)
+    u = (j + 0.5) / V
+    ks = O.sample_temperature(np.full((V, V), 1.25), 0.8, u)
+    assert (ks == j).all()
+
+
+def test_sampling_inverse_cdf_frequencies():
+    """A uniform grid of N values of u lands in class k about p_k N times (within
+    one), the defining property of inverse-CDF sampling."""
+    rng = np.random.default_rng(11)
+    logits = rng.standard_normal(12) * 2.0
+    T = 1.3
+    z = np.exp((logits - logits.max()) / T)
+    p = z / z.sum()
+    N = 20000
+    u = (np.arange(N) + 0.5) / N
+    ks = O.sample_temperature(np.tile(logits, (N, 1)), T, u)
+    counts = np.bincount(ks, minlength=12)
+    assert np.all(np.abs(counts - p * N) <= 1.0)
+
+
+def test_sampling_low_temperature_is_greedy_and_zero_is_greedy():
+    """As T -> 0 the distribution concentrates on the largest logit; T <= 0 is
+    the greedy limit itself (lowest index on ties)."""
+    rng = np.random.default_rng(12)
+    logits = rng.standard_normal((6, 50))
+    u = rng.random(6)
+    assert (O.sample_temperature(logits, 1e-4, u) == np.argmax(logits, axis=1)).all()
+    tied = np.array([[1.0, 3.0, 3.0, 0.0]])
+    assert O.sample_temperature(tied, 0.0, np.array([0.9])).tolist() == [1]
