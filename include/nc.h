@@ -262,6 +262,19 @@ NC_API nc_status nc_op_attention_decode_noalloc(const void* q, const void* k, co
  * [rows, n], out dev int32 [rows]. */
 NC_API nc_status nc_op_argmax(const float* x, int32_t rows, int32_t n, int32_t* out, void* stream);
 
+/* Temperature sampling (Microgpt summary, section 推理（生成）, items 1 and 2: draw
+ * the next token from the predicted distribution; the temperature divides the
+ * logits, a lower one sharpening the distribution, a higher one flattening it).
+ * out[r] = the smallest k with sum_{v <= k} p[r, v] > u[r], where
+ * p[r, :] = softmax(logits[r, :] / temperature) (inverse CDF; fp32 arithmetic,
+ * row max subtracted first; the last index if rounding leaves every partial sum at
+ * or below u[r] Z). temperature <= 0 gives the greedy index (lowest on ties).
+ * logits dev fp32 [rows, n]; u dev fp32 [rows]: the caller's random numbers, one
+ * per row, clamped into [0, 1); out dev int32 [rows]. Nothing is allocated. Errors:
+ * NC_ERR_INVALID_ARG for a NULL pointer, rows < 0 or n <= 0. */
+NC_API nc_status nc_op_sample(const float* logits, int32_t rows, int32_t n, float temperature,
+                              const float* u, int32_t* out, void* stream);
+
 /* ------------------------------------------------------------------------
  * Measurement: per-kernel-class device time and a launch counter. Host-side
  * bookkeeping only; results are unchanged.

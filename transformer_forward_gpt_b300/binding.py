@@ -25,7 +25,7 @@ EXPORTS = (
     "nc_op_attention_decode_scratch_bytes", "nc_op_attention_decode", "nc_op_argmax",
     "nc_kv_cache_set_length", "nc_profile_begin", "nc_profile_end", "nc_launch_count",
     "nc_op_attention_decode_noalloc", "nc_model_set_decode_path", "nc_decode_trace",
-    "nc_decode_trace_entries",
+    "nc_decode_trace_entries", "nc_op_sample",
 )
 
 KERNEL_KINDS = ("embed", "norm", "qkv", "attn_prefill", "attn_decode", "oproj", "fc", "proj",
@@ -89,6 +89,7 @@ def load(path: str = LIB_PATH):
         "nc_op_attention_decode": (C.c_int, [vp, vp, vp, vp, i32, i32, i32, i32, i32, i32,
                                              C.c_int, vp, sz, vp]),
         "nc_op_argmax": (C.c_int, [vp, i32, i32, vp, vp]),
+        "nc_op_sample": (C.c_int, [vp, i32, i32, C.c_float, vp, vp, vp]),
         "nc_kv_cache_set_length": (C.c_int, [vp, i32]),
         "nc_profile_begin": (C.c_int, [vp]),
         "nc_profile_end": (C.c_int, [vp, vp, C.POINTER(NcKernelTime)]),
@@ -265,6 +266,11 @@ def nc_op_attention_decode(q, k, v, o, B, H, Hkv, length, t_max, hd, dtype, scra
 
 def nc_op_argmax(x, rows, n, out, stream=None):
     _check(load().nc_op_argmax(_ptr(x), rows, n, _ptr(out), _stream(stream)), "nc_op_argmax")
+
+
+def nc_op_sample(logits, rows, n, temperature, u, out, stream=None):
+    _check(load().nc_op_sample(_ptr(logits), rows, n, float(temperature), _ptr(u), _ptr(out),
+                               _stream(stream)), "nc_op_sample")
 
 
 def nc_op_attention_decode_noalloc(q, k, v, o, B, H, Hkv, length, t_max, hd, dtype, stream=None):

@@ -1014,4 +1014,13 @@ nc_status nc_op_argmax(const float* x, int32_t rows, int32_t n, int32_t* out, vo
   return check_launch();
 }
 
+nc_status nc_op_sample(const float* logits, int32_t rows, int32_t n, float temperature,
+                       const float* u, int32_t* out, void* stream) {
+  NC_CHECK(logits && u && out, NC_ERR_INVALID_ARG, "NULL pointer");
+  NC_CHECK(rows >= 0 && n > 0, NC_ERR_INVALID_ARG, "bad sizes");
+  if (rows == 0) return NC_OK;
+  nc::launch_sample(logits, rows, n, temperature, u, out, static_cast<cudaStream_t>(stream));
+  return check_launch();
+}
+
 }  // extern "C"

@@ -78,6 +78,9 @@ void launch_attention_combine(const float* scratch, void* o, int BH, int hd, int
 void launch_convert16(const void* src, nc_dtype from, void* dst, nc_dtype to, int64_t n,
                       cudaStream_t s);
 void launch_argmax(const float* x, int rows, int n, int32_t* out, cudaStream_t s);
+// ---- temperature sampling (sample.cu)
+void launch_sample(const float* logits, int B, int V, float temperature, const float* u,
+                   int32_t* out, cudaStream_t s);
 void launch_gather_rows(const float* x, float* y, int B, int T, int d, cudaStream_t s);
 
 }  // namespace nc
