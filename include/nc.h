@@ -145,6 +145,19 @@ NC_API void nc_kv_cache_free(nc_kv_cache* c);
 NC_API nc_status nc_prefill(nc_model* m, const int32_t* tokens, int32_t B, int32_t T,
                             float* logits, nc_kv_cache* c, void* stream);
 
+/* Continues a prefill: runs tokens (dev int32 [B, T]) at positions L..L+T-1,
+ * where L is the cache's current length (the same for all its sequences), with
+ * attention over positions 0..L+T-1 of the cache. Writes their K/V, sets the
+ * length to L + T, and writes the T positions' logits (dev fp32 [B, T, vocab]).
+ * L = 0 is nc_prefill; calling it in pieces gives the same K/V and logits as one
+ * call over the whole sequence (up to the summation order of fp32 sums). T = 1 is
+ * one decode step through the per-kernel path. Requires the bounds of nc_prefill
+ * and L + T <= cache t_max; NC_ERR_UNSUPPORTED for T > 1 with L > 0 on an fp32
+ * model. (CSDN nanochat article, Engine paragraph: prefill and decode over a
+ * KV cache; the pages do not fix how a prompt is split.) */
+NC_API nc_status nc_prefill_continue(nc_model* m, const int32_t* tokens, int32_t B, int32_t T,
+                                     float* logits, nc_kv_cache* c, void* stream);
+
 /* As nc_prefill, but the LM head runs only on position T-1 of each sequence:
  * logits_last (dev fp32 [B, vocab], may be NULL) and argmax_out (dev int32 [B],
  * may be NULL; the greedy next token, lowest index on ties). */

@@ -317,3 +317,23 @@ def test_sampling_low_temperature_is_greedy_and_zero_is_greedy():
     assert (O.sample_temperature(logits, 1e-4, u) == np.argmax(logits, axis=1)).all()
     tied = np.array([[1.0, 3.0, 3.0, 0.0]])
     assert O.sample_temperature(tied, 0.0, np.array([0.9])).tolist() == [1]
+
+
+def test_prefill_in_chunks_equals_one_prefill():
+    """Running a prompt in pieces through the KV cache gives the one-shot prefill's
+    logits and cache (KV cache paragraph: earlier positions are read back, not
+    recomputed)."""
+    shape = _small(n_kv_head=1)
+    cfg = _cfg(shape)
+    wte, layers, lm = _weights(shape)
+    toks = synth.make_tokens(shape, 2, 9)
+    full, fcache = O.prefill(cfg, wte, layers, lm, toks)
+    cache = O.KVCache(cfg, 2, 9)
+    parts = []
+    for a, b in [(0, 3), (3, 7), (7, 9)]:
+        parts.append(O.forward(cfg, wte, layers, lm, toks[:, a:b], cache, a))
+    np.testing.assert_allclose(np.concatenate(parts, axis=1), full, rtol=0, atol=1e-11)
+    for l in range(cfg["n_layer"]):
+        np.testing.assert_allclose(cache.k[l], fcache.k[l], rtol=0, atol=1e-12)
+        np.testing.assert_allclose(cache.v[l], fcache.v[l], rtol=0, atol=1e-12)
+    assert cache.length == 9

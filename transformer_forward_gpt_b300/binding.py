@@ -25,7 +25,7 @@ EXPORTS = (
     "nc_op_attention_decode_scratch_bytes", "nc_op_attention_decode", "nc_op_argmax",
     "nc_kv_cache_set_length", "nc_profile_begin", "nc_profile_end", "nc_launch_count",
     "nc_op_attention_decode_noalloc", "nc_model_set_decode_path", "nc_decode_trace",
-    "nc_decode_trace_entries", "nc_op_sample",
+    "nc_decode_trace_entries", "nc_op_sample", "nc_prefill_continue",
 )
 
 KERNEL_KINDS = ("embed", "norm", "qkv", "attn_prefill", "attn_decode", "oproj", "fc", "proj",
@@ -77,6 +77,7 @@ def load(path: str = LIB_PATH):
                                        C.POINTER(i32), C.POINTER(i32)]),
         "nc_kv_cache_free": (None, [vp]),
         "nc_prefill": (C.c_int, [vp, vp, i32, i32, vp, vp, vp]),
+        "nc_prefill_continue": (C.c_int, [vp, vp, i32, i32, vp, vp, vp]),
         "nc_prefill_last": (C.c_int, [vp, vp, i32, i32, vp, vp, vp, vp]),
         "nc_decode_step": (C.c_int, [vp, vp, i32, i32, vp, vp, vp, vp]),
         "nc_generate_host": (C.c_int, [vp, vp, i32, i32, i32, vp, vp, vp]),
@@ -198,6 +199,11 @@ def nc_kv_cache_free(cache):
 def nc_prefill(model, tokens, B, T, logits, cache, stream=None):
     _check(load().nc_prefill(model, _ptr(tokens), B, T, _ptr(logits), cache, _stream(stream)),
            "nc_prefill")
+
+
+def nc_prefill_continue(model, tokens, B, T, logits, cache, stream=None):
+    _check(load().nc_prefill_continue(model, _ptr(tokens), B, T, _ptr(logits), cache,
+                                      _stream(stream)), "nc_prefill_continue")
 
 
 def nc_prefill_last(model, tokens, B, T, logits_last, argmax_out, cache, stream=None):

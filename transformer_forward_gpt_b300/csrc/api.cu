@@ -519,9 +519,11 @@ nc_status run_blocks(nc_model* m, nc_kv_cache* c, int B, int rows_per_seq, int p
     } else if (tc) {
       const int64_t one_layer = (int64_t)c->batch * Hkv * c->t_max * hd;
       nc_status st = nc::tc_attention_prefill_tc(m->q, dst.k_cache, dst.v_cache, m->att, B, H,
-                                                 Hkv, rows_per_seq, c->t_max, 1, one_layer, 0, dt,
-                                                 m->status, s);
-      if (st != NC_OK)   // descriptors could not be built: the mma.sync kernel needs none
+                                                 Hkv, rows_per_seq, pos0, c->t_max, 1, one_layer,
+                                                 0, dt, m->status, s);
+      // descriptors could not be built: the mma.sync kernel needs none (it serves
+      // prefill from position 0 only)
+      if (st != NC_OK && pos0 == 0)
         st = nc::tc_attention_prefill(m->q, dst.k_cache, dst.v_cache, m->att, B, H, Hkv,
                                       rows_per_seq, c->t_max, dt, s);
       if (st != NC_OK) return st;
@@ -590,17 +592,19 @@ nc_status check_prefill_args(nc_model* m, const int32_t* tokens, int32_t B, int3
   return NC_OK;
 }
 
+// Runs T positions of B sequences starting at absolute position pos0 (the cache
+// already holds positions 0..pos0-1) and sets the cache length to pos0 + T.
 nc_status prefill_common(nc_model* m, const int32_t* tokens, int32_t B, int32_t T,
-                         nc_kv_cache* c, cudaStream_t s) {
+                         nc_kv_cache* c, cudaStream_t s, int32_t pos0 = 0) {
   const int64_t M = (int64_t)B * T;
   {
     ProfScope ps(m, NC_K_EMBED, s);
     nc::launch_embed_norm(tokens, m->wte, m->cfg.dtype, m->x, m->xn, m->adt, M, m->cfg.d_model,
                           m->cfg.vocab, m->cfg.rms_eps, m->status, s);
   }
-  nc_status st = run_blocks(m, c, B, T, 0, s);
+  nc_status st = run_blocks(m, c, B, T, pos0, s);
   if (st != NC_OK) return st;
-  c->len = T;
+  c->len = pos0 + T;
   return NC_OK;
 }
 
@@ -770,6 +774,22 @@ nc_status nc_prefill(nc_model* m, const int32_t* tokens, int32_t B, int32_t T, f
   NC_CHECK(logits && aligned16(logits), NC_ERR_INVALID_ARG, "logits NULL or misaligned");
   cudaStream_t s = static_cast<cudaStream_t>(stream);
   st = prefill_common(m, tokens, B, T, c, s);
+  if (st != NC_OK) return st;
+  return run_lm_head(m, m->xn, (int64_t)B * T, logits, s);
+}
+
+nc_status nc_prefill_continue(nc_model* m, const int32_t* tokens, int32_t B, int32_t T,
+                              float* logits, nc_kv_cache* c, void* stream) {
+  nc_status st = check_prefill_args(m, tokens, B, T, c);
+  if (st != NC_OK) return st;
+  NC_CHECK(logits && aligned16(logits), NC_ERR_INVALID_ARG, "logits NULL or misaligned");
+  const int32_t pos0 = c->len;
+  NC_CHECK((int64_t)pos0 + T <= c->t_max && (int64_t)pos0 + T <= m->cfg.max_seq,
+           NC_ERR_INVALID_ARG, "cache length %d + T=%d exceeds t_max %d", pos0, T, c->t_max);
+  NC_CHECK(T == 1 || pos0 == 0 || m->adt != NC_F32, NC_ERR_UNSUPPORTED,
+           "continuing a prefill needs a 16-bit model");
+  cudaStream_t s = static_cast<cudaStream_t>(stream);
+  st = prefill_common(m, tokens, B, T, c, s, pos0);
   if (st != NC_OK) return st;
   return run_lm_head(m, m->xn, (int64_t)B * T, logits, s);
 }
@@ -974,8 +994,8 @@ nc_status nc_op_attention_prefill(const void* q, const void* k, const void* v, v
   if (dtype == NC_BF16 || dtype == NC_F16) {
     NC_CHECK(hd == 128, NC_ERR_UNSUPPORTED, "16-bit attention needs head_dim 128");
     const int64_t one_layer = (int64_t)B * Hkv * t_max * hd;
-    nc_status st = nc::tc_attention_prefill_tc(q, k, v, o, B, H, Hkv, T, t_max, 1, one_layer, 0,
-                                               dtype, nullptr, s);
+    nc_status st = nc::tc_attention_prefill_tc(q, k, v, o, B, H, Hkv, T, 0, t_max, 1, one_layer,
+                                               0, dtype, nullptr, s);
     if (st == NC_OK) return NC_OK;
     return nc::tc_attention_prefill(q, k, v, o, B, H, Hkv, T, t_max, dtype, s);
   }

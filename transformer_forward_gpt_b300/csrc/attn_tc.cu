@@ -139,10 +139,16 @@ __device__ __forceinline__ bool flag_wait(const uint32_t* flag, uint32_t target,
 
 struct AttnArgs {
   int B, H, Hkv, T, n_qt, n_items;
+  int pos0;           // absolute position of query row 0 (keys 0 .. pos0 + T - 1)
   float scale_log2;
   void* o;            // [B, T, H*128]
   uint32_t* status;
 };
+
+// Key tiles query tile qt reads: those holding keys up to its last query's position.
+__device__ __forceinline__ int key_tiles(const AttnArgs& a, int qt) {
+  return (a.pos0 + min(a.T, (qt + 1) * kBq) - 1) / kBk + 1;
+}
 
 // k-th item of CTA c (snake order over items sorted heaviest first), or -1
 __device__ __forceinline__ int item_of(int k, int c, int G, int n_items) {
@@ -257,7 +263,7 @@ __global__ void __launch_bounds__(kThreads, 1)
         if (item < 0 || *abort_flag) break;
         const int qt = a.n_qt - 1 - item / per_qt, bh = item % per_qt;
         const int bg = (bh / a.H) * a.Hkv + (bh % a.H) / (a.H / a.Hkv);
-        const int n = qt + 1;
+        const int n = key_tiles(a, qt);
         // Q of the previous item is no longer read once its last S is done
         if (k > 0 && !mbar_wait_sleep(q_empty, (k - 1) & 1, a.status)) { ok = false; break; }
         mbar_arrive_expect_tx(q_full, kTile);
@@ -291,7 +297,7 @@ __global__ void __launch_bounds__(kThreads, 1)
       for (int k = 0; ok; ++k) {
         const int item = item_of(k, c, G, a.n_items);
         if (item < 0 || *abort_flag) break;
-        const int n = a.n_qt - item / per_qt;
+        const int n = key_tiles(a, a.n_qt - 1 - item / per_qt);
         if (!mbar_wait_sleep(q_full, k & 1, a.status)) { ok = false; break; }
         for (int j = 0; j < n; ++j) {
           const uint32_t gg = g + j;
@@ -332,7 +338,7 @@ __global__ void __launch_bounds__(kThreads, 1)
       for (int k = 0; ok; ++k) {
         const int item = item_of(k, c, G, a.n_items);
         if (item < 0 || *abort_flag) break;
-        const int n = a.n_qt - item / per_qt;
+        const int n = key_tiles(a, a.n_qt - 1 - item / per_qt);
         for (int j = 0; j < n; ++j) {
           const uint32_t gg = g + j;
           // P of the tile in TMEM; the first product of an item overwrites O, so
@@ -384,8 +390,11 @@ __global__ void __launch_bounds__(kThreads, 1)
       if (item < 0 || *abort_flag) break;
       const int qt = a.n_qt - 1 - item / per_qt, bh = item % per_qt;
       const int b = bh / a.H, h = bh % a.H;
-      const int n = qt + 1;
-      const int qpos = qt * kBq + row;
+      const int n = key_tiles(a, qt);
+      const int qrow = qt * kBq + row;     // row of q and of the output
+      const int qpos = a.pos0 + qrow;      // its absolute position
+      // tiles from this one on hold keys past the tile's first query: masked
+      const int first_masked = (a.pos0 + qt * kBq) / kBk;
       float m_ref = -INFINITY, l_sum = 0.f;
       for (int j = 0; j < n; ++j) {
         const uint32_t gg = g + j;
@@ -396,7 +405,7 @@ __global__ void __launch_bounds__(kThreads, 1)
         // this half of the score row in one 64-column TMEM load; causal mask
         float sv[64];
         tmem_ld64_sync(sb, sv);
-        if (j == qt) {
+        if (j >= first_masked) {
           const int kmax = qpos - j * kBk - 64 * half;   // keys i > kmax are masked
 #pragma unroll
           for (int i = 0; i < 64; ++i)
@@ -476,10 +485,10 @@ __global__ void __launch_bounds__(kThreads, 1)
       if (!ok) break;
       l_sum += xl[row * 2 + (half ^ 1)];
       tc_fence_after();
-      // O / l for output columns [64 half, 64 half + 64) -> out[b, qpos, h*128 ..]
+      // O / l for output columns [64 half, 64 half + 64) -> out[b, qrow, h*128 ..]
       const float inv = 1.f / l_sum;
-      const bool valid = qpos < a.T;
-      T16* orow = out + ((int64_t)b * a.T + (valid ? qpos : 0)) * (a.H * kHd) + h * kHd + 64 * half;
+      const bool valid = qrow < a.T;
+      T16* orow = out + ((int64_t)b * a.T + (valid ? qrow : 0)) * (a.H * kHd) + h * kHd + 64 * half;
 #pragma unroll 1
       for (int cc = 0; cc < 2; ++cc) {
         float v[32];
@@ -551,19 +560,22 @@ __device__ uint32_t g_attn_status;
 // q [B, H, T, 128]; K/V of layer `layer` at k + layer * layer_stride elements,
 // each [B_cache, Hkv, t_max, 128] (only sequences 0..B-1 and rows < T used).
 nc_status tc_attention_prefill_tc(const void* q, const void* k, const void* v, void* o, int B,
-                                  int H, int Hkv, int T, int t_max, int n_layers,
+                                  int H, int Hkv, int T, int pos0, int t_max, int n_layers,
                                   int64_t layer_stride, int layer, nc_dtype dt, uint32_t* status,
                                   cudaStream_t s) {
+  if (pos0 < 0 || pos0 + T > t_max) return NC_ERR_INVALID_ARG;
   const bool half = dt == NC_F16;
   CUtensorMap mq, mk, mv;
   const uint64_t kv_rows_bytes = (uint64_t)t_max * 256;
+  const uint64_t n_keys = (uint64_t)pos0 + T;   // cache rows at or past it read as zeros
   if (!make_rows_map(&mq, q, half, 3, T, (uint64_t)B * H, (uint64_t)T * 256, 1, 0) ||
-      !make_rows_map(&mk, k, half, 4, T, (uint64_t)B * Hkv, kv_rows_bytes, n_layers,
+      !make_rows_map(&mk, k, half, 4, n_keys, (uint64_t)B * Hkv, kv_rows_bytes, n_layers,
                      (uint64_t)layer_stride * 2) ||
-      !make_rows_map(&mv, v, half, 4, T, (uint64_t)B * Hkv, kv_rows_bytes, n_layers,
+      !make_rows_map(&mv, v, half, 4, n_keys, (uint64_t)B * Hkv, kv_rows_bytes, n_layers,
                      (uint64_t)layer_stride * 2))
     return NC_ERR_CUDA;
   AttnArgs a;
+  a.pos0 = pos0;
   a.B = B;
   a.H = H;
   a.Hkv = Hkv;

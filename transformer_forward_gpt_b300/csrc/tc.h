@@ -33,12 +33,14 @@ nc_status tc_lm_head(TcModel* t, const void* xn, int64_t M, float* logits, float
 // Causal attention over q [B, H, T, 128], cache k/v [B, Hkv, t_max, 128] -> o [B, T, H*128].
 nc_status tc_attention_prefill(const void* q, const void* k, const void* v, void* o, int B, int H,
                                int Hkv, int T, int t_max, nc_dtype dt, cudaStream_t s);
-// The same attention on tcgen05 (TMEM scores and output, TMA-fed K/V ring).
-// K/V of layer `layer` are k/v + layer * layer_stride elements ([B_cache, Hkv,
-// t_max, 128] each, sequences 0..B-1 and rows < T read). status: device word
-// for bounded-wait timeouts (NULL: a library-wide word).
+// The same attention on tcgen05 (TMEM scores and output, TMA-fed K/V rings), for
+// queries at absolute positions pos0 .. pos0 + T - 1 (q row i is position pos0 + i)
+// over keys 0 .. pos0 + T - 1. K/V of layer `layer` are k/v + layer * layer_stride
+// elements ([B_cache, Hkv, t_max, 128] each, sequences 0..B-1 and rows
+// < pos0 + T read). status: device word for bounded-wait timeouts (NULL: a
+// library-wide word). NC_ERR_INVALID_ARG if pos0 < 0 or pos0 + T > t_max.
 nc_status tc_attention_prefill_tc(const void* q, const void* k, const void* v, void* o, int B,
-                                  int H, int Hkv, int T, int t_max, int n_layers,
+                                  int H, int Hkv, int T, int pos0, int t_max, int n_layers,
                                   int64_t layer_stride, int layer, nc_dtype dt, uint32_t* status,
                                   cudaStream_t s);
 // C[M, N] = A[M, K] B[N, K]^T, fp32 out (single-step entry point).
