@@ -72,3 +72,19 @@ def test_status_strings(lib):
     assert lib.nc_status_string(0) == b"ok"
     assert lib.nc_status_string(binding.NC_ERR_BOUNDS) == b"token id out of range"
     assert binding.nc_version().startswith("nc-b300")
+
+
+def test_sample_and_continue_reject_bad_arguments_on_the_host(lib):
+    """Argument checks of nc_op_sample and nc_prefill_continue happen before any
+    device call (no GPU needed); zero rows is a valid empty call."""
+    fake = 1 << 20   # never dereferenced: the checks return first
+    for args in [(None, 2, 8, 1.0, fake, fake), (fake, 2, 8, 1.0, None, fake),
+                 (fake, 2, 8, 1.0, fake, None), (fake, 2, 0, 1.0, fake, fake),
+                 (fake, -1, 8, 1.0, fake, fake)]:
+        with pytest.raises(binding.NcError) as e:
+            binding.nc_op_sample(*args, stream=0)
+        assert e.value.code == binding.NC_ERR_INVALID_ARG
+    binding.nc_op_sample(fake, 0, 8, 0.7, fake, fake, stream=0)   # no rows: nothing to do
+    with pytest.raises(binding.NcError) as e:
+        binding.nc_prefill_continue(None, fake, 1, 4, fake, None, stream=0)
+    assert e.value.code == binding.NC_ERR_INVALID_ARG
