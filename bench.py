@@ -527,6 +527,35 @@ def run_reference(args):
     print(json.dumps(line), flush=True)
 
 
+def run_op_attention(args):
+    """Profiling aid: the tcgen05 prefill attention alone, through the C ABI, at
+    the d20 prefill shape (4 sequences, 10 query and 10 KV heads, 2048 positions,
+    seeded N(0, 1) fp16 q, k, v). --warmup calls, then --steps calls timed with
+    CUDA events; prints the time per call and the algorithmic rate (4 * head_dim
+    FLOPs per visible (query, key) pair and head)."""
+    import torch
+    from transformer_forward_gpt_b300 import binding as nc
+    B, H, Hkv, T, hd = 4, 10, 10, 2048, 128
+    torch.manual_seed(0)
+    q = torch.randn(B, H, T, hd, device="cuda").half()
+    k = torch.randn(B, Hkv, T, hd, device="cuda").half()
+    v = torch.randn(B, Hkv, T, hd, device="cuda").half()
+    o = torch.empty(B, T, H * hd, device="cuda", dtype=torch.half)
+    for _ in range(args.warmup):
+        nc.nc_op_attention_prefill(q, k, v, o, B, H, Hkv, T, T, hd, nc.NC_F16)
+    torch.cuda.synchronize()
+    e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    e0.record()
+    for _ in range(args.steps):
+        nc.nc_op_attention_prefill(q, k, v, o, B, H, Hkv, T, T, hd, nc.NC_F16)
+    e1.record()
+    torch.cuda.synchronize()
+    ms = e0.elapsed_time(e1) / args.steps
+    flop = 4.0 * hd * H * B * T * (T + 1) / 2
+    print(f"profiling aid: attention B{B} H{H} Hkv{Hkv} T{T}: {ms * 1e3:.1f} us per call, "
+          f"{flop / (ms / 1e3) / 1e12:.0f} TFLOP/s", flush=True)
+
+
 def main():
     ap = argparse.ArgumentParser(description=__doc__.splitlines()[0])
     ap.add_argument("--gpus", type=int, default=1)
@@ -541,12 +570,16 @@ def main():
                     help="profiling aid: smaller prefill batch (no JSON line)")
     ap.add_argument("--decode-steps", type=int, default=None,
                     help="profiling aid: fewer decode steps per step (no JSON line)")
+    ap.add_argument("--op", choices=("attention",), default=None,
+                    help="profiling aid: time one kernel on its own (no JSON line)")
     ap.add_argument("--cpu-budget", type=float, default=30.0)
     args = ap.parse_args()
     if args.warmup < 3 and args.impl == "ours":
         print("warning: fewer than 3 warm-up steps", file=sys.stderr)
     if args.impl == "reference":
         run_reference(args)
+    elif args.op == "attention":
+        run_op_attention(args)
     else:
         run_ours(args)
 

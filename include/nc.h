@@ -113,7 +113,12 @@ NC_API const char* nc_last_error(void);
 /* Number of weight values of a shape: 2*vocab*d + n_layer*(per-layer matrices). */
 NC_API int64_t nc_param_count(const nc_config* cfg);
 
-/* Validates cfg, builds the cos/sin tables (computed in fp64 on the host, stored
+/* The model's parameters are the matrices the Microgpt summary lists in section
+ * 模型参数 (token embedding, the attention and MLP matrices of every layer, and
+ * the final output projection; no biases, no norm gains); the cos/sin tables are
+ * the precomputed rotary embedding of 復刻 ChatGPT 有多難？ (jxzklqfsx.com),
+ * section 為什么可以訓練如此之快, kept in GPU memory.
+ * Validates cfg, builds the cos/sin tables (computed in fp64 on the host, stored
  * fp32 on the device), allocates the workspace for max_batch*max_seq tokens and
  * the device status word, and builds the TMA descriptors of the weights. Uses the
  * current CUDA device. On failure *out is NULL and nothing is leaked. */
@@ -126,13 +131,21 @@ NC_API void nc_model_destroy(nc_model* m);
  * norm, V as projected. */
 NC_API size_t nc_kv_cache_bytes(const nc_config* cfg, int32_t batch, int32_t t_max);
 
-/* Creates a cache for `batch` sequences of up to t_max positions (t_max <= cfg
+/* The KV cache of 復刻 ChatGPT 有多難？ (jxzklqfsx.com), section
+ * 為什么可以訓練如此之快 (the KV-cache paragraph: keys and values of earlier
+ * positions are kept so decode does not recompute them) and of the CSDN nanochat
+ * article (wap.jaobe.com), inference paragraph (the Engine's cache, filled by
+ * prefill and extended by each decode step).
+ * Creates a cache for `batch` sequences of up to t_max positions (t_max <= cfg
  * max_seq). mem == NULL: the library allocates and owns the memory. Otherwise
  * mem is a caller-owned device buffer of nc_kv_cache_bytes() bytes (256-byte
  * aligned) that must outlive the cache. Starts with length 0. */
 NC_API nc_status nc_kv_cache_alloc(const nc_model* m, int32_t batch, int32_t t_max, void* mem,
                                    nc_kv_cache** out);
-/* Device pointers to the K and V arrays and the number of filled positions. */
+/* The same cache (jxzklqfsx.com, KV-cache paragraph) seen from outside: device
+ * pointers to the K and V arrays, the number of filled positions, and the batch
+ * and t_max it was created with. Any output pointer may be NULL. Returns
+ * NC_ERR_INVALID_ARG for a NULL cache. */
 NC_API nc_status nc_kv_cache_view(const nc_kv_cache* c, void** k, void** v, int32_t* len,
                                   int32_t* batch, int32_t* t_max);
 NC_API void nc_kv_cache_free(nc_kv_cache* c);

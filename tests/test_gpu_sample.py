@@ -94,3 +94,20 @@ def test_sample_frequencies_follow_the_distribution(cuda_device):
     p = O.softmax_rows(base.astype(np.float32).astype(np.float64)[None, :] / T)[0]
     counts = np.bincount(got, minlength=40)
     assert np.all(np.abs(counts - p * N) <= 2.0)
+
+
+def test_sample_never_draws_a_zero_probability_tail(cuda_device):
+    """u just below 1 with a tail of -inf logits: u Z can round up to Z in fp32,
+    and the draw must then be the last token of nonzero probability, as the
+    inverse CDF gives, never one of the masked tail."""
+    V, live = 4096, 1000
+    logits = np.zeros((4, V))
+    logits[:, live:] = -np.inf
+    logits[1, :live] = np.linspace(-3.0, 3.0, live)
+    u = [0.99999994, 0.99999994, 0.9999999, 0.5]
+    got = _run(logits, 1.0, u)
+    assert (got < live).all(), got
+    ref = O.sample_temperature(logits.astype(np.float32).astype(np.float64), 1.0,
+                               np.asarray(u, dtype=np.float32).astype(np.float64))
+    assert (ref < live).all()
+    assert got[0] == live - 1 and got[1] == live - 1

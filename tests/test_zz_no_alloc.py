@@ -15,30 +15,41 @@ from transformer_forward_gpt_b300 import binding as nc
 pytestmark = pytest.mark.gpu
 
 
-def _inputs(B, H, Hkv, length, t_max, hd, seed):
+def _inputs(B, H, Hkv, t_max, hd, dtype, seed):
     import torch
     rng = np.random.default_rng(seed)
-    f = lambda *s: torch.from_numpy(rng.standard_normal(s).astype(np.float32)).cuda().half()
+    tt = torch.float16 if dtype == nc.NC_F16 else torch.float32
+    f = lambda *s: torch.from_numpy(rng.standard_normal(s).astype(np.float32)).cuda().to(tt)
     return f(B, H, hd), f(B, Hkv, t_max, hd), f(B, Hkv, t_max, hd)
 
 
-@pytest.mark.parametrize("B,H,Hkv,length", [(32, 10, 1, 1100), (4, 13, 13, 2049)])
-def test_noalloc_matches_scratch_entry_point_twice(cuda_device, B, H, Hkv, length):
+# Each case makes two calls in a row with different lengths. The second call of
+# the MHA case is much shorter (5 splits of the key range, then 2), so a result
+# that read partials left in the shared array by the first call would differ.
+# The fp32 head_dim-64 case runs the CUDA-core kernel instead of the tensor-core one.
+@pytest.mark.parametrize("B,H,Hkv,lengths,hd,dtype", [
+    (32, 10, 1, (1100, 1099), 128, nc.NC_F16),
+    (4, 13, 13, (2049, 100), 128, nc.NC_F16),
+    (3, 8, 2, (700, 65), 64, nc.NC_F32),
+])
+def test_noalloc_matches_scratch_entry_point_twice(cuda_device, B, H, Hkv, lengths, hd, dtype):
     import torch
-    hd, t_max = 128, length + 8
-    for call in range(2):      # two calls in a row: the shared array keeps old contents
-        q, k, v = _inputs(B, H, Hkv, length - call, t_max, hd, seed=length + call)
-        n = length - call
-        ref = torch.empty(B, H * hd, device="cuda", dtype=torch.float16)
+    tt = torch.float16 if dtype == nc.NC_F16 else torch.float32
+    t_max = lengths[0] + 8
+    for call, n in enumerate(lengths):   # the shared array keeps the previous call's contents
+        q, k, v = _inputs(B, H, Hkv, t_max, hd, dtype, seed=n + call)
+        ref = torch.empty(B, H * hd, device="cuda", dtype=tt)
         nbytes = nc.nc_op_attention_decode_scratch_bytes(B, H, t_max, hd)
         scratch = torch.empty(nbytes, dtype=torch.uint8, device="cuda")
-        nc.nc_op_attention_decode(q, k, v, ref, B, H, Hkv, n, t_max, hd, nc.NC_F16, scratch, nbytes)
-        got = torch.full((B, H * hd), float("nan"), device="cuda", dtype=torch.float16)
-        nc.nc_op_attention_decode_noalloc(q, k, v, got, B, H, Hkv, n, t_max, hd, nc.NC_F16)
+        nc.nc_op_attention_decode(q, k, v, ref, B, H, Hkv, n, t_max, hd, dtype, scratch, nbytes)
+        got = torch.full((B, H * hd), float("nan"), device="cuda", dtype=tt)
+        nc.nc_op_attention_decode_noalloc(q, k, v, got, B, H, Hkv, n, t_max, hd, dtype)
         torch.cuda.synchronize()
-        # same kernel, same inputs: the tests' fp16 rounding bound is far looser than needed
+        # the same kernels on the same inputs: a bound of one rounding of the output
+        # type is far looser than needed
+        eps = 2.0 ** -11 if dtype == nc.NC_F16 else 2.0 ** -23
         d = (got.float() - ref.float()).abs()
-        bound = 2.0 ** -11 * ref.float().abs() + 1e-5
+        bound = eps * ref.float().abs() + 1e-6
         assert bool((d <= bound).all()), f"call {call}: max diff {d.max().item():.3g}"
 
 

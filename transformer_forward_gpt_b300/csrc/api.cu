@@ -7,6 +7,9 @@
 
 #include <algorithm>
 #include <atomic>
+#include <map>
+#include <mutex>
+#include <utility>
 #include <vector>
 
 #include "common.cuh"
@@ -69,6 +72,20 @@ struct ProfRec {
 
 namespace nc {
 void count_launches(int n) { g_launches.fetch_add(n, std::memory_order_relaxed); }
+bool ensure_dyn_smem(const void* func, size_t bytes) {
+  int dev = 0;
+  if (cudaGetDevice(&dev) != cudaSuccess) return false;
+  static std::mutex mu;
+  static std::map<std::pair<const void*, int>, size_t> set_bytes;
+  std::lock_guard<std::mutex> lock(mu);
+  size_t& have = set_bytes[std::make_pair(func, dev)];
+  if (have >= bytes) return true;
+  if (cudaFuncSetAttribute(func, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)bytes) !=
+      cudaSuccess)
+    return false;
+  have = bytes;
+  return true;
+}
 void set_last_error(const char* fmt, ...) {
   va_list ap;
   va_start(ap, fmt);

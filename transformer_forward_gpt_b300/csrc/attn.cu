@@ -243,13 +243,7 @@ template <class T16>
 nc_status launch_attn(const void* q, const void* k, const void* v, void* o, int B, int H, int Hkv,
                       int T, int t_max, cudaStream_t s) {
   const size_t smem = 5 * kTileBytes;
-  static bool configured = false;
-  if (!configured) {
-    if (cudaFuncSetAttribute(attn_prefill_mma_kernel<T16>,
-                             cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem) != cudaSuccess)
-      return NC_ERR_CUDA;
-    configured = true;
-  }
+  if (!ensure_dyn_smem((const void*)attn_prefill_mma_kernel<T16>, smem)) return NC_ERR_CUDA;
   dim3 grid((T + kBq - 1) / kBq, B * H);
   const float scale_log2 = 1.4426950408889634f / sqrtf((float)kHd);
   attn_prefill_mma_kernel<T16><<<grid, 128, smem, s>>>((const T16*)q, (const T16*)k,

@@ -281,22 +281,13 @@ void launch_attention_decode_mma(const void* q, const void* k, const void* v, vo
   const float scale_log2 = 1.4426950408889634f / sqrtf((float)kHd);
   dim3 grid(ns, B * Hkv);
   if (dt == NC_F16) {
-    static bool cfg = false;
-    if (!cfg) {
-      cudaFuncSetAttribute(attn_decode_mma_kernel<f16>, cudaFuncAttributeMaxDynamicSharedMemorySize,
-                           (int)smem);
-      cfg = true;
-    }
+    // a refusal leaves the launch below to fail, which the caller's error check reports
+    ensure_dyn_smem((const void*)attn_decode_mma_kernel<f16>, smem);
     attn_decode_mma_kernel<f16><<<grid, 128, smem, s>>>((const f16*)q, (const f16*)k, (const f16*)v,
                                                          scratch, H, Hkv, len, t_max, ns, tps,
                                                          scale_log2);
   } else {
-    static bool cfg = false;
-    if (!cfg) {
-      cudaFuncSetAttribute(attn_decode_mma_kernel<bf16>,
-                           cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
-      cfg = true;
-    }
+    ensure_dyn_smem((const void*)attn_decode_mma_kernel<bf16>, smem);
     attn_decode_mma_kernel<bf16><<<grid, 128, smem, s>>>((const bf16*)q, (const bf16*)k,
                                                           (const bf16*)v, scratch, H, Hkv, len,
                                                           t_max, ns, tps, scale_log2);

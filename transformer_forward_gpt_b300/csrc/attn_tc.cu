@@ -587,32 +587,17 @@ nc_status tc_attention_prefill_tc(const void* q, const void* k, const void* v, v
   if (!status && cudaGetSymbolAddress(reinterpret_cast<void**>(&status), g_attn_status) != cudaSuccess)
     return NC_ERR_CUDA;
   a.status = status;
-  static int sms = 0;
-  if (sms == 0) {
-    int dev = 0;
-    if (cudaGetDevice(&dev) != cudaSuccess ||
-        cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev) != cudaSuccess || sms <= 0)
-      return NC_ERR_CUDA;
-  }
+  int sms = 0, dev = 0;
+  if (cudaGetDevice(&dev) != cudaSuccess ||
+      cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev) != cudaSuccess || sms <= 0)
+    return NC_ERR_CUDA;
   // one persistent CTA per SM (at most one per item)
   const unsigned grid = (unsigned)std::min(a.n_items, sms);
   if (half) {
-    static bool cfg = false;
-    if (!cfg) {
-      if (cudaFuncSetAttribute(attn_prefill_tc_kernel<f16>,
-                               cudaFuncAttributeMaxDynamicSharedMemorySize, (int)kSmem) != cudaSuccess)
-        return NC_ERR_CUDA;
-      cfg = true;
-    }
+    if (!ensure_dyn_smem((const void*)attn_prefill_tc_kernel<f16>, kSmem)) return NC_ERR_CUDA;
     attn_prefill_tc_kernel<f16><<<grid, kThreads, kSmem, s>>>(mq, mk, mv, a, layer);
   } else {
-    static bool cfg = false;
-    if (!cfg) {
-      if (cudaFuncSetAttribute(attn_prefill_tc_kernel<bf16>,
-                               cudaFuncAttributeMaxDynamicSharedMemorySize, (int)kSmem) != cudaSuccess)
-        return NC_ERR_CUDA;
-      cfg = true;
-    }
+    if (!ensure_dyn_smem((const void*)attn_prefill_tc_kernel<bf16>, kSmem)) return NC_ERR_CUDA;
     attn_prefill_tc_kernel<bf16><<<grid, kThreads, kSmem, s>>>(mq, mk, mv, a, layer);
   }
   count_launches(1);

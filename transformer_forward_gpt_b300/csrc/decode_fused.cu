@@ -1434,13 +1434,7 @@ template <int NT, class T16, class TW>
 static nc_status launch_t(const CUtensorMap& tk, const CUtensorMap& tv, Params p, int sms,
                           size_t smem, cudaStream_t s) {
   auto kern = decode_step_kernel<NT, T16, TW>;
-  static size_t configured = 0;
-  if (configured < smem) {
-    if (cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem) !=
-        cudaSuccess)
-      return NC_ERR_CUDA;
-    configured = smem;
-  }
+  if (!ensure_dyn_smem((const void*)kern, smem)) return NC_ERR_CUDA;
   void* args[] = {(void*)&tk, (void*)&tv, (void*)&p};
   const cudaError_t e = cudaLaunchCooperativeKernel((const void*)kern, dim3(sms), dim3(kThreads),
                                                     args, smem, s);

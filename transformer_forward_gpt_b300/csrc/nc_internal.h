@@ -12,6 +12,11 @@ namespace nc {
 void count_launches(int n);
 // Sets the thread-local text nc_last_error() returns.
 void set_last_error(const char* fmt, ...);
+// Raises the dynamic shared-memory limit of kernel `func` to at least `bytes` on
+// the current device. The attribute belongs to one device, so the sizes already
+// set are remembered per (kernel, device); concurrent callers are serialised.
+// Returns false if the runtime refuses.
+bool ensure_dyn_smem(const void* func, size_t bytes);
 
 // Where the rows of a projection output go (prefill: rows = B*T tokens of B
 // sequences starting at position pos0 = 0; decode: rows = B, one per sequence, at

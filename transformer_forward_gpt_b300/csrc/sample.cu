@@ -9,7 +9,10 @@
 // each thread owns a contiguous chunk of the row, sums its e[v], and a block scan
 // turns the chunk sums into intervals [lo, hi) that tile [0, Z).
 // The one thread whose interval holds u Z rescans its chunk in order and stops at
-// the first index where the running sum passes u Z. A temperature <= 0 is the
+// the first index where the running sum passes u Z. Where fp32 rounding leaves
+// no interval holding u Z (u Z rounded up to Z) or the running sum never passes
+// it, the draw is the last index of nonzero probability, so a token of zero
+// probability (a logit of -inf) is never drawn. A temperature <= 0 is the
 // zero-temperature limit: the greedy index, lowest on ties.
 #include <float.h>
 #include <math.h>
@@ -32,6 +35,17 @@ __device__ __forceinline__ float block_max(float v, float* red) {
   __syncthreads();
   v = lane < kWarps ? red[lane] : -INFINITY;
   for (int o = 16; o > 0; o >>= 1) v = fmaxf(v, __shfl_xor_sync(0xffffffffu, v, o));
+  __syncthreads();
+  return v;
+}
+
+__device__ __forceinline__ int block_max_int(int v, int* red) {
+  for (int o = 16; o > 0; o >>= 1) v = max(v, __shfl_xor_sync(0xffffffffu, v, o));
+  const int lane = threadIdx.x % 32, wid = threadIdx.x / 32;
+  if (lane == 0) red[wid] = v;
+  __syncthreads();
+  v = lane < kWarps ? red[lane] : INT_MIN;
+  for (int o = 16; o > 0; o >>= 1) v = max(v, __shfl_xor_sync(0xffffffffu, v, o));
   __syncthreads();
   return v;
 }
@@ -108,7 +122,12 @@ __global__ void __launch_bounds__(kThreads) sample_kernel(const float* __restric
   const int chunk = (V + kThreads - 1) / kThreads;
   const int c0 = min(V, tid * chunk), c1 = min(V, c0 + chunk);
   float s = 0.f;
-  for (int i = c0; i < c1; ++i) s += expf((row[i] - m) * inv_t);
+  int last_nz = -1;   // the chunk's last index of nonzero probability
+  for (int i = c0; i < c1; ++i) {
+    const float e = expf((row[i] - m) * inv_t);
+    s += e;
+    if (e > 0.f) last_nz = i;
+  }
   float lo, hi, z;
   block_intervals(s, redf, &lo, &hi, &z);
   float uu = u[blockIdx.x];
@@ -117,7 +136,7 @@ __global__ void __launch_bounds__(kThreads) sample_kernel(const float* __restric
   int k = INT_MAX;
   if (c0 < c1 && lo <= target && target < hi) {
     float acc = lo;
-    k = c1 - 1;   // rounding left the running sum at or below target: the chunk's end
+    k = last_nz;   // rounding left the running sum at or below target (hi > lo: last_nz >= c0)
     for (int i = c0; i < c1; ++i) {
       acc += expf((row[i] - m) * inv_t);
       if (acc > target) {
@@ -127,7 +146,8 @@ __global__ void __launch_bounds__(kThreads) sample_kernel(const float* __restric
     }
   }
   k = block_min_int(k, redi);
-  if (tid == 0) out[blockIdx.x] = k < V ? k : V - 1;   // none: target rounded up to z
+  if (k == INT_MAX) k = block_max_int(last_nz, redi);   // target rounded up to z
+  if (tid == 0) out[blockIdx.x] = k >= 0 && k < V ? k : V - 1;
 }
 
 }  // namespace

@@ -60,12 +60,9 @@ struct Seg {
 };
 struct Sched {
   int64_t pos, end;   // stream-K position / end, or persistent unit / units
-  int step, num_mu, rank, mc;
+  int step;
   bool sk;
-  __device__ __forceinline__ void init(const GemmArgs& p, int mc_, int rank_) {
-    mc = mc_;
-    rank = rank_;
-    num_mu = (p.num_m_blk + mc - 1) / mc;
+  __device__ __forceinline__ void init(const GemmArgs& p) {
     sk = p.stream_k != 0;
     if (sk) {
       const int64_t total = (int64_t)p.num_m_blk * p.num_n_blk * p.num_k_blk;
@@ -73,9 +70,9 @@ struct Sched {
       end = total * (blockIdx.x + 1) / gridDim.x;
       step = 0;
     } else {
-      pos = blockIdx.x / mc;
-      end = (int64_t)num_mu * p.num_n_blk * p.k_splits;
-      step = gridDim.x / mc;
+      pos = blockIdx.x;
+      end = (int64_t)p.num_m_blk * p.num_n_blk * p.k_splits;
+      step = gridDim.x;
     }
   }
   __device__ __forceinline__ bool next(const GemmArgs& p, Seg& g) {
@@ -90,8 +87,8 @@ struct Sched {
       pos += g.kb1 - g.kb0;
     } else {
       const int u = (int)pos;
-      g.mb = (u % num_mu) * mc + rank;
-      const int rest = u / num_mu;
+      g.mb = u % p.num_m_blk;
+      const int rest = u / p.num_m_blk;
       g.nb = rest % p.num_n_blk;
       g.ks = rest / p.num_n_blk;
       g.kb0 = g.ks * p.k_per_split;
@@ -295,11 +292,7 @@ __device__ __forceinline__ void epi_swap(const GemmArgs& p, uint32_t taddr, int 
 }
 
 // --------------------------------------------------------------------- kernel
-// MC = 2: CTAs run in clusters of two that take adjacent 128-row blocks of A
-// and the same B tile; each CTA loads half of the B tile and multicasts it to
-// both, so B is read from L2 once per pair. A stage is refilled only when both
-// CTAs' MMAs have released it (the empty barriers count both commits).
-template <int BN, int EPI, class T16, int MC>
+template <int BN, int EPI, class T16>
 __global__ void __launch_bounds__(192, 1)
     gemm_tc_kernel(const __grid_constant__ CUtensorMap tmA0, const __grid_constant__ CUtensorMap tmA1,
                    const __grid_constant__ CUtensorMap tmA2, const __grid_constant__ CUtensorMap tmB0,
@@ -322,7 +315,7 @@ __global__ void __launch_bounds__(192, 1)
   if (threadIdx.x == 0) {
     for (int s = 0; s < S; ++s) {
       mbar_init(&full[s], 1);
-      mbar_init(&empty[s], MC);
+      mbar_init(&empty[s], 1);
     }
     for (int b = 0; b < 2; ++b) {
       mbar_init(&tfull[b], 1);
@@ -341,11 +334,8 @@ __global__ void __launch_bounds__(192, 1)
   }
   tc_fence_before();
   __syncthreads();
-  if (MC > 1) cluster_sync_all();   // the peer's barriers exist before any multicast
   tc_fence_after();
   const uint32_t tmem_base = *tmem_slot;
-  // work segments; a cluster walks the same sequence
-  const int rank = MC > 1 ? (int)cluster_ctarank() : 0;
 
   if (warp == 0) {
     if (lane == 0) {
@@ -353,7 +343,7 @@ __global__ void __launch_bounds__(192, 1)
       int stage = 0, issued = 0;
       uint32_t phase = 0;
       Sched sc;
-      sc.init(p, MC, rank);
+      sc.init(p);
       Seg sg;
       while (!*abort_flag && sc.next(p, sg)) {
         const int mb = sg.mb, nb = sg.nb;
@@ -368,23 +358,11 @@ __global__ void __launch_bounds__(192, 1)
           int local;
           const CUtensorMap* ma = pick_map(&tmA0, &tmA1, &tmA2, mb * 128, p.a_split0, p.a_split1, local);
           tma_load_2d(sa, ma, &full[stage], kb * 64, local);
-          if (MC > 1) {
-            // this CTA's share of the B tile, to both CTAs of the pair
 #pragma unroll
-            for (int h = rank * (BN / C::kBoxRowsB / MC); h < (rank + 1) * (BN / C::kBoxRowsB / MC);
-                 ++h) {
-              const CUtensorMap* mb_ = pick_map(&tmB0, &tmB1, &tmB2, nb * BN + h * C::kBoxRowsB,
-                                                p.b_split0, p.b_split1, local);
-              tma_load_2d_mc(sb + h * C::kBoxRowsB * 128, mb_, &full[stage], kb * 64, local,
-                             (uint16_t)((1u << MC) - 1));
-            }
-          } else {
-#pragma unroll
-            for (int h = 0; h < BN / C::kBoxRowsB; ++h) {
-              const CUtensorMap* mb_ = pick_map(&tmB0, &tmB1, &tmB2, nb * BN + h * C::kBoxRowsB,
-                                                p.b_split0, p.b_split1, local);
-              tma_load_2d(sb + h * C::kBoxRowsB * 128, mb_, &full[stage], kb * 64, local);
-            }
+          for (int h = 0; h < BN / C::kBoxRowsB; ++h) {
+            const CUtensorMap* mb_ = pick_map(&tmB0, &tmB1, &tmB2, nb * BN + h * C::kBoxRowsB,
+                                              p.b_split0, p.b_split1, local);
+            tma_load_2d(sb + h * C::kBoxRowsB * 128, mb_, &full[stage], kb * 64, local);
           }
           if (++stage == S) {
             stage = 0;
@@ -411,7 +389,7 @@ __global__ void __launch_bounds__(192, 1)
       int acc = 0;
       uint32_t acc_phase = 0;
       Sched sc;
-      sc.init(p, MC, rank);
+      sc.init(p);
       Seg sg;
       while (!*abort_flag && sc.next(p, sg)) {
         const int kb0 = sg.kb0, kb1 = sg.kb1;
@@ -436,10 +414,7 @@ __global__ void __launch_bounds__(192, 1)
             mma_f16kind_ss(d_tmem, sdesc_kmajor_sw128(a_addr + k * 32),
                         sdesc_kmajor_sw128(b_addr + k * 32), kIdesc, (kb > kb0 || k > 0) ? 1u : 0u);
           }
-          if (MC > 1)
-            mma_commit_mc(&empty[stage], (uint16_t)((1u << MC) - 1));
-          else
-            mma_commit(&empty[stage]);
+          mma_commit(&empty[stage]);
           if (++stage == S) {
             stage = 0;
             phase ^= 1;
@@ -459,7 +434,7 @@ __global__ void __launch_bounds__(192, 1)
     int acc = 0;
     uint32_t acc_phase = 0;
     Sched sc;
-    sc.init(p, MC, rank);
+    sc.init(p);
     Seg sg;
     while (sc.next(p, sg)) {
       const int mb = sg.mb, nb = sg.nb, ks = sg.ks;
@@ -494,9 +469,6 @@ __global__ void __launch_bounds__(192, 1)
     tc_fence_after();
     tmem_dealloc(tmem_base, C::kTmemCols);
   }
-  // the peer may still multicast into this CTA's shared memory or arrive on its
-  // barriers until it is done too
-  if (MC > 1) cluster_sync_all();
 }
 
 
@@ -564,64 +536,13 @@ static int sm_count_now() {
   return n;
 }
 
-// Tile-mode GEMMs with 256-wide N tiles run in clusters of two that share the
-// B tile through TMA multicast when NC_GEMM_MC=1 is set in the environment.
-static bool use_multicast() {
-  static int v = -1;
-  if (v < 0) {
-    const char* e = getenv("NC_GEMM_MC");
-    v = (e && e[0] == '1') ? 1 : 0;
-  }
-  return v == 1;
-}
-
 template <int BN, int EPI, class T16>
 static nc_status launch_gemm(const CUtensorMap& a0, const CUtensorMap& a1, const CUtensorMap& a2,
                              const CUtensorMap& b0, const CUtensorMap& b1, const CUtensorMap& b2,
                              const GemmArgs& args, int sm_count, cudaStream_t s) {
   using C = TileCfg<BN>;
-  if constexpr (BN == 256 && EPI != EPI_SWAP) {
-    if (use_multicast() && !args.stream_k) {
-      auto kern = gemm_tc_kernel<BN, EPI, T16, 2>;
-      static int max_pairs = -1;
-      cudaLaunchConfig_t cfg = {};
-      cudaLaunchAttribute at[1];
-      at[0].id = cudaLaunchAttributeClusterDimension;
-      at[0].val.clusterDim.x = 2;
-      at[0].val.clusterDim.y = 1;
-      at[0].val.clusterDim.z = 1;
-      cfg.blockDim = dim3(192);
-      cfg.dynamicSmemBytes = C::kSmemBytes;
-      cfg.attrs = at;
-      cfg.numAttrs = 1;
-      if (max_pairs < 0) {
-        max_pairs = 0;
-        if (cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize,
-                                 (int)C::kSmemBytes) == cudaSuccess) {
-          cfg.gridDim = dim3(2 * (sm_count / 2));
-          int n = 0;
-          if (cudaOccupancyMaxActiveClusters(&n, kern, &cfg) == cudaSuccess) max_pairs = n;
-        }
-        cudaGetLastError();
-      }
-      if (max_pairs > 0) {
-        const int pair_units = (args.num_m_blk + 1) / 2 * args.num_n_blk * args.k_splits;
-        cfg.gridDim = dim3(2 * std::min(pair_units, max_pairs));
-        cfg.stream = s;
-        const cudaError_t e = cudaLaunchKernelEx(&cfg, kern, a0, a1, a2, b0, b1, b2, args);
-        count_launches(1);
-        return e == cudaSuccess ? NC_OK : NC_ERR_CUDA;
-      }
-    }
-  }
-  auto kern = gemm_tc_kernel<BN, EPI, T16, 1>;
-  static bool configured = false;
-  if (!configured) {
-    if (cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize,
-                             (int)C::kSmemBytes) != cudaSuccess)
-      return NC_ERR_CUDA;
-    configured = true;
-  }
+  auto kern = gemm_tc_kernel<BN, EPI, T16>;
+  if (!ensure_dyn_smem((const void*)kern, C::kSmemBytes)) return NC_ERR_CUDA;
   const int units = args.num_m_blk * args.num_n_blk * args.k_splits;
   const int grid = args.stream_k ? sm_count : std::min(units, sm_count);
   kern<<<grid, 192, C::kSmemBytes, s>>>(a0, a1, a2, b0, b1, b2, args);
