@@ -333,12 +333,15 @@ NC_API int64_t nc_launch_count(void);
  * after the final norm and after the LM head), and the last entry at the end.
  * Then, for the phase ending at barrier k, six marks at 2*nbar + 2 + 6(k-1) + m
  * (nbar = barriers per step): projections record m = 3 when they start staging
- * the activations, 0 when that is done, 1 after the multiply loop and 2 after
- * adding the partial sums of each run; attention records m = 0 after preparing q, 1 after the key tiles, 2
- * after writing its partial state and 3 after the merge, for each (sequence, KV
+ * the activations, 0 when that is done, 1 when an accumulator has been read from
+ * tensor memory and 2 after adding its partial sums (per row group; the last one
+ * stays); attention records m = 0 after preparing q, 1 after the key tiles, 2
+ * after writing its partial state and 3 at the end, for each (sequence, KV
  * head) it covers (later segments overwrite earlier ones; unused marks stay as
  * they were); m = 4 is when CTA 0's producer started loading the phase's weights
- * or K/V tiles; m = 5 is unused. capacity must be at least nc_decode_trace_entries(cfg), else nothing is
+ * or K/V tiles; m = 5 is unused. After those 8 * nbar + 2 entries, every CTA c < 256 of the launch
+ * records, for barrier k, its arrival and exit time at 8 * nbar + 2 + 2 * (256 * (k - 1) + c)
+ * (+ 1). capacity must be at least nc_decode_trace_entries(cfg), else nothing is
  * recorded. dev_buf NULL switches it off. Only the first 32 sequences' launch of
  * a step is traced. The readings cost one store each. */
 NC_API nc_status nc_decode_trace(nc_model* m, uint64_t* dev_buf, int32_t capacity);

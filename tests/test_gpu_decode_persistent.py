@@ -132,8 +132,13 @@ def test_phase_trace_is_ordered(cuda_device):
     main = t[: 2 * nbar + 2]
     assert (np.diff(main) >= 0).all(), "barrier timestamps must be non-decreasing"
     assert main[-1] > main[0]
-    marks = t[2 * nbar + 2:].reshape(-1, 6)
+    marks = t[2 * nbar + 2: 8 * nbar + 2].reshape(-1, 6)
     for k in range(2, nbar):   # producer started each streamed phase before it ended
         if marks[k - 1, 4]:
             assert marks[k - 1, 4] <= main[2 * k - 1]
+    # per CTA and barrier: arrival <= exit, and no CTA leaves before the last arrives
+    sms = torch.cuda.get_device_properties(0).multi_processor_count
+    per = t[8 * nbar + 2:].reshape(nbar, 256, 2)[:, :min(sms, 256)]
+    assert (per[:, :, 0] > 0).all() and (per[:, :, 0] <= per[:, :, 1]).all()
+    assert (per[:, :, 1].min(axis=1) >= per[:, :, 0].max(axis=1)).all()
     assert nc.nc_model_check(model.handle) == nc.NC_OK

@@ -129,13 +129,12 @@ struct nc_model {
   int decode_path = NC_DECODE_AUTO;
   int sms = 0;
   nc::dec::Layout dlay{};
-  uint8_t* dpack = nullptr;     // weights in mma-fragment order
+  uint8_t* dpack = nullptr;     // weights in 16 KB swizzled units
   void* dws = nullptr;          // its scratch
   float* d_qkv = nullptr;
   float* d_hacc = nullptr;
   float* d_ss = nullptr;
-  void* d_xnf = nullptr;
-  unsigned int* d_cnt = nullptr;
+  void* d_xnf = nullptr;         // final-norm image of the LM head's B operand
   unsigned long long* d_amkey = nullptr;
   unsigned int* d_amcnt = nullptr;
   unsigned long long* d_bar = nullptr;
@@ -629,9 +628,12 @@ nc_status prefill_common(nc_model* m, const int32_t* tokens, int32_t B, int32_t 
 // ------------------------------------------------ persistent decode step
 bool decode_fused_applies(const nc_model* m) {
   const nc_config& c = m->cfg;
-  return m->adt != NC_F32 &&
-         nc::dec::supported(c.d_model, c.n_head, c.n_kv_head, c.d_mlp, c.head_dim) &&
-         c.vocab % 4 == 0;
+  if (m->adt == NC_F32 || c.vocab % 4 != 0) return false;
+  int dev = 0, sms = 0;
+  if (cudaGetDevice(&dev) != cudaSuccess ||
+      cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev) != cudaSuccess || sms <= 0)
+    return false;
+  return nc::dec::supported(c.d_model, c.n_head, c.n_kv_head, c.d_mlp, c.head_dim, c.vocab, sms);
 }
 
 nc_status decode_fused_init(nc_model* m, cudaStream_t s) {
@@ -653,7 +655,7 @@ nc_status decode_fused_init(nc_model* m, cudaStream_t s) {
   };
   const size_t o_qkv = carve((size_t)2 * K * m->dlay.nqkv_pad * 4),
                o_h = carve((size_t)K * c.d_mlp * 4), o_ss = carve((size_t)2 * c.n_layer * K * 4),
-               o_xnf = carve((size_t)c.d_model * 64), o_cnt = carve((size_t)K * c.n_kv_head * 4),
+               o_xnf = carve((size_t)m->dlay.xn_img_bytes),
                o_key = carve((size_t)K * 8), o_amc = carve((size_t)K * 4), o_bar = carve(8);
   if (cudaMalloc(&m->dws, off) != cudaSuccess) {
     cudaGetLastError();
@@ -667,7 +669,6 @@ nc_status decode_fused_init(nc_model* m, cudaStream_t s) {
   m->d_hacc = reinterpret_cast<float*>(b + o_h);
   m->d_ss = reinterpret_cast<float*>(b + o_ss);
   m->d_xnf = b + o_xnf;
-  m->d_cnt = reinterpret_cast<unsigned int*>(b + o_cnt);
   m->d_amkey = reinterpret_cast<unsigned long long*>(b + o_key);
   m->d_amcnt = reinterpret_cast<unsigned int*>(b + o_amc);
   m->d_bar = reinterpret_cast<unsigned long long*>(b + o_bar);
@@ -743,10 +744,8 @@ nc_status decode_fused(nc_model* m, const int32_t* tokens, int32_t B, int32_t po
     p.qkv_acc = m->d_qkv;
     p.hacc = m->d_hacc;
     p.ss = m->d_ss;
-    p.att = m->att;
-    p.xnf = m->d_xnf;
+    p.xn_img = m->d_xnf;
     p.logits = (logits ? logits : m->logits_tmp) + (size_t)b0 * cfg.vocab;
-    p.attn_count = m->d_cnt;
     p.argmax_key = m->d_amkey;
     p.argmax_count = m->d_amcnt;
     p.bar_counter = m->d_bar;
@@ -757,7 +756,7 @@ nc_status decode_fused(nc_model* m, const int32_t* tokens, int32_t B, int32_t po
     p.trace = (b0 == 0 && m->dec_trace && m->dec_trace_cap >= nc::dec::trace_entries(cfg.n_layer))
                   ? m->dec_trace
                   : nullptr;
-    p.rec_stride = (G * (cfg.head_dim + 2) + 3) / 4 * 4;
+    p.rec_stride = G * (cfg.head_dim + 4);
     const size_t part = (size_t)Bc * cfg.n_kv_head * p.attn_slots * p.rec_stride * 4;
     if (part > m->d_part_bytes) {
       // grows on the first calls of a larger shape only (the free waits for the device)

@@ -11,10 +11,13 @@ namespace dec {
 constexpr int kMaxTok = 32;   // sequences per launch (larger batches run in chunks)
 
 // Byte layout of the packed decode weights: per layer [QKV | O | FC | PROJ],
-// then the LM head; each matrix in 8 KB units of 128 rows x 32 columns.
+// then the LM head; each matrix in 16 KB units of 128 rows x 64 columns. The
+// final norm is kept as an image of the LM head's B operand: per 64-column
+// chunk, kMaxTok token rows of 128 bytes.
 struct Layout {
   int nqkv, nqkv_pad, vpad;
   int64_t off_o, off_fc, off_proj, layer_bytes, total_bytes;
+  int64_t xn_img_bytes;
 };
 
 struct PackSrc {
@@ -32,7 +35,7 @@ struct Params {
   int B, b_off, pos, cache_batch, t_max;
   int L, d, H, Hkv, F, V, vpad, nqkv, nqkv_pad;
   int stages, act_bytes, attn_slots;
-  int rec_stride;             // floats per partial record: G*(128+2) rounded up to 4
+  int rec_stride;             // floats per partial record: G heads x [m, l, -, -, o[128]]
   float eps, scale_log2;
   int64_t layer_bytes, off_o, off_fc, off_proj;
   const int32_t* tokens;      // [B]
@@ -47,11 +50,9 @@ struct Params {
   float* qkv_acc;             // [2][kMaxTok][nqkv_pad]
   float* hacc;                // [kMaxTok][F]
   float* ss;                  // [2 L][kMaxTok]
-  void* att;                  // [kMaxTok][H*128] 16-bit
-  void* xnf;                  // final-norm fragments [d/16][NT][32] x 8 bytes
+  void* xn_img;               // final norm, B-chunk image [d/64][kMaxTok][128 B]
   float* logits;              // [B][V]
   float* attn_part;           // partial softmax states
-  unsigned int* attn_count;   // [kMaxTok * Hkv]
   unsigned long long* argmax_key;   // [kMaxTok]
   unsigned int* argmax_count;       // [kMaxTok]
   unsigned long long* bar_counter;  // grid barrier arrivals (monotonic)
@@ -66,15 +67,21 @@ struct Params {
 
 Layout layout_of(int L, int d, int H, int Hkv, int F, int V);
 int64_t packed_bytes(int N, int K);
-bool supported(int d, int H, int Hkv, int F, int hd);
+// Whether the persistent step has a configuration for this shape on P SMs.
+bool supported(int d, int H, int Hkv, int F, int hd, int V, int P);
 nc_status pack_weights(const PackSrc& src, bool half, uint8_t* out, cudaStream_t s);
 int attn_slots_needed(int B, int Hkv, int pos, int P);
 // TMA view of a KV array (all layers) as [rows, 128] 16-bit values.
 bool make_cache_map(CUtensorMap* map, void* base, uint64_t rows, bool half);
 // Grid barriers one launch passes (its arrivals are that times the grid size).
 inline int barriers_per_step(int L) { return 5 * L + 3; }
-// Entries of a full trace (barrier times plus 6 marks per phase).
-inline int trace_entries(int L) { return 8 * barriers_per_step(L) + 2; }
+// CTAs whose barrier arrival and exit times a trace records.
+constexpr int kTraceCtas = 256;
+// Entries of a full trace: CTA 0's barrier times, 6 marks per phase, then per
+// barrier and CTA (up to kTraceCtas) its arrival and exit time.
+inline int trace_entries(int L) {
+  return 8 * barriers_per_step(L) + 2 + 2 * kTraceCtas * barriers_per_step(L);
+}
 // Enqueues one step for p.B <= kMaxTok sequences on `sms` CTAs (cooperative launch).
 nc_status launch_step(const CUtensorMap& tk, const CUtensorMap& tv, Params p, bool half,
                       nc_dtype wdt, int sms, cudaStream_t s);
