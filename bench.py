@@ -295,6 +295,8 @@ def run_ours(args):
     # end to end through the C ABI with host buffers
     e2e = (run_e2e(nc, synth, mp, cp, md, cd, sp, Bp, Tp, sd, Bd, Td, steps, args, dev, stream)
            if not args.no_e2e else {"prefill": None, "decode": None})
+    report = (report_configs(nc, synth, peaks, peak_src, dev, stream)
+              if not args.no_report else None)
 
     if rank != 0:
         return
@@ -361,6 +363,7 @@ def run_ours(args):
                    "e2e": e2e["decode"]},
         "roofline": roof,
         "kernel_ms_per_step": {k: round(v[0], 3) for k, v in merged.items()},
+        "report": report,
         "e2e": e2e["prefill"],
         "gpu_launches": int(launches),
         "clocks": clocks,
@@ -369,6 +372,98 @@ def run_ours(args):
     if world == 1 and not args.no_cpu_baseline:
         line["cpu_baseline"] = cpu_baseline(budget_s=args.cpu_budget)
     print(json.dumps(line), flush=True)
+
+
+def report_configs(nc, synth, peaks, peak_src, dev, stream, reps=5):
+    """The other configurations of the workload table, each timed on its own after
+    the headline step (CUDA events on the launching stream, warm-up first):
+    d12 and d26 prefill (all logits) with their tensor-roofline fractions, d26
+    KV-cache decode (B64, 64 steps at context 2048..2111) with its HBM fraction,
+    and the headline d20 prefill with literal bf16 activations and KV cache
+    (act_dtype bf16) beside the default fp16 operands. Inputs are larger than L2."""
+    import torch
+    out = {}
+
+    def timed(fn, n):
+        fn()
+        fn()
+        torch.cuda.synchronize()
+        e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+        e0.record(stream)
+        for _ in range(n):
+            fn()
+        e1.record(stream)
+        torch.cuda.synchronize()
+        return e0.elapsed_time(e1) / n
+
+    def prefill_case(key, wl_name, act_dtype, note):
+        wl = synth.WORKLOADS[wl_name]
+        sh, B, T = wl.shape, wl.batch, wl.seq
+        W = synth.make_weights(sh)
+        m = nc.Model(W, max_seq=T, max_batch=B, act_dtype=act_dtype)
+        del W
+        c = m.cache(B, T)
+        tok = torch.from_numpy(synth.make_tokens(sh, B, T)).to(dev)
+        logits = torch.empty(B, T, sh.vocab, device=dev)
+        ms = timed(lambda: nc.nc_prefill(m.handle, tok, B, T, logits, c.handle, stream), reps)
+        g, a = prefill_flops(sh, B, T)
+        tf = (g + a) / (ms / 1e3) / 1e12
+        out[key] = {"workload": f"{sh.name} prefill B{B}xT{T}", "tok_s": round(B * T / (ms / 1e3), 1),
+                    "ms": round(ms, 3), "tflops": round(tf, 1),
+                    "frac_of_peak": round(tf / peaks["bf16_tflops"], 4),
+                    "peak": peaks["bf16_tflops"], "peak_source": f"{peak_src} bf16", "operands": note}
+        del logits, tok
+        c.close()
+        m.close()
+        torch.cuda.empty_cache()
+
+    def decode_case():
+        wl = synth.WORKLOADS["d26_decode"]
+        sh, B, T0, steps = wl.shape, wl.batch, wl.seq, wl.decode_steps
+        W = synth.make_weights(sh)
+        m = nc.Model(W, max_seq=T0 + steps, max_batch=B)
+        del W
+        c = m.cache(B, T0 + steps)
+        tok0 = torch.empty(B, dtype=torch.int32, device=dev)
+        nc.nc_prefill_last(m.handle, torch.from_numpy(synth.make_tokens(sh, B, T0)).to(dev), B, T0, None,
+                           tok0, c.handle, stream)
+        buf = torch.empty(B, dtype=torch.int32, device=dev)
+
+        def decode_window():
+            nc.nc_kv_cache_set_length(c.handle, T0)
+            buf.copy_(tok0)
+            for j in range(steps):
+                nc.nc_decode_step(m.handle, buf, B, T0 + j, None, buf, c.handle, stream)
+
+        ms = timed(decode_window, 2)
+        per_step = ms / steps
+        byts = sum(decode_bytes(sh, B, T0 + j) for j in range(steps)) / steps
+        gbs = byts / (per_step / 1e3) / 1e9
+        out["d26_decode"] = {"workload": f"d26 decode B{B} ctx {T0}..{T0 + steps - 1}, {steps} steps",
+                             "tok_s": round(B / (per_step / 1e3), 1), "ms_per_token_step": round(per_step, 4),
+                             "gbs": round(gbs, 1), "algorithmic_mb_per_step": round(byts / 1e6, 1),
+                             "frac_of_peak": round(gbs / peaks["hbm_gbs"], 4), "peak": peaks["hbm_gbs"],
+                             "peak_source": f"{peak_src} HBM copy",
+                             "launches_per_step": -(-B // 32)}
+        if nc.nc_model_check(m.handle) != nc.NC_OK:
+            raise RuntimeError("device status set during the report configurations")
+        c.close()
+        m.close()
+        torch.cuda.empty_cache()
+
+    def guarded(key, fn, *a):
+        try:
+            fn(*a)
+        except Exception as e:   # a failing extra measurement is reported, not fatal
+            out[key] = {"error": f"{type(e).__name__}: {e}"[:300]}
+            torch.cuda.empty_cache()
+
+    guarded("d12_prefill", prefill_case, "d12_prefill", "d12_prefill", nc.NC_F16, "fp16 (bf16 weights)")
+    guarded("d26_prefill", prefill_case, "d26_prefill", "d26_prefill", nc.NC_F16, "fp16 (bf16 weights)")
+    guarded("d20_prefill_bf16_mode", prefill_case, "d20_prefill_bf16_mode", "d20_prefill", nc.NC_BF16,
+            "bf16 activations and KV cache")
+    guarded("d26_decode", decode_case)
+    return out
 
 
 def recorded_traffic(kind):
@@ -564,6 +659,8 @@ def main():
     ap.add_argument("--impl", choices=("ours", "reference"), default="ours")
     ap.add_argument("--no-cpu-baseline", action="store_true")
     ap.add_argument("--no-e2e", action="store_true", help="skip the host-buffer runs")
+    ap.add_argument("--no-report", action="store_true",
+                    help="skip the other configurations (d12, d26, bf16 mode)")
     ap.add_argument("--phase", choices=("both", "prefill", "decode"), default="both",
                     help="profiling aid: run only one phase of the step (no JSON line)")
     ap.add_argument("--prefill-batch", type=int, default=None,

@@ -196,9 +196,10 @@ NC_API nc_status nc_decode_step(nc_model* m, const int32_t* tokens, int32_t B, i
  *   NC_DECODE_KERNELS     always one kernel per step of the block.
  * The persistent kernel runs a whole decode step for up to 32 sequences as one
  * cooperative launch with one CTA per SM: a producer warp streams every weight
- * matrix (packed once, on first use, into a model-owned copy in mma-fragment
- * order) and the KV cache through shared memory, while the other warps compute
- * the phases of the step between grid-wide barriers. Larger batches run as
+ * matrix (packed once, on first use, into a model-owned copy of 16 KB units in
+ * the tensor core's swizzled layout) and the KV cache through shared memory, an
+ * MMA warp runs the projections on tcgen05, and the other warps compute the
+ * phases of the step between grid-wide barriers. Larger batches run as
  * several launches of up to 32 sequences. Projection partial sums are added in
  * fp32 in a run-dependent order. The fp32 path always uses kernels. */
 typedef enum { NC_DECODE_AUTO = 0, NC_DECODE_PERSISTENT = 1, NC_DECODE_KERNELS = 2 } nc_decode_path;
@@ -219,6 +220,35 @@ NC_API nc_status nc_generate_host(nc_model* m, const int32_t* prompt, int32_t B,
  * >= len count as empty again and are overwritten by the next prefill / decode
  * steps (e.g. to roll back rejected tokens, or to replay a decode window). */
 NC_API nc_status nc_kv_cache_set_length(nc_kv_cache* c, int32_t len);
+
+/* Per-sequence cache lengths (the KV cache of jxzklqfsx.com, KV-cache paragraph,
+ * kept for sequences of different lengths, as an Engine serving several requests
+ * does: CSDN nanochat article, wap.jaobe.com, inference paragraph).
+ * Every prefill / decode call sets the lengths of the sequences it ran; the
+ * uniform calls (nc_prefill_continue, nc_decode_step) need all of their B
+ * sequences at the same length. nc_kv_cache_set_lengths shortens sequences
+ * [0, n) to lens[b] (host int32 [n]; each 0 <= lens[b] <= its current length;
+ * NC_ERR_INVALID_ARG otherwise, nothing changed): a batch prefilled to a common
+ * padded length T becomes ragged by cutting each sequence back to its own prompt
+ * length (causal attention makes the kept rows independent of the cut ones).
+ * nc_kv_cache_lengths copies the lengths of sequences [0, n) to lens (host). The
+ * largest length is what nc_kv_cache_view reports. */
+NC_API nc_status nc_kv_cache_set_lengths(nc_kv_cache* c, const int32_t* lens, int32_t n);
+NC_API nc_status nc_kv_cache_lengths(const nc_kv_cache* c, int32_t* lens, int32_t n);
+
+/* One decode step with a position per sequence (jxzklqfsx.com, KV-cache
+ * paragraph; CSDN nanochat article, Engine paragraph): sequence b's token
+ * tokens[b] (dev int32 [B]) sits at position pos[b] (HOST int32 [B]), which must
+ * equal that sequence's cache length; its K/V are written at pos[b], it attends
+ * over positions 0..pos[b] with RoPE at pos[b], and its length becomes
+ * pos[b] + 1. Outputs as nc_decode_step. Runs on the persistent kernel only:
+ * NC_ERR_UNSUPPORTED for fp32 models, shapes the persistent kernel does not
+ * take, or a model switched to NC_DECODE_KERNELS. NC_ERR_INVALID_ARG (nothing
+ * enqueued) when a position differs from its cache length, is 0, or leaves no
+ * room (pos[b] + 1 > t_max). */
+NC_API nc_status nc_decode_step_ragged(nc_model* m, const int32_t* tokens, const int32_t* pos,
+                                       int32_t B, float* logits, int32_t* argmax_out,
+                                       nc_kv_cache* c, void* stream);
 
 /* Synchronises `stream`, reads and clears the device status word. Returns NC_OK,
  * NC_ERR_BOUNDS or NC_ERR_DEVICE_TIMEOUT (or NC_ERR_CUDA). */

@@ -8,9 +8,9 @@ within tolerance, slots past the length still holding the poison value).
 
 The shapes cover: every N-tile width of the kernel (B = 1, 5, 12, 20, 32) and
 batches above 32 (several launches), MQA / GQA / MHA (one query head per KV
-head), contexts whose last 16-position tile is partial, long contexts where
-one (sequence, KV head) spans several CTAs (the partial softmax states are
-merged by the last of them), d_model 768 / 1280 / 1664, and bf16 storage.
+head), contexts whose last 32-position tile is partial, long contexts where
+one (sequence, KV head) spans several CTAs (the O projection merges their
+partial softmax states), d_model 768 / 1280 / 1664, and bf16 storage.
 """
 import numpy as np
 import pytest
@@ -76,6 +76,13 @@ def test_batch_above_32_runs_in_chunks(cuda_device):
 def test_long_context_spans_ctas(cuda_device):
     # 2 sequences x 1 KV head x 63 tiles: each (sequence, KV head) covers ~74 CTAs
     _run(_small(synth.D20_MQA, n_layer=2, vocab=1000), 2, 1000, 3)
+
+
+def test_tiles_shared_evenly_over_many_laps(cuda_device):
+    """More (sequence, KV head) pairs than CTAs: the tiles of all pairs are shared
+    evenly, about 50 per CTA, so the ring of stages turns over many times within
+    one attention phase and the CTAs hold pieces of several pairs."""
+    _run(_small(synth.D26, n_layer=1, vocab=512), 12, 1500, 2, seqs=[0, 5, 11])
 
 
 @pytest.mark.parametrize("base", [synth.D12, synth.D26])

@@ -26,6 +26,7 @@ EXPORTS = (
     "nc_kv_cache_set_length", "nc_profile_begin", "nc_profile_end", "nc_launch_count",
     "nc_op_attention_decode_noalloc", "nc_model_set_decode_path", "nc_decode_trace",
     "nc_decode_trace_entries", "nc_op_sample", "nc_prefill_continue",
+    "nc_decode_step_ragged", "nc_kv_cache_set_lengths", "nc_kv_cache_lengths",
 )
 
 KERNEL_KINDS = ("embed", "norm", "qkv", "attn_prefill", "attn_decode", "oproj", "fc", "proj",
@@ -100,6 +101,9 @@ def load(path: str = LIB_PATH):
         "nc_model_set_decode_path": (C.c_int, [vp, C.c_int]),
         "nc_decode_trace": (C.c_int, [vp, vp, i32]),
         "nc_decode_trace_entries": (i32, [C.POINTER(NcConfig)]),
+        "nc_decode_step_ragged": (C.c_int, [vp, vp, C.POINTER(i32), i32, vp, vp, vp, vp]),
+        "nc_kv_cache_set_lengths": (C.c_int, [vp, C.POINTER(i32), i32]),
+        "nc_kv_cache_lengths": (C.c_int, [vp, C.POINTER(i32), i32]),
     }
     for name, (res, args) in sig.items():
         f = getattr(lib, name)
@@ -284,6 +288,24 @@ def nc_op_attention_decode_noalloc(q, k, v, o, B, H, Hkv, length, t_max, hd, dty
     _check(load().nc_op_attention_decode_noalloc(_ptr(q), _ptr(k), _ptr(v), _ptr(o), B, H, Hkv,
                                                  length, t_max, hd, dtype, _stream(stream)),
            "nc_op_attention_decode_noalloc")
+
+
+def nc_decode_step_ragged(model, tokens, pos, B, logits, argmax_out, cache, stream=None):
+    """pos: host sequence of B positions (one per sequence)."""
+    arr = (C.c_int32 * B)(*[int(x) for x in pos])
+    _check(load().nc_decode_step_ragged(model, _ptr(tokens), arr, B, _ptr(logits), _ptr(argmax_out),
+                                        cache, _stream(stream)), "nc_decode_step_ragged")
+
+
+def nc_kv_cache_set_lengths(cache, lens):
+    arr = (C.c_int32 * len(lens))(*[int(x) for x in lens])
+    _check(load().nc_kv_cache_set_lengths(cache, arr, len(lens)), "nc_kv_cache_set_lengths")
+
+
+def nc_kv_cache_lengths(cache, n):
+    arr = (C.c_int32 * n)()
+    _check(load().nc_kv_cache_lengths(cache, arr, n), "nc_kv_cache_lengths")
+    return list(arr)
 
 
 def nc_kv_cache_set_length(cache, length):

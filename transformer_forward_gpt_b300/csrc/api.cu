@@ -188,7 +188,8 @@ struct nc_kv_cache {
   void* v = nullptr;
   void* mem = nullptr;
   bool owns = false;
-  int32_t batch = 0, t_max = 0, len = 0;
+  int32_t batch = 0, t_max = 0, len = 0;   // len: the largest of lens
+  std::vector<int32_t> lens;                 // filled positions of each sequence
   size_t layer_elems = 0;  // batch * Hkv * t_max * hd
   bool maps = false;       // TMA views of K and V for the persistent decode step
   CUtensorMap tmk, tmv;
@@ -445,6 +446,7 @@ nc_status nc_kv_cache_alloc(const nc_model* m, int32_t batch, int32_t t_max, voi
   c->batch = batch;
   c->t_max = t_max;
   c->layer_elems = (size_t)batch * m->cfg.n_kv_head * t_max * m->cfg.head_dim;
+  c->lens.assign(batch, 0);
   if (!mem) {
     if (cudaMalloc(&c->mem, bytes) != cudaSuccess) {
       cudaGetLastError();
@@ -608,8 +610,20 @@ nc_status check_prefill_args(nc_model* m, const int32_t* tokens, int32_t B, int3
   return NC_OK;
 }
 
+// Sets the lengths of sequences [0, B) to n and len to the largest length.
+void set_lens(nc_kv_cache* c, int32_t B, int32_t n) {
+  for (int32_t b = 0; b < B; ++b) c->lens[b] = n;
+  c->len = *std::max_element(c->lens.begin(), c->lens.end());
+}
+// True when sequences [0, B) all hold n positions.
+bool lens_equal(const nc_kv_cache* c, int32_t B, int32_t n) {
+  for (int32_t b = 0; b < B; ++b)
+    if (c->lens[b] != n) return false;
+  return true;
+}
+
 // Runs T positions of B sequences starting at absolute position pos0 (the cache
-// already holds positions 0..pos0-1) and sets the cache length to pos0 + T.
+// already holds positions 0..pos0-1) and sets their cache lengths to pos0 + T.
 nc_status prefill_common(nc_model* m, const int32_t* tokens, int32_t B, int32_t T,
                          nc_kv_cache* c, cudaStream_t s, int32_t pos0 = 0) {
   const int64_t M = (int64_t)B * T;
@@ -620,7 +634,7 @@ nc_status prefill_common(nc_model* m, const int32_t* tokens, int32_t B, int32_t 
   }
   nc_status st = run_blocks(m, c, B, T, pos0, s);
   if (st != NC_OK) return st;
-  c->len = pos0 + T;
+  set_lens(c, B, pos0 + T);
   return NC_OK;
 }
 
@@ -693,8 +707,10 @@ nc_status decode_fused_init(nc_model* m, cudaStream_t s) {
   return NC_OK;
 }
 
-nc_status decode_fused(nc_model* m, const int32_t* tokens, int32_t B, int32_t pos, float* logits,
-                       int32_t* argmax_out, nc_kv_cache* c, cudaStream_t s) {
+// One persistent decode step for B sequences; sequence b's new token sits at
+// position pos[b] (host array), which is also its cache length.
+nc_status decode_fused(nc_model* m, const int32_t* tokens, int32_t B, const int32_t* pos,
+                       float* logits, int32_t* argmax_out, nc_kv_cache* c, cudaStream_t s) {
   nc_status st = decode_fused_init(m, s);
   if (st != NC_OK) return st;
   const nc_config& cfg = m->cfg;
@@ -713,7 +729,7 @@ nc_status decode_fused(nc_model* m, const int32_t* tokens, int32_t B, int32_t po
     nc::dec::Params p{};
     p.B = Bc;
     p.b_off = b0;
-    p.pos = pos;
+    for (int i = 0; i < Bc; ++i) p.pos[i] = pos[b0 + i];
     p.cache_batch = c->batch;
     p.t_max = c->t_max;
     p.L = cfg.n_layer;
@@ -725,7 +741,8 @@ nc_status decode_fused(nc_model* m, const int32_t* tokens, int32_t B, int32_t po
     p.vpad = m->dlay.vpad;
     p.nqkv = m->dlay.nqkv;
     p.nqkv_pad = m->dlay.nqkv_pad;
-    p.attn_slots = nc::dec::attn_slots_needed(Bc, cfg.n_kv_head, pos, m->sms);
+    p.attn_slots = nc::dec::plan_attention(p, m->sms);
+    NC_CHECK(p.attn_slots > 0, NC_ERR_UNSUPPORTED, "decode attention work too large");
     p.eps = cfg.rms_eps;
     p.scale_log2 = (float)(1.4426950408889634 / sqrt((double)cfg.head_dim));
     p.layer_bytes = m->dlay.layer_bytes;
@@ -799,7 +816,9 @@ nc_status nc_prefill_continue(nc_model* m, const int32_t* tokens, int32_t B, int
   nc_status st = check_prefill_args(m, tokens, B, T, c);
   if (st != NC_OK) return st;
   NC_CHECK(logits && aligned16(logits), NC_ERR_INVALID_ARG, "logits NULL or misaligned");
-  const int32_t pos0 = c->len;
+  const int32_t pos0 = c->lens[0];
+  NC_CHECK(lens_equal(c, B, pos0), NC_ERR_INVALID_ARG,
+           "continuing a prefill needs the same cache length for all %d sequences", B);
   NC_CHECK((int64_t)pos0 + T <= c->t_max && (int64_t)pos0 + T <= m->cfg.max_seq,
            NC_ERR_INVALID_ARG, "cache length %d + T=%d exceeds t_max %d", pos0, T, c->t_max);
   NC_CHECK(T == 1 || pos0 == 0 || m->adt != NC_F32, NC_ERR_UNSUPPORTED,
@@ -841,8 +860,8 @@ nc_status nc_decode_step(nc_model* m, const int32_t* tokens, int32_t B, int32_t 
   NC_CHECK(!logits || aligned16(logits), NC_ERR_INVALID_ARG, "logits misaligned");
   NC_CHECK(B >= 1 && B <= c->batch && B <= m->cfg.max_batch, NC_ERR_INVALID_ARG,
            "B=%d out of range", B);
-  NC_CHECK(pos == c->len, NC_ERR_INVALID_ARG, "pos %d must equal the cache length %d", pos,
-           c->len);
+  NC_CHECK(lens_equal(c, B, pos), NC_ERR_INVALID_ARG,
+           "pos %d must equal the cache length of each of the %d sequences", pos, B);
   NC_CHECK(pos >= 1, NC_ERR_INVALID_ARG, "decode needs a prefilled cache (pos >= 1)");
   NC_CHECK(pos + 1 <= c->t_max, NC_ERR_INVALID_ARG, "cache full (t_max %d)", c->t_max);
   cudaStream_t s = static_cast<cudaStream_t>(stream);
@@ -850,8 +869,9 @@ nc_status nc_decode_step(nc_model* m, const int32_t* tokens, int32_t B, int32_t 
   NC_CHECK(fused_ok || m->decode_path != NC_DECODE_PERSISTENT, NC_ERR_UNSUPPORTED,
            "the persistent decode step does not support this shape");
   if (fused_ok && m->decode_path != NC_DECODE_KERNELS) {
-    nc_status st = decode_fused(m, tokens, B, pos, logits, argmax_out, c, s);
-    if (st == NC_OK) c->len = pos + 1;
+    const std::vector<int32_t> pv(B, pos);
+    nc_status st = decode_fused(m, tokens, B, pv.data(), logits, argmax_out, c, s);
+    if (st == NC_OK) set_lens(c, B, pos + 1);
     return st;
   }
   {
@@ -869,8 +889,34 @@ nc_status nc_decode_step(nc_model* m, const int32_t* tokens, int32_t B, int32_t 
     nc::launch_argmax(lg, B, m->cfg.vocab, argmax_out, s);
   }
   st = check_launch();
-  if (st == NC_OK) c->len = pos + 1;
+  if (st == NC_OK) set_lens(c, B, pos + 1);
   return st;
+}
+
+nc_status nc_decode_step_ragged(nc_model* m, const int32_t* tokens, const int32_t* pos, int32_t B,
+                                float* logits, int32_t* argmax_out, nc_kv_cache* c, void* stream) {
+  NC_CHECK(m && c && tokens && pos, NC_ERR_INVALID_ARG, "NULL model, cache, tokens or positions");
+  NC_CHECK(c->model == m, NC_ERR_INVALID_ARG, "cache belongs to another model");
+  NC_CHECK(logits || argmax_out, NC_ERR_INVALID_ARG, "need logits or argmax_out");
+  NC_CHECK(!logits || aligned16(logits), NC_ERR_INVALID_ARG, "logits misaligned");
+  NC_CHECK(B >= 1 && B <= c->batch && B <= m->cfg.max_batch, NC_ERR_INVALID_ARG,
+           "B=%d out of range", B);
+  for (int32_t b = 0; b < B; ++b) {
+    NC_CHECK(pos[b] == c->lens[b], NC_ERR_INVALID_ARG,
+             "pos[%d] = %d must equal that sequence's cache length %d", b, pos[b], c->lens[b]);
+    NC_CHECK(pos[b] >= 1, NC_ERR_INVALID_ARG, "sequence %d: decode needs a prefilled cache", b);
+    NC_CHECK(pos[b] + 1 <= c->t_max, NC_ERR_INVALID_ARG, "sequence %d: cache full (t_max %d)", b,
+             c->t_max);
+  }
+  NC_CHECK(decode_fused_applies(m) && m->decode_path != NC_DECODE_KERNELS, NC_ERR_UNSUPPORTED,
+           "per-sequence positions need the persistent decode step (16-bit model of a supported "
+           "shape)");
+  nc_status st = decode_fused(m, tokens, B, pos, logits, argmax_out, c,
+                              static_cast<cudaStream_t>(stream));
+  if (st != NC_OK) return st;
+  for (int32_t b = 0; b < B; ++b) c->lens[b] = pos[b] + 1;
+  c->len = *std::max_element(c->lens.begin(), c->lens.end());
+  return NC_OK;
 }
 
 nc_status nc_generate_host(nc_model* m, const int32_t* prompt, int32_t B, int32_t T,
@@ -882,7 +928,7 @@ nc_status nc_generate_host(nc_model* m, const int32_t* prompt, int32_t B, int32_
   if (st != NC_OK) return st;
   cudaStream_t s = static_cast<cudaStream_t>(stream);
   NC_CUDA(cudaMemcpyAsync(m->tok_dev, prompt, sizeof(int32_t) * B * T, cudaMemcpyHostToDevice, s));
-  c->len = 0;
+  set_lens(c, c->batch, 0);
   st = nc_prefill_last(m, m->tok_dev, B, T, nullptr, m->gen_dev, c, stream);
   if (st != NC_OK) return st;
   for (int j = 0; j < steps; ++j) {
@@ -919,7 +965,26 @@ nc_status nc_model_set_decode_path(nc_model* m, nc_decode_path path) {
 nc_status nc_kv_cache_set_length(nc_kv_cache* c, int32_t len) {
   NC_CHECK(c, NC_ERR_INVALID_ARG, "cache is NULL");
   NC_CHECK(len >= 0 && len <= c->len, NC_ERR_INVALID_ARG, "length %d outside [0, %d]", len, c->len);
-  c->len = len;
+  for (auto& l : c->lens) l = std::min(l, len);
+  c->len = *std::max_element(c->lens.begin(), c->lens.end());
+  return NC_OK;
+}
+
+nc_status nc_kv_cache_set_lengths(nc_kv_cache* c, const int32_t* lens, int32_t n) {
+  NC_CHECK(c && lens, NC_ERR_INVALID_ARG, "NULL cache or lengths");
+  NC_CHECK(n >= 1 && n <= c->batch, NC_ERR_INVALID_ARG, "n=%d outside [1, %d]", n, c->batch);
+  for (int32_t b = 0; b < n; ++b)
+    NC_CHECK(lens[b] >= 0 && lens[b] <= c->lens[b], NC_ERR_INVALID_ARG,
+             "sequence %d: length %d outside [0, %d]", b, lens[b], c->lens[b]);
+  for (int32_t b = 0; b < n; ++b) c->lens[b] = lens[b];
+  c->len = *std::max_element(c->lens.begin(), c->lens.end());
+  return NC_OK;
+}
+
+nc_status nc_kv_cache_lengths(const nc_kv_cache* c, int32_t* lens, int32_t n) {
+  NC_CHECK(c && lens, NC_ERR_INVALID_ARG, "NULL cache or output");
+  NC_CHECK(n >= 1 && n <= c->batch, NC_ERR_INVALID_ARG, "n=%d outside [1, %d]", n, c->batch);
+  for (int32_t b = 0; b < n; ++b) lens[b] = c->lens[b];
   return NC_OK;
 }
 

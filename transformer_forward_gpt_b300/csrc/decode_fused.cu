@@ -170,39 +170,65 @@ __host__ __device__ __forceinline__ int owner_of(int total, int f, int P) {
   return total < P ? f : (int)((unsigned)((f + 1) * P - 1) / (unsigned)total);
 }
 
-// Attention work: tiles of kKeys positions over (sequence, KV head) pairs bg. With
-// no more pairs than CTAs, every pair gets its own consecutive block of floor or
-// ceil(P / pairs) CTAs and each CTA one contiguous tile range of one pair (one
-// partial state per CTA); otherwise the flattened (pair, tile) space is shared
-// evenly. attn_work gives CTA c's flattened range [f0, f1) (f = bg * nt + tile);
-// attn_group the CTAs holding tiles of pair bg: c_first, c_first + 1, ... (ns).
-__host__ __device__ __forceinline__ void attn_work(int bhkv, int nt, int c, int P, int& f0,
-                                                   int& f1) {
-  if (bhkv <= P) {
-    const int bg = (int)((unsigned)((c + 1) * bhkv - 1) / (unsigned)P);
-    const int cs = (int)((unsigned)(bg * P) / (unsigned)bhkv);
-    const int ce = (int)((unsigned)((bg + 1) * P) / (unsigned)bhkv);
+// Attention work: tiles of kKeys positions over (sequence, KV head) pairs bg =
+// b * Hkv + g; sequence b attends over positions 0..pos[b], so each of its pairs
+// has tiles_of(b) tiles. Tiles are numbered pair after pair (f). With per-pair
+// CTA blocks every CTA holds one contiguous tile range of one pair (one partial
+// state per CTA); otherwise CTA c holds an even share of all tiles.
+// attn_work gives CTA c's range [f0, f1); attn_group the CTAs holding tiles of
+// pair bg: c_first, c_first + 1, ... (ns of them).
+__host__ __device__ __forceinline__ int tiles_of(const Params& p, int b) {
+  return (p.pos[b] + kKeys) / kKeys;
+}
+__host__ __device__ __forceinline__ int tile0_of(const Params& p, int bg) {
+  const int b = (int)((unsigned)bg / (unsigned)p.Hkv);
+  return p.tile_pre[b] + (bg - b * p.Hkv) * tiles_of(p, b);
+}
+// pair of tile f, and f's index j within the pair
+__device__ __forceinline__ int pair_at(const Params& p, int f, int& j) {
+  int lo = 0, hi = p.B;   // tile_pre[lo] <= f < tile_pre[hi]
+  while (hi - lo > 1) {
+    const int mid = (lo + hi) >> 1;
+    if (p.tile_pre[mid] <= f) lo = mid; else hi = mid;
+  }
+  f -= p.tile_pre[lo];
+  const int nt = tiles_of(p, lo);
+  const int g = (int)((unsigned)f / (unsigned)nt);
+  j = f - g * nt;
+  return lo * p.Hkv + g;
+}
+__host__ __device__ __forceinline__ void attn_work(const Params& p, int c, int P, int& f0, int& f1) {
+  if (p.attn_blocks) {
+    // the pair whose block holds c: pair_c0 increases strictly from 0 to P
+    int lo = 0, hi = p.B * p.Hkv;
+    while (hi - lo > 1) {
+      const int mid = (lo + hi) >> 1;
+      if (p.pair_c0[mid] <= c) lo = mid; else hi = mid;
+    }
+    const int cs = p.pair_c0[lo], ce = p.pair_c0[lo + 1];
+    const int nt = tiles_of(p, (int)((unsigned)lo / (unsigned)p.Hkv));
     int j0, j1;
     share(nt, c - cs, ce - cs, j0, j1);
-    f0 = bg * nt + j0;
-    f1 = bg * nt + j1;
+    const int t0 = tile0_of(p, lo);
+    f0 = t0 + j0;
+    f1 = t0 + j1;
   } else {
-    share(bhkv * nt, c, P, f0, f1);
+    share(p.attn_total, c, P, f0, f1);
   }
 }
-__host__ __device__ __forceinline__ void attn_group(int bhkv, int nt, int bg, int P, int& c_first,
+__host__ __device__ __forceinline__ void attn_group(const Params& p, int bg, int P, int& c_first,
                                                     int& ns) {
-  if (bhkv <= P) {
-    c_first = (int)((unsigned)(bg * P) / (unsigned)bhkv);
-    const int n = (int)((unsigned)((bg + 1) * P) / (unsigned)bhkv) - c_first;
+  const int nt = tiles_of(p, (int)((unsigned)bg / (unsigned)p.Hkv));
+  if (p.attn_blocks) {
+    c_first = p.pair_c0[bg];
+    const int n = p.pair_c0[bg + 1] - c_first;
     ns = n < nt ? n : nt;
   } else {
-    const int total = bhkv * nt;
-    c_first = owner_of(total, bg * nt, P);
-    ns = owner_of(total, bg * nt + nt - 1, P) - c_first + 1;
+    const int t0 = tile0_of(p, bg);
+    c_first = owner_of(p.attn_total, t0, P);
+    ns = owner_of(p.attn_total, t0 + nt - 1, P) - c_first + 1;
   }
 }
-__host__ __device__ __forceinline__ int attn_tiles_of(int pos) { return (pos + kKeys) / kKeys; }
 
 // ------------------------------------------------------------------- state
 // A position in the ring of stages; every role keeps its own copy.
@@ -458,16 +484,18 @@ __device__ void produce_gemv(const Params& p, Ring& r, const Gemv& g, uint64_t p
 
 __device__ void produce_attn(const Params& p, Ring& r, const CUtensorMap* tk, const CUtensorMap* tv,
                              int l, uint64_t pol, bool& ok) {
-  const int nt = attn_tiles_of(p.pos);
   int f0, f1;
-  attn_work(p.B * p.Hkv, nt, blockIdx.x, gridDim.x, f0, f1);
-  int bg = (int)((unsigned)f0 / (unsigned)nt), j = f0 - bg * nt;
+  attn_work(p, blockIdx.x, gridDim.x, f0, f1);
+  int j = 0;
+  int bg = f0 < f1 ? pair_at(p, f0, j) : 0;
+  int nt = tiles_of(p, (int)((unsigned)bg / (unsigned)p.Hkv));
   for (int f = f0; f < f1 && ok; ++f, ++j) {
     if (j == nt) {
       j = 0;
       ++bg;
+      nt = tiles_of(p, (int)((unsigned)bg / (unsigned)p.Hkv));
     }
-    const int b = bg / p.Hkv, g = bg % p.Hkv;
+    const int b = (int)((unsigned)bg / (unsigned)p.Hkv), g = bg - b * p.Hkv;
     const int64_t row =
         (((int64_t)l * p.cache_batch + p.b_off + b) * p.Hkv + g) * p.t_max + kKeys * j;
     if (!bwait(&r.empty[r.stage], r.parity ^ 1u, p)) {
@@ -562,12 +590,11 @@ __device__ void mma_role(const Params& p, const Shared& sh, Ring r, uint32_t tme
   int run = 0;
   uint32_t bphase = 0;
   bool ok = true;
-  const int nt = attn_tiles_of(p.pos);
+  int f0, f1;   // the attention phase's stages belong to the consumers
+  attn_work(p, blockIdx.x, gridDim.x, f0, f1);
   for (int l = 0; l < p.L && ok; ++l) {
     ok = mma_gemv<T16>(p, sh, r, gemv_of(p, l, PH_QKV), tmem_base, run, bphase);
     if (!ok) break;
-    int f0, f1;   // the attention phase's stages belong to the consumers
-    attn_work(p.B * p.Hkv, nt, blockIdx.x, gridDim.x, f0, f1);
     r.skip(f1 - f0);
     ok = mma_gemv<T16>(p, sh, r, gemv_of(p, l, PH_O), tmem_base, run, bphase) &&
          mma_gemv<T16>(p, sh, r, gemv_of(p, l, PH_FC), tmem_base, run, bphase) &&
@@ -618,7 +645,6 @@ __device__ void stage_b(const Params& p, const Shared& sh, const Gemv& g, const 
     const int tok = tid >> 3, j = tid & 7;
     const bool tok_ok = tok < p.B;
     const int G = p.H / p.Hkv;
-    const int nt = attn_tiles_of(p.pos);
     uint8_t* dst = sh.act + bchunk_off(tok, j);
     for (int s = 0; s < rg.nslots; ++s) {
       const int c = rg.chunk(s, g.nch);
@@ -629,7 +655,7 @@ __device__ void stage_b(const Params& p, const Shared& sh, const Gemv& g, const 
       if (tok_ok) {
         const int bg = tok * p.Hkv + h / G;
         int c_first, ns;
-        attn_group(p.B * p.Hkv, nt, bg, gridDim.x, c_first, ns);
+        attn_group(p, bg, gridDim.x, c_first, ns);
         const float* rec = static_cast<const float*>(g.act) +
                            (int64_t)bg * p.attn_slots * p.rec_stride + (h % G) * kRecHead;
         for (int s0 = 0; s0 < ns; s0 += 8) {
@@ -878,22 +904,24 @@ __device__ bool consume_attn(const Params& p, Shared& sh, int l, int k) {
   const int tid = threadIdx.x - 64;
   const int gq = lane >> 2, tq = lane & 3;
   Ring& r = sh.ring;
-  const int nt = attn_tiles_of(p.pos);
   int f0, f1;
-  attn_work(p.B * p.Hkv, nt, blockIdx.x, gridDim.x, f0, f1);
+  attn_work(p, blockIdx.x, gridDim.x, f0, f1);
   const int G = p.H / p.Hkv;
   const int qd = p.H * kHd, kvd = p.Hkv * kHd;
   const float* acc_l = p.qkv_acc + (int64_t)(l & 1) * kMaxTok * p.nqkv_pad;
   const float* ss_l = p.ss + (2 * l) * kMaxTok;
-  const int len = p.pos + 1;
-  const int last_tile = nt - 1;
-  const int rp = p.pos - kKeys * last_tile;   // row of pos in the last tile
   bool ok = true;
   int f = f0;
-  int bg = (int)((unsigned)f0 / (unsigned)nt), j0 = f0 - bg * nt;
+  int j0 = 0;
+  int bg = f0 < f1 ? pair_at(p, f0, j0) : 0;
   while (f < f1) {
-    const int j1 = min(nt, j0 + (f1 - f));
     const int b = (int)((unsigned)bg / (unsigned)p.Hkv), g = bg - b * p.Hkv;
+    const int pos = p.pos[b];
+    const int nt = tiles_of(p, b);
+    const int len = pos + 1;
+    const int last_tile = nt - 1;
+    const int rp = pos - kKeys * last_tile;   // row of pos in the last tile
+    const int j1 = min(nt, j0 + (f1 - f));
     const float ssb = __ldcg(ss_l + b);   // used after the q/k/v loads are issued
     const float* accb = acc_l + (int64_t)b * p.nqkv_pad;
     // ---- Q tile of the group's query heads (rows >= G zero) and, in the CTA that
@@ -903,8 +931,8 @@ __device__ bool consume_attn(const Params& p, Shared& sh, int l, int k) {
     {
       const int nrow = (has_last && warp < 2) ? 3 : 2;
       float av[3][4];
-      const float* cs = p.cos_tab + (int64_t)p.pos * (kHd / 2);
-      const float* sn = p.sin_tab + (int64_t)p.pos * (kHd / 2);
+      const float* cs = p.cos_tab + (int64_t)pos * (kHd / 2);
+      const float* sn = p.sin_tab + (int64_t)pos * (kHd / 2);
       float cv[2], sv[2];
 #pragma unroll
       for (int jj = 0; jj < 2; ++jj) {
@@ -951,7 +979,7 @@ __device__ bool consume_attn(const Params& p, Shared& sh, int l, int k) {
           for (int jj = 0; jj < 4; ++jj) st16<T16>(sh.sq, warp + 8 * rr, lane + 32 * jj, o[jj]);
         } else {
           const int64_t crow =
-              (((int64_t)l * p.cache_batch + p.b_off + b) * p.Hkv + g) * p.t_max + p.pos;
+              (((int64_t)l * p.cache_batch + p.b_off + b) * p.Hkv + g) * p.t_max + pos;
           T16* dstc = static_cast<T16*>(is_v ? p.v_cache : p.k_cache) + crow * kHd;
 #pragma unroll
           for (int jj = 0; jj < 4; ++jj) {
@@ -969,11 +997,15 @@ __device__ bool consume_attn(const Params& p, Shared& sh, int l, int k) {
     float o[16][4];
 #pragma unroll
     for (int i = 0; i < 16; ++i) o[i][0] = o[i][1] = o[i][2] = o[i][3] = 0.f;
-    // tiles j0.. are dealt round-robin to the warps; a warp waits only for its own
-    for (int j = j0 + warp; j < j1; j += kCons) {
+    // Every ring stage belongs to one warp (stage index mod 8), which takes the
+    // tiles landing there in order. A warp thus waits on each of its stages'
+    // fills one after another and can never reach a fill two ahead of the
+    // producer, where the barrier's parity would match an older, completed fill.
+    for (int j = j0; j < j1; ++j) {
       int st_i;
       uint32_t par;
       r.ahead(j - j0, st_i, par);
+      if (st_i % kCons != warp) continue;
       ok = ok && __all_sync(0xffffffffu, bwait(&r.full[st_i], par, p));
       uint8_t* st = r.base + (size_t)st_i * kStage;
       if (ok) {
@@ -1028,7 +1060,7 @@ __device__ bool consume_attn(const Params& p, Shared& sh, int l, int k) {
     // partial record of this CTA for (b, g): per head [m, l, -, -, o[128]]; the
     // O projection's staging combines the records of all CTAs of the pair
     int c_first, n_slots;
-    attn_group(p.B * p.Hkv, nt, bg, gridDim.x, c_first, n_slots);
+    attn_group(p, bg, gridDim.x, c_first, n_slots);
     const int slot = blockIdx.x - c_first;
     float* rec = p.attn_part + ((int64_t)bg * p.attn_slots + slot) * p.rec_stride;
     float* const mall = reinterpret_cast<float*>(sh.act);
@@ -1445,13 +1477,29 @@ bool supported(int d, int H, int Hkv, int F, int hd, int V, int P) {
   return st >= 4;
 }
 
-// Largest number of partial-state slots any (sequence, KV head) gets.
-int attn_slots_needed(int B, int Hkv, int pos, int P) {
-  const int nt = attn_tiles_of(pos);
+int plan_attention(Params& p, int P) {
+  const int pairs = p.B * p.Hkv;
+  int64_t total = 0;
+  for (int b = 0; b < p.B; ++b) {
+    if (total >= (int64_t(1) << 31)) return -1;
+    p.tile_pre[b] = (int)total;
+    total += (int64_t)tiles_of(p, b) * p.Hkv;
+  }
+  if (total * (P + 1) >= (int64_t(1) << 31)) return -1;
+  p.tile_pre[p.B] = (int)total;
+  p.attn_total = (int)total;
+  p.attn_blocks = (pairs <= P && P <= kMaxAttnBlocks) ? 1 : 0;
+  if (p.attn_blocks) {
+    // every pair one CTA, the other P - pairs CTAs in proportion to its tiles
+    for (int bg = 0; bg <= pairs; ++bg) {
+      const int64_t t0 = bg == pairs ? total : tile0_of(p, bg);
+      p.pair_c0[bg] = (unsigned short)(bg + (int64_t)(P - pairs) * t0 / total);
+    }
+  }
   int best = 1;
-  for (int bg = 0; bg < B * Hkv; ++bg) {
+  for (int bg = 0; bg < pairs; ++bg) {
     int c_first, ns;
-    attn_group(B * Hkv, nt, bg, P, c_first, ns);
+    attn_group(p, bg, P, c_first, ns);
     best = std::max(best, ns);
   }
   return best;
@@ -1475,9 +1523,8 @@ static nc_status launch_t(const CUtensorMap& tk, const CUtensorMap& tv, Params p
 
 nc_status launch_step(const CUtensorMap& tk, const CUtensorMap& tv, Params p, bool half,
                       nc_dtype wdt, int sms, cudaStream_t s) {
-  if ((int64_t)p.B * p.Hkv * attn_tiles_of(p.pos) * (sms + 1) >= (int64_t(1) << 31)) {
-    set_last_error("decode step: attention work of %d sequences at position %d is too large", p.B,
-                   p.pos);
+  if ((int64_t)p.attn_total * (sms + 1) >= (int64_t(1) << 31)) {
+    set_last_error("decode step: attention work of %d sequences is too large", p.B);
     return NC_ERR_UNSUPPORTED;
   }
   const int act = (int)round_up(std::max(b_slots_needed(p.d, p.H, p.F, p.nqkv_pad, p.vpad, sms) *

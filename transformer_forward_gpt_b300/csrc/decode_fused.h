@@ -31,8 +31,19 @@ struct PackSrc {
   const void* lm;
 };
 
+// Attention work of a launch is cut into tiles of 32 positions per (sequence,
+// KV head) pair. With no more pairs than CTAs, pair bg owns the CTA block
+// [pair_c0[bg], pair_c0[bg + 1]) and spreads its tiles over it; otherwise the
+// tiles of all pairs, concatenated, are shared evenly.
+constexpr int kMaxAttnBlocks = 256;
+
 struct Params {
-  int B, b_off, pos, cache_batch, t_max;
+  int B, b_off, cache_batch, t_max;
+  int pos[kMaxTok];           // position of each sequence's new token (its cache length)
+  int tile_pre[kMaxTok + 1];  // attention tiles of the pairs of sequences 0..b-1 (all KV heads)
+  int attn_total;             // attention tiles of all pairs
+  int attn_blocks;            // 1: per-pair CTA blocks (pair_c0); 0: tiles shared evenly
+  unsigned short pair_c0[kMaxAttnBlocks + 1];
   int L, d, H, Hkv, F, V, vpad, nqkv, nqkv_pad;
   int stages, act_bytes, attn_slots;
   int rec_stride;             // floats per partial record: G heads x [m, l, -, -, o[128]]
@@ -70,7 +81,10 @@ int64_t packed_bytes(int N, int K);
 // Whether the persistent step has a configuration for this shape on P SMs.
 bool supported(int d, int H, int Hkv, int F, int hd, int V, int P);
 nc_status pack_weights(const PackSrc& src, bool half, uint8_t* out, cudaStream_t s);
-int attn_slots_needed(int B, int Hkv, int pos, int P);
+// Fills p.attn_total, p.attn_blocks and p.pair_c0 from p.pos, p.B, p.Hkv for
+// P CTAs; returns the largest number of CTAs that share one pair's tiles (the
+// partial states to merge), or -1 if the work is too large for 32-bit indices.
+int plan_attention(Params& p, int P);
 // TMA view of a KV array (all layers) as [rows, 128] 16-bit values.
 bool make_cache_map(CUtensorMap* map, void* base, uint64_t rows, bool half);
 // Grid barriers one launch passes (its arrivals are that times the grid size).
