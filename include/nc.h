@@ -236,6 +236,35 @@ NC_API nc_status nc_kv_cache_set_length(nc_kv_cache* c, int32_t len);
 NC_API nc_status nc_kv_cache_set_lengths(nc_kv_cache* c, const int32_t* lens, int32_t n);
 NC_API nc_status nc_kv_cache_lengths(const nc_kv_cache* c, int32_t* lens, int32_t n);
 
+/* One decode step that also draws each sequence's next token (Microgpt summary,
+ * section 推理（生成）, items 1-2: the next token is drawn from the predicted
+ * distribution, the logits divided by a temperature first). As nc_decode_step
+ * for tokens, B, pos and the cache, then next_out[b] (dev int32 [B], may alias
+ * tokens) = the smallest index k whose cumulative probability under
+ * softmax(logits[b] / temperature) exceeds u[b] (dev float [B], the caller's
+ * uniforms in [0, 1); values outside are clamped) -- the inverse CDF, so a run is
+ * reproducible from its inputs. temperature <= 0 gives the greedy index (lowest
+ * on ties) and u may be NULL. The draw happens inside the step: every SM keeps
+ * the logits of its whole vocabulary row groups in tensor memory, merges its
+ * softmax partials with the others' and the SM whose share of the cumulative
+ * distribution holds u scans its rows, so the logits are never written unless
+ * `logits` (dev fp32 [B, V], may be NULL) asks for them. Sums are fp32: where u
+ * lies within rounding of a cumulative boundary the neighbouring index may be
+ * drawn. Persistent path only (NC_ERR_UNSUPPORTED otherwise, or for a
+ * vocabulary above 6 * 128 rows per SM). */
+NC_API nc_status nc_decode_step_sample(nc_model* m, const int32_t* tokens, int32_t B, int32_t pos,
+                                       float temperature, const float* u, int32_t* next_out,
+                                       float* logits, nc_kv_cache* c, void* stream);
+
+/* nc_generate_host with sampling: prompt and out_tokens as there; u (HOST float
+ * [steps + 1, B]) holds the uniforms, row 0 for the token after the prompt
+ * (drawn from the prefill's last logits by the nc_op_sample kernel), row j + 1
+ * for decode step j (nc_decode_step_sample). temperature <= 0: greedy, u may be
+ * NULL. */
+NC_API nc_status nc_generate_host_sample(nc_model* m, const int32_t* prompt, int32_t B, int32_t T,
+                                         int32_t steps, float temperature, const float* u,
+                                         int32_t* out_tokens, nc_kv_cache* c, void* stream);
+
 /* One decode step with a position per sequence (jxzklqfsx.com, KV-cache
  * paragraph; CSDN nanochat article, Engine paragraph): sequence b's token
  * tokens[b] (dev int32 [B]) sits at position pos[b] (HOST int32 [B]), which must

@@ -27,6 +27,7 @@ EXPORTS = (
     "nc_op_attention_decode_noalloc", "nc_model_set_decode_path", "nc_decode_trace",
     "nc_decode_trace_entries", "nc_op_sample", "nc_prefill_continue",
     "nc_decode_step_ragged", "nc_kv_cache_set_lengths", "nc_kv_cache_lengths",
+    "nc_decode_step_sample", "nc_generate_host_sample",
 )
 
 KERNEL_KINDS = ("embed", "norm", "qkv", "attn_prefill", "attn_decode", "oproj", "fc", "proj",
@@ -102,6 +103,8 @@ def load(path: str = LIB_PATH):
         "nc_decode_trace": (C.c_int, [vp, vp, i32]),
         "nc_decode_trace_entries": (i32, [C.POINTER(NcConfig)]),
         "nc_decode_step_ragged": (C.c_int, [vp, vp, C.POINTER(i32), i32, vp, vp, vp, vp]),
+        "nc_decode_step_sample": (C.c_int, [vp, vp, i32, i32, C.c_float, vp, vp, vp, vp, vp]),
+        "nc_generate_host_sample": (C.c_int, [vp, vp, i32, i32, i32, C.c_float, vp, vp, vp, vp]),
         "nc_kv_cache_set_lengths": (C.c_int, [vp, C.POINTER(i32), i32]),
         "nc_kv_cache_lengths": (C.c_int, [vp, C.POINTER(i32), i32]),
     }
@@ -295,6 +298,22 @@ def nc_decode_step_ragged(model, tokens, pos, B, logits, argmax_out, cache, stre
     arr = (C.c_int32 * B)(*[int(x) for x in pos])
     _check(load().nc_decode_step_ragged(model, _ptr(tokens), arr, B, _ptr(logits), _ptr(argmax_out),
                                         cache, _stream(stream)), "nc_decode_step_ragged")
+
+
+def nc_decode_step_sample(model, tokens, B, pos, temperature, u, next_out, logits, cache,
+                          stream=None):
+    _check(load().nc_decode_step_sample(model, _ptr(tokens), B, pos, float(temperature), _ptr(u),
+                                        _ptr(next_out), _ptr(logits), cache, _stream(stream)),
+           "nc_decode_step_sample")
+
+
+def nc_generate_host_sample(model, prompt, B, T, steps, temperature, u, out_tokens, cache,
+                            stream=None):
+    """prompt: pinned/host int32 [B, T]; u: host float32 [steps + 1, B] (or None when greedy);
+    out_tokens: host int32 [steps + 1, B]."""
+    _check(load().nc_generate_host_sample(model, _ptr(prompt), B, T, steps, float(temperature),
+                                          _ptr(u), _ptr(out_tokens), cache, _stream(stream)),
+           "nc_generate_host_sample")
 
 
 def nc_kv_cache_set_lengths(cache, lens):

@@ -121,6 +121,7 @@ struct nc_model {
   float* logits_tmp = nullptr;  // [max_batch, V]
   int32_t* tok_dev = nullptr;   // [Mmax]
   int32_t* gen_dev = nullptr;   // [max_seq + 1, max_batch] generated tokens
+  float* gen_u = nullptr;       // [max_seq + 1, max_batch] uniforms of a sampled generation
   float* attn_scratch = nullptr;
   size_t attn_scratch_bytes = 0;
   nc::TcModel* tc = nullptr;    // tensor-core state (16-bit models)
@@ -138,6 +139,7 @@ struct nc_model {
   unsigned long long* d_amkey = nullptr;
   unsigned int* d_amcnt = nullptr;
   unsigned long long* d_bar = nullptr;
+  float4* d_lm_part = nullptr;  // per-CTA softmax partials of the sampling mode
   float* d_part = nullptr;      // partial softmax states (grown on demand)
   size_t d_part_bytes = 0;
   unsigned long long bar_base = 0;
@@ -360,6 +362,7 @@ nc_status nc_model_create(const nc_config* cfg, const nc_weights* w, nc_model** 
                o_xnl = carve((size_t)cfg->max_batch * d * es),
                o_lt = carve((size_t)cfg->max_batch * cfg->vocab * 4), o_tok = carve(Mmax * 4),
                o_gen = carve(((size_t)cfg->max_seq + 1) * cfg->max_batch * 4),
+               o_genu = carve(((size_t)cfg->max_seq + 1) * cfg->max_batch * 4),
                o_as = carve(m->attn_scratch_bytes);
   m->ws_bytes = off;
   if (cudaMalloc(&m->ws, m->ws_bytes) != cudaSuccess) {
@@ -379,6 +382,7 @@ nc_status nc_model_create(const nc_config* cfg, const nc_weights* w, nc_model** 
   m->logits_tmp = reinterpret_cast<float*>(base + o_lt);
   m->tok_dev = reinterpret_cast<int32_t*>(base + o_tok);
   m->gen_dev = reinterpret_cast<int32_t*>(base + o_gen);
+  m->gen_u = reinterpret_cast<float*>(base + o_genu);
   m->attn_scratch = reinterpret_cast<float*>(base + o_as);
 
   if (m->adt != NC_F32) {
@@ -670,7 +674,8 @@ nc_status decode_fused_init(nc_model* m, cudaStream_t s) {
   const size_t o_qkv = carve((size_t)2 * K * m->dlay.nqkv_pad * 4),
                o_h = carve((size_t)K * c.d_mlp * 4), o_ss = carve((size_t)2 * c.n_layer * K * 4),
                o_xnf = carve((size_t)m->dlay.xn_img_bytes),
-               o_key = carve((size_t)K * 8), o_amc = carve((size_t)K * 4), o_bar = carve(8);
+               o_key = carve((size_t)K * 8), o_amc = carve((size_t)K * 4), o_bar = carve(8),
+               o_lmp = carve((size_t)nc::dec::kMaxAttnBlocks * K * 16);
   if (cudaMalloc(&m->dws, off) != cudaSuccess) {
     cudaGetLastError();
     m->dws = nullptr;
@@ -686,6 +691,7 @@ nc_status decode_fused_init(nc_model* m, cudaStream_t s) {
   m->d_amkey = reinterpret_cast<unsigned long long*>(b + o_key);
   m->d_amcnt = reinterpret_cast<unsigned int*>(b + o_amc);
   m->d_bar = reinterpret_cast<unsigned long long*>(b + o_bar);
+  m->d_lm_part = reinterpret_cast<float4*>(b + o_lmp);
   m->bar_base = 0;
   uint8_t* pack = nullptr;
   if (cudaMalloc(&pack, (size_t)m->dlay.total_bytes) != cudaSuccess) {
@@ -707,10 +713,19 @@ nc_status decode_fused_init(nc_model* m, cudaStream_t s) {
   return NC_OK;
 }
 
+// Sampling of the persistent step: off (greedy index from the logits in memory),
+// or drawn inside the step from whole vocabulary row groups kept on chip.
+struct StepSample {
+  bool on = false;
+  float temperature = 0.f;   // <= 0: greedy index
+  const float* u = nullptr;  // dev [B]
+};
+
 // One persistent decode step for B sequences; sequence b's new token sits at
 // position pos[b] (host array), which is also its cache length.
 nc_status decode_fused(nc_model* m, const int32_t* tokens, int32_t B, const int32_t* pos,
-                       float* logits, int32_t* argmax_out, nc_kv_cache* c, cudaStream_t s) {
+                       float* logits, int32_t* argmax_out, nc_kv_cache* c, cudaStream_t s,
+                       const StepSample& smp = StepSample()) {
   nc_status st = decode_fused_init(m, s);
   if (st != NC_OK) return st;
   const nc_config& cfg = m->cfg;
@@ -763,6 +778,13 @@ nc_status decode_fused(nc_model* m, const int32_t* tokens, int32_t B, const int3
     p.ss = m->d_ss;
     p.xn_img = m->d_xnf;
     p.logits = (logits ? logits : m->logits_tmp) + (size_t)b0 * cfg.vocab;
+    p.sample = smp.on ? 1 : 0;
+    if (smp.on) {
+      p.logits = logits ? logits + (size_t)b0 * cfg.vocab : nullptr;   // never written if NULL
+      p.temp_k = smp.temperature > 0.f ? (float)(1.4426950408889634 / smp.temperature) : 0.f;
+      p.u = smp.u ? smp.u + b0 : nullptr;
+      p.lm_part = m->d_lm_part;
+    }
     p.argmax_key = m->d_amkey;
     p.argmax_count = m->d_amcnt;
     p.bar_counter = m->d_bar;
@@ -891,6 +913,74 @@ nc_status nc_decode_step(nc_model* m, const int32_t* tokens, int32_t B, int32_t 
   st = check_launch();
   if (st == NC_OK) set_lens(c, B, pos + 1);
   return st;
+}
+
+nc_status nc_decode_step_sample(nc_model* m, const int32_t* tokens, int32_t B, int32_t pos,
+                                float temperature, const float* u, int32_t* next_out,
+                                float* logits, nc_kv_cache* c, void* stream) {
+  NC_CHECK(m && c && tokens && next_out, NC_ERR_INVALID_ARG, "NULL model, cache, tokens or next_out");
+  NC_CHECK(c->model == m, NC_ERR_INVALID_ARG, "cache belongs to another model");
+  NC_CHECK(!(temperature > 0.f) || u, NC_ERR_INVALID_ARG, "sampling at temperature %g needs u",
+           (double)temperature);
+  NC_CHECK(!logits || aligned16(logits), NC_ERR_INVALID_ARG, "logits misaligned");
+  NC_CHECK(B >= 1 && B <= c->batch && B <= m->cfg.max_batch, NC_ERR_INVALID_ARG,
+           "B=%d out of range", B);
+  NC_CHECK(lens_equal(c, B, pos), NC_ERR_INVALID_ARG,
+           "pos %d must equal the cache length of each of the %d sequences", pos, B);
+  NC_CHECK(pos >= 1, NC_ERR_INVALID_ARG, "decode needs a prefilled cache (pos >= 1)");
+  NC_CHECK(pos + 1 <= c->t_max, NC_ERR_INVALID_ARG, "cache full (t_max %d)", c->t_max);
+  NC_CHECK(decode_fused_applies(m) && m->decode_path != NC_DECODE_KERNELS, NC_ERR_UNSUPPORTED,
+           "sampling inside the step needs the persistent decode step (16-bit model of a "
+           "supported shape)");
+  nc_status st = decode_fused_init(m, static_cast<cudaStream_t>(stream));
+  if (st != NC_OK) return st;
+  const int groups = (m->dlay.vpad + 127) / 128;
+  NC_CHECK(m->sms <= nc::dec::kMaxAttnBlocks &&
+               (groups + m->sms - 1) / m->sms <= nc::dec::kMaxResidentGroups,
+           NC_ERR_UNSUPPORTED, "vocabulary of %d too large to keep on chip for the draw",
+           m->cfg.vocab);
+  StepSample smp;
+  smp.on = true;
+  smp.temperature = temperature;
+  smp.u = u;
+  const std::vector<int32_t> pv(B, pos);
+  st = decode_fused(m, tokens, B, pv.data(), logits, next_out, c, static_cast<cudaStream_t>(stream),
+                    smp);
+  if (st == NC_OK) set_lens(c, B, pos + 1);
+  return st;
+}
+
+nc_status nc_generate_host_sample(nc_model* m, const int32_t* prompt, int32_t B, int32_t T,
+                                  int32_t steps, float temperature, const float* u,
+                                  int32_t* out_tokens, nc_kv_cache* c, void* stream) {
+  NC_CHECK(m && c && prompt && out_tokens, NC_ERR_INVALID_ARG, "NULL argument");
+  NC_CHECK(!(temperature > 0.f) || u, NC_ERR_INVALID_ARG, "sampling needs u");
+  NC_CHECK(steps >= 0 && T + steps <= c->t_max && steps + 1 <= m->cfg.max_seq,
+           NC_ERR_INVALID_ARG, "T + steps exceeds the cache (t_max %d)", c->t_max);
+  nc_status st = check_prefill_args(m, m->tok_dev, B, T, c);
+  if (st != NC_OK) return st;
+  cudaStream_t s = static_cast<cudaStream_t>(stream);
+  NC_CUDA(cudaMemcpyAsync(m->tok_dev, prompt, sizeof(int32_t) * B * T, cudaMemcpyHostToDevice, s));
+  if (temperature > 0.f)
+    NC_CUDA(cudaMemcpyAsync(m->gen_u, u, sizeof(float) * B * (steps + 1), cudaMemcpyHostToDevice,
+                            s));
+  set_lens(c, c->batch, 0);
+  st = nc_prefill_last(m, m->tok_dev, B, T, m->logits_tmp, nullptr, c, stream);
+  if (st != NC_OK) return st;
+  {
+    ProfScope ps(m, NC_K_ARGMAX, s);
+    nc::launch_sample(m->logits_tmp, B, m->cfg.vocab, temperature, m->gen_u, m->gen_dev, s);
+  }
+  for (int j = 0; j < steps; ++j) {
+    st = nc_decode_step_sample(m, m->gen_dev + (size_t)j * B, B, T + j, temperature,
+                               m->gen_u + (size_t)(j + 1) * B, m->gen_dev + (size_t)(j + 1) * B,
+                               nullptr, c, stream);
+    if (st != NC_OK) return st;
+  }
+  NC_CUDA(cudaMemcpyAsync(out_tokens, m->gen_dev, sizeof(int32_t) * B * (steps + 1),
+                          cudaMemcpyDeviceToHost, s));
+  NC_CUDA(cudaStreamSynchronize(s));
+  return NC_OK;
 }
 
 nc_status nc_decode_step_ragged(nc_model* m, const int32_t* tokens, const int32_t* pos, int32_t B,

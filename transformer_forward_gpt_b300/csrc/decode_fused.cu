@@ -73,7 +73,11 @@ constexpr int kRecHead = 4 + kHd;           // floats per head of a partial reco
 // lies in [2^-37, 2^-3.6], far inside fp32, and no maximum has to be found first.
 constexpr float kScoreRef = 20.f;
 constexpr int kMergeBytes = kCons * (16 * kMergeStride + 32) * 4;
-constexpr int kTmemCols = 2 * kTok;         // two accumulators
+// Tensor memory: two alternating accumulators, then (sampling mode) one per
+// vocabulary row group of the LM head that the CTA keeps until the draw.
+constexpr int kTmemResident = 2 * kTok;
+constexpr int kTmemCols = 256;
+static_assert(kTmemResident + kMaxResidentGroups * kTok <= kTmemCols, "TMEM columns");
 
 enum Phase : int { PH_QKV = 0, PH_ATTN = 1, PH_O = 2, PH_FC = 3, PH_PROJ = 4 };
 // Activation sources of a projection: fp32 x (+ sum of squares), fp32 FC sums
@@ -373,6 +377,7 @@ struct Gemv {
   int act_ld;          // row pitch (elements) of an fp32 source
   const float* ss_in;  // ACT_H32: sums of squares giving the per-token scale
   float* ss_out;       // ACT_X32: sums of squares of x accumulated here (or null)
+  int whole;           // 1: CTAs take whole row groups (LM head, sampling mode)
 };
 
 __device__ __forceinline__ Gemv gemv_of(const Params& p, int l, int ph) {
@@ -440,6 +445,7 @@ __device__ __forceinline__ Gemv gemv_lm(const Params& p) {
   g.n_valid = p.V;
   g.act_kind = ACT_IMG;
   g.act = p.xn_img;
+  g.whole = p.sample;
   return g;
 }
 
@@ -460,7 +466,14 @@ struct Range {
 };
 __device__ __forceinline__ Range range_of(const Gemv& g) {
   Range r;
-  share(g.groups * g.nch, blockIdx.x, gridDim.x, r.u0, r.u1);
+  if (g.whole) {
+    int g0, g1;
+    share(g.groups, blockIdx.x, gridDim.x, g0, g1);
+    r.u0 = g0 * g.nch;
+    r.u1 = g1 * g.nch;
+  } else {
+    share(g.groups * g.nch, blockIdx.x, gridDim.x, r.u0, r.u1);
+  }
   r.all = r.u1 - r.u0 >= g.nch;
   r.nslots = r.all ? g.nch : r.u1 - r.u0;
   r.g0 = (int)((unsigned)r.u0 / (unsigned)g.nch);
@@ -557,14 +570,16 @@ __device__ bool mma_gemv(const Params& p, const Shared& sh, Ring& r, const Gemv&
   tc_fence_after();
   constexpr uint32_t kIdesc = idesc_f32acc(Fmt16<T16>::code, kUnitRows, kTok);
   const uint32_t act = smem_u32(sh.act);
-  // runs: one per row group of the range; slots in range order (or by chunk)
-  int u = rg.u0, kp = rg.c0, sl = 0;
+  // runs: one per row group of the range; slots in range order (or by chunk).
+  // Whole-group ranges (sampling mode) give run r of the phase its own
+  // accumulator, kept until the draw.
+  int u = rg.u0, kp = rg.c0, sl = 0, rr = 0;
   while (u < rg.u1) {
     const int n = min(g.nch - kp, rg.u1 - u);
     const int a = run & 1;
     if (!bwait(&sh.acc_empty[a], ((run >> 1) & 1) ^ 1u, p)) return false;
     tc_fence_after();
-    const uint32_t d = tmem_base + a * kTok;
+    const uint32_t d = g.whole ? tmem_base + kTmemResident + (rr++) * kTok : tmem_base + a * kTok;
     for (int i = 0; i < n; ++i, ++sl) {
       if (!bwait(&r.full[r.stage], r.parity, p)) return false;
       tc_fence_after();
@@ -1228,6 +1243,245 @@ __device__ void phase_argmax(const Params& p) {
   }
 }
 
+// ------------------------------------------------------- sampling mode
+// Running softmax state of one token over the vocabulary rows a thread has seen
+// (log2 domain: w = 2^((l - m) k), k = log2(e) / temperature) and its greedy best.
+struct TokStat {
+  float m, s, bv;
+  int bi;
+};
+__device__ __forceinline__ TokStat stat_merge(TokStat a, const TokStat& b, float k) {
+  const float M = fmaxf(a.m, b.m);
+  if (M == -INFINITY) {
+    a.s = 0.f;
+  } else {
+    a.s = a.s * ex2_approx((a.m - M) * k) + b.s * ex2_approx((b.m - M) * k);
+  }
+  a.m = M;
+  if (b.bv > a.bv || (b.bv == a.bv && b.bi < a.bi)) {
+    a.bv = b.bv;
+    a.bi = b.bi;
+  }
+  return a;
+}
+
+// LM head of the sampling mode. The CTA's whole row groups were multiplied into
+// their own accumulators; each thread reads its row (vocabulary index f) for 16
+// tokens from each of them, writes the logits if asked, and folds them into its
+// per-token state. The CTA's states are then merged through shared memory into
+// one partial per token in p.lm_part[blockIdx.x]. The accumulators stay in
+// tensor memory for the draw.
+template <class T16>
+__device__ bool consume_lm_sample(const Params& p, Shared& sh, const Gemv& g, int k,
+                                  uint32_t tmem_base, int& run) {
+  const Range rg = range_of(g);
+  const int warp = threadIdx.x / 32, lane = threadIdx.x % 32;
+  const int quarter = warp % 4, half = (warp - 2) / 4;
+  const int tid = threadIdx.x - 64;
+  const float kt = p.temp_k;
+  TokStat st[16];
+#pragma unroll
+  for (int i = 0; i < 16; ++i) st[i] = TokStat{-INFINITY, 0.f, -INFINITY, 0x7fffffff};
+  bool ok = true;
+  if (rg.u0 < rg.u1) {
+    trace_mark(p, k, 3);
+    stage_b<T16>(p, sh, g, rg);
+    trace_mark(p, k, 0);
+    int grp = rg.g0, rr = 0;
+    for (int u = rg.u0; u < rg.u1; u += g.nch, ++grp, ++rr) {
+      const int a = run & 1;
+      float v[16];
+#pragma unroll
+      for (int i = 0; i < 16; ++i) v[i] = 0.f;
+      ok = ok && __all_sync(0xffffffffu, bwait(&sh.acc_full[a], (run >> 1) & 1, p));
+      if (ok) {
+        tc_fence_after();
+        tmem_ld16_sync(tmem_base + ((uint32_t)(quarter * 32) << 16) + kTmemResident + rr * kTok +
+                           half * 16,
+                       v);
+      }
+      tc_fence_before();
+      __syncwarp();
+      if (lane == 0) mbar_arrive(&sh.acc_empty[a]);
+      ++run;
+      const int f = grp * kUnitRows + quarter * 32 + lane;
+      if (!ok || f >= g.n_valid) continue;
+#pragma unroll
+      for (int i = 0; i < 16; ++i) {
+        const int tok = half * 16 + i;
+        if (p.logits && tok < p.B) p.logits[(int64_t)tok * p.V + f] = v[i];
+        if (v[i] > st[i].bv) {   // rows come in increasing f: ties keep the lower index
+          st[i].bv = v[i];
+          st[i].bi = f;
+        }
+        if (kt > 0.f) {
+          if (v[i] > st[i].m) {
+            st[i].s = st[i].s * ex2_approx((st[i].m - v[i]) * kt) + 1.f;
+            st[i].m = v[i];
+          } else {
+            st[i].s += ex2_approx((v[i] - st[i].m) * kt);
+          }
+        }
+      }
+    }
+    trace_mark(p, k, 1);
+  }
+  // Every accumulator has been read, so no MMA reads the B chunks any more: the
+  // area holds the states, [token][quarter][lane] (token t from the warps of half t / 16).
+  bar_consumers();
+  TokStat* ts = reinterpret_cast<TokStat*>(sh.act);
+#pragma unroll
+  for (int i = 0; i < 16; ++i) ts[((half * 16 + i) * 4 + quarter) * 32 + lane] = st[i];
+  bar_consumers();
+  {
+    // thread: token t = tid / 8 merges 16 of the token's 128 states, then 8 lanes merge
+    const int t = tid >> 3, part = tid & 7;
+    TokStat a{-INFINITY, 0.f, -INFINITY, 0x7fffffff};
+    for (int e = part * 16; e < part * 16 + 16; ++e) a = stat_merge(a, ts[t * 128 + e], kt);
+#pragma unroll
+    for (int o = 1; o < 8; o <<= 1) {
+      TokStat b;
+      b.m = __shfl_xor_sync(0xffffffffu, a.m, o);
+      b.s = __shfl_xor_sync(0xffffffffu, a.s, o);
+      b.bv = __shfl_xor_sync(0xffffffffu, a.bv, o);
+      b.bi = __shfl_xor_sync(0xffffffffu, a.bi, o);
+      a = stat_merge(a, b, kt);
+    }
+    if (part == 0)
+      p.lm_part[blockIdx.x * kMaxTok + t] = make_float4(a.m, a.s, a.bv, __int_as_float(a.bi));
+  }
+  trace_mark(p, k, 2);
+  return ok;
+}
+
+// The draw. Every CTA merges the partials of all CTAs for each token in the same
+// fixed order: the maximum M, then the weights W_c = s_c 2^((m_c - M) k) summed
+// one after another, so that CTA c's interval [C_c, C_c + W_c) of [0, Z) is the
+// same value in every CTA and the intervals tile [0, Z) exactly. The CTA whose
+// interval holds u Z scans its rows of the token in vocabulary order: the
+// smallest index whose cumulative weight passes u Z (the last row of nonzero
+// weight if rounding leaves it beyond the CTA's rows). Greedy: the best value
+// over all partials, lowest index on ties, written by CTA 0.
+__device__ void phase_sample(const Params& p, Shared& sh, uint32_t tmem_base) {
+  const int tid = threadIdx.x - 64;
+  const int warp = threadIdx.x / 32, lane = threadIdx.x % 32;
+  const int quarter = warp % 4;
+  const float kt = p.temp_k;
+  int* own = reinterpret_cast<int*>(sh.act);                  // [kMaxTok]
+  float* resid = reinterpret_cast<float*>(own + kMaxTok);     // [kMaxTok]
+  float* mt = resid + kMaxTok;                                // [kMaxTok]
+  float* tot = mt + kMaxTok;                                  // [kMaxResidentGroups][4]
+  int* found = reinterpret_cast<int*>(tot + 4 * kMaxResidentGroups);   // [1]
+  int* lastnz = found + 1;                                    // [4]
+  if (tid < kMaxTok) own[tid] = 0;
+  bar_consumers();
+  if (tid < p.B) {
+    const int t = tid;
+    float M = -INFINITY, bv = -INFINITY;
+    int bi = 0x7fffffff;
+    for (int c = 0; c < (int)gridDim.x; ++c) {
+      const float4 e = __ldcg(p.lm_part + c * kMaxTok + t);
+      M = fmaxf(M, e.x);
+      const int ei = __float_as_int(e.w);
+      if (e.z > bv || (e.z == bv && ei < bi)) {
+        bv = e.z;
+        bi = ei;
+      }
+    }
+    if (!(kt > 0.f)) {
+      if (blockIdx.x == 0 && p.argmax_out) p.argmax_out[t] = bi;
+    } else {
+      float Z = 0.f, C = 0.f, W = 0.f;
+      int last = -1;
+      for (int c = 0; c < (int)gridDim.x; ++c) {
+        const float4 e = __ldcg(p.lm_part + c * kMaxTok + t);
+        const float w = e.x == -INFINITY ? 0.f : e.y * ex2_approx((e.x - M) * kt);
+        if (c == (int)blockIdx.x) {
+          C = Z;
+          W = w;
+        }
+        if (w > 0.f) last = c;
+        Z = Z + w;
+      }
+      const float uu = fminf(fmaxf(__ldcg(p.u + t), 0.f), 0x1.fffffep-1f);
+      const float tg = uu * Z;
+      int o = (W > 0.f && C <= tg && tg < C + W) ? 1 : 0;
+      if (!o && tg >= Z && (int)blockIdx.x == last) o = 2;   // rounded past the total
+      own[t] = o;
+      resid[t] = o == 2 ? INFINITY : tg - C;
+      mt[t] = M;
+    }
+  }
+  bar_consumers();
+  if (!(kt > 0.f) || !p.argmax_out) return;
+  int g0, g1;
+  share(p.vpad / kUnitRows, blockIdx.x, gridDim.x, g0, g1);
+  const int ng = g1 - g0;
+  for (int t = 0; t < p.B; ++t) {
+    if (!own[t]) continue;   // the same decision in every thread (shared memory)
+    // warps 2..5 hold the four lane quarters (rows q * 32 + lane of every group)
+    const bool scan = warp < 6;
+    float incl[kMaxResidentGroups], w[kMaxResidentGroups];
+    if (scan) {
+      int lnz = -1;
+#pragma unroll
+      for (int r = 0; r < kMaxResidentGroups; ++r) {
+        incl[r] = 0.f;
+        w[r] = 0.f;
+        if (r >= ng) continue;
+        uint32_t raw;
+        asm volatile("tcgen05.ld.sync.aligned.32x32b.x1.b32 {%0}, [%1];\n"
+                     "tcgen05.wait::ld.sync.aligned;\n"
+                     : "=r"(raw)
+                     : "r"(tmem_base + ((uint32_t)(quarter * 32) << 16) + kTmemResident + r * kTok + t)
+                     : "memory");
+        const int f = (g0 + r) * kUnitRows + quarter * 32 + lane;
+        w[r] = f < p.V ? ex2_approx((__uint_as_float(raw) - mt[t]) * kt) : 0.f;
+        float x = w[r];
+#pragma unroll
+        for (int o = 1; o < 32; o <<= 1) {
+          const float y = __shfl_up_sync(0xffffffffu, x, o);
+          if (lane >= o) x += y;
+        }
+        incl[r] = x;
+        if (lane == 31) tot[r * 4 + quarter] = x;
+        if (w[r] > 0.f) lnz = f;
+      }
+#pragma unroll
+      for (int o = 16; o > 0; o >>= 1) lnz = max(lnz, __shfl_xor_sync(0xffffffffu, lnz, o));
+      if (lane == 0) lastnz[quarter] = lnz;
+    }
+    if (tid == 0) *found = 0;
+    bar_consumers();
+    if (scan) {
+      // base of (group r, quarter q): the totals before it, summed in one fixed order
+      const float rs = resid[t];
+      float base = 0.f;
+#pragma unroll
+      for (int r = 0; r < kMaxResidentGroups; ++r) {
+        if (r >= ng) break;
+#pragma unroll
+        for (int q = 0; q < 4; ++q) {
+          if (q == quarter) {
+            const float prev = __shfl_up_sync(0xffffffffu, incl[r], 1);
+            const float lo = lane == 0 ? base : base + prev;
+            const float hi = base + incl[r];
+            if (w[r] > 0.f && lo <= rs && rs < hi) {
+              p.argmax_out[t] = (g0 + r) * kUnitRows + quarter * 32 + lane;
+              *found = 1;
+            }
+          }
+          base = base + tot[r * 4 + q];
+        }
+      }
+    }
+    bar_consumers();
+    if (tid == 0 && !*found)
+      p.argmax_out[t] = max(max(lastnz[0], lastnz[1]), max(lastnz[2], lastnz[3]));
+    bar_consumers();
+  }
+}
+
 template <class T16, class TW>
 __device__ void consumers(const Params& p, Shared& sh, uint32_t tmem_base) {
   int nbar = 0, run = 0;
@@ -1236,7 +1490,7 @@ __device__ void consumers(const Params& p, Shared& sh, uint32_t tmem_base) {
   phase_embed<TW>(p);
   zero_f32(p.qkv_acc, p.B * p.nqkv_pad);
   zero_f32(p.ss, 2 * p.L * kMaxTok);
-  zero_f32(p.logits, p.B * p.V);
+  if (!p.sample) zero_f32(p.logits, p.B * p.V);   // sampling mode stores whole rows
   {
     const int tid = threadIdx.x - 64;
     const int64_t gt = (int64_t)blockIdx.x * 256 + tid;
@@ -1262,9 +1516,13 @@ __device__ void consumers(const Params& p, Shared& sh, uint32_t tmem_base) {
   }
   phase_final_norm<T16>(p);
   if (!grid_barrier(p, sh, ++nbar)) return;
-  const bool lm = consume_gemv<T16>(p, sh, gemv_lm(p), nbar + 1, tmem_base, run);
+  const bool lm = p.sample ? consume_lm_sample<T16>(p, sh, gemv_lm(p), nbar + 1, tmem_base, run)
+                          : consume_gemv<T16>(p, sh, gemv_lm(p), nbar + 1, tmem_base, run);
   if (!grid_barrier(p, sh, ++nbar) || !lm) return;
-  phase_argmax(p);
+  if (p.sample)
+    phase_sample(p, sh, tmem_base);
+  else
+    phase_argmax(p);
   if (p.trace && blockIdx.x == 0 && threadIdx.x == 64) p.trace[2 * nbar + 1] = global_timer_ns();
 }
 
@@ -1435,7 +1693,7 @@ Layout layout_of(int L, int d, int H, int Hkv, int F, int V) {
 
 // Shared memory of a launch: the ring, the B-chunk / merge area, the Q tile,
 // the new K/V row, barriers and flags. The B area holds the most chunks any
-// CTA's range of any projection needs.
+// CTA's range of any projection needs, and at least every chunk of d_model.
 static int b_slots_needed(int d, int H, int F, int nqkv_pad, int vpad, int P) {
   auto need = [&](int64_t units, int nch) {
     const int64_t per = (units + P - 1) / P;
@@ -1446,7 +1704,10 @@ static int b_slots_needed(int d, int H, int F, int nqkv_pad, int vpad, int P) {
   n = std::max(n, need((int64_t)(d / kUnitRows) * (qd / kUnitCols), qd / kUnitCols));
   n = std::max(n, need((int64_t)(F / kUnitRows) * (d / kUnitCols), d / kUnitCols));
   n = std::max(n, need((int64_t)(d / kUnitRows) * (F / kUnitCols), F / kUnitCols));
-  n = std::max(n, need((int64_t)(vpad / kUnitRows) * (d / kUnitCols), d / kUnitCols));
+  // the LM head: every chunk of d (a CTA that owns whole row groups in sampling
+  // mode stages all of them, whatever the vocabulary)
+  n = std::max(n, d / kUnitCols);
+  (void)vpad;
   return n;
 }
 

@@ -62,7 +62,15 @@ struct Params {
   float* hacc;                // [kMaxTok][F]
   float* ss;                  // [2 L][kMaxTok]
   void* xn_img;               // final norm, B-chunk image [d/64][kMaxTok][128 B]
-  float* logits;              // [B][V]
+  float* logits;              // [B][V]; in sampling mode optional (NULL: never written)
+  // Sampling mode: the LM head gives every CTA whole row groups of the vocabulary,
+  // keeps their logits in tensor memory, and the step ends with a draw from
+  // softmax(logits / temperature) (the greedy index when temp_k is 0) instead of
+  // a pass over the logits in memory.
+  int sample;
+  float temp_k;               // log2(e) / temperature, 0 for the greedy index
+  const float* u;             // [B] uniforms in [0, 1), one per sequence
+  float4* lm_part;            // [gridDim][kMaxTok] per CTA: max, exp-sum, best value, best index
   float* attn_part;           // partial softmax states
   unsigned long long* argmax_key;   // [kMaxTok]
   unsigned int* argmax_count;       // [kMaxTok]
@@ -87,6 +95,8 @@ nc_status pack_weights(const PackSrc& src, bool half, uint8_t* out, cudaStream_t
 int plan_attention(Params& p, int P);
 // TMA view of a KV array (all layers) as [rows, 128] 16-bit values.
 bool make_cache_map(CUtensorMap* map, void* base, uint64_t rows, bool half);
+// Vocabulary row groups a CTA may keep in tensor memory in sampling mode.
+constexpr int kMaxResidentGroups = 6;
 // Grid barriers one launch passes (its arrivals are that times the grid size).
 inline int barriers_per_step(int L) { return 5 * L + 3; }
 // CTAs whose barrier arrival and exit times a trace records.
