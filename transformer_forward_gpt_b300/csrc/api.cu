@@ -140,8 +140,8 @@ struct nc_model {
   unsigned int* d_amcnt = nullptr;
   unsigned long long* d_bar = nullptr;
   float4* d_lm_part = nullptr;  // per-CTA softmax partials of the sampling mode
-  float* d_part = nullptr;      // partial softmax states (grown on demand)
-  size_t d_part_bytes = 0;
+  float* d_att_num = nullptr;   // attention numerators [2][kMaxTok][H * head_dim]
+  float* d_att_den = nullptr;   // and denominators [2][kMaxTok][H]
   unsigned long long bar_base = 0;
   unsigned long long* dec_trace = nullptr;   // caller's buffer (nc_decode_trace)
   int32_t dec_trace_cap = 0;
@@ -262,7 +262,6 @@ void nc_model_destroy(nc_model* m) {
   cudaFree(m->wcopy);
   cudaFree(m->dpack);
   cudaFree(m->dws);
-  cudaFree(m->d_part);
   cudaFree(m->ws);
   cudaFree(m->cos_tab);
   cudaFree(m->sin_tab);
@@ -675,7 +674,9 @@ nc_status decode_fused_init(nc_model* m, cudaStream_t s) {
                o_h = carve((size_t)K * c.d_mlp * 4), o_ss = carve((size_t)2 * c.n_layer * K * 4),
                o_xnf = carve((size_t)m->dlay.xn_img_bytes),
                o_key = carve((size_t)K * 8), o_amc = carve((size_t)K * 4), o_bar = carve(8),
-               o_lmp = carve((size_t)nc::dec::kMaxAttnBlocks * K * 16);
+               o_lmp = carve((size_t)nc::dec::kMaxAttnBlocks * K * 16),
+               o_an = carve((size_t)2 * K * c.n_head * c.head_dim * 4),
+               o_ad = carve((size_t)2 * K * c.n_head * 4);
   if (cudaMalloc(&m->dws, off) != cudaSuccess) {
     cudaGetLastError();
     m->dws = nullptr;
@@ -692,6 +693,8 @@ nc_status decode_fused_init(nc_model* m, cudaStream_t s) {
   m->d_amcnt = reinterpret_cast<unsigned int*>(b + o_amc);
   m->d_bar = reinterpret_cast<unsigned long long*>(b + o_bar);
   m->d_lm_part = reinterpret_cast<float4*>(b + o_lmp);
+  m->d_att_num = reinterpret_cast<float*>(b + o_an);
+  m->d_att_den = reinterpret_cast<float*>(b + o_ad);
   m->bar_base = 0;
   uint8_t* pack = nullptr;
   if (cudaMalloc(&pack, (size_t)m->dlay.total_bytes) != cudaSuccess) {
@@ -737,7 +740,6 @@ nc_status decode_fused(nc_model* m, const int32_t* tokens, int32_t B, const int3
              NC_ERR_CUDA, "TMA descriptors of the KV cache could not be built");
     c->maps = true;
   }
-  const int G = cfg.n_head / cfg.n_kv_head;
   ProfScope ps(m, NC_K_DECODE_STEP, s);
   for (int b0 = 0; b0 < B; b0 += nc::dec::kMaxTok) {
     const int Bc = std::min(nc::dec::kMaxTok, B - b0);
@@ -756,8 +758,8 @@ nc_status decode_fused(nc_model* m, const int32_t* tokens, int32_t B, const int3
     p.vpad = m->dlay.vpad;
     p.nqkv = m->dlay.nqkv;
     p.nqkv_pad = m->dlay.nqkv_pad;
-    p.attn_slots = nc::dec::plan_attention(p, m->sms);
-    NC_CHECK(p.attn_slots > 0, NC_ERR_UNSUPPORTED, "decode attention work too large");
+    NC_CHECK(nc::dec::plan_attention(p, m->sms) > 0, NC_ERR_UNSUPPORTED,
+             "decode attention work too large");
     p.eps = cfg.rms_eps;
     p.scale_log2 = (float)(1.4426950408889634 / sqrt((double)cfg.head_dim));
     p.layer_bytes = m->dlay.layer_bytes;
@@ -795,23 +797,8 @@ nc_status decode_fused(nc_model* m, const int32_t* tokens, int32_t B, const int3
     p.trace = (b0 == 0 && m->dec_trace && m->dec_trace_cap >= nc::dec::trace_entries(cfg.n_layer))
                   ? m->dec_trace
                   : nullptr;
-    p.rec_stride = G * (cfg.head_dim + 4);
-    const size_t part = (size_t)Bc * cfg.n_kv_head * p.attn_slots * p.rec_stride * 4;
-    if (part > m->d_part_bytes) {
-      // grows on the first calls of a larger shape only (the free waits for the device)
-      cudaFree(m->d_part);
-      m->d_part = nullptr;
-      m->d_part_bytes = 0;
-      const size_t want = part * 2;
-      if (cudaMalloc(&m->d_part, want) != cudaSuccess) {
-        cudaGetLastError();
-        m->d_part = nullptr;
-        set_err("decode attention scratch of %zu bytes failed", want);
-        return NC_ERR_OOM;
-      }
-      m->d_part_bytes = want;
-    }
-    p.attn_part = m->d_part;
+    p.att_num = m->d_att_num;
+    p.att_den = m->d_att_den;
     st = nc::dec::launch_step(c->tmk, c->tmv, p, f16, cfg.dtype, m->sms, s);
     if (st != NC_OK) return st;
     m->bar_base += (unsigned long long)nc::dec::barriers_per_step(cfg.n_layer) * m->sms;

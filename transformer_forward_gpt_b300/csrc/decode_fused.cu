@@ -66,7 +66,6 @@ constexpr int kChunkBytes = kTok * 128;     // one 64-column chunk of kTok token
 constexpr int kHd = 128;
 constexpr int kKeys = 32;                   // positions per K/V tile
 constexpr int kMergeStride = 132;           // floats per row of a warp's merge area
-constexpr int kRecHead = 4 + kHd;           // floats per head of a partial record: m, l, -, -, o
 // Partial softmax states are combined with weights 2^(m - kScoreRef). QK
 // RMS-norm makes |q.k| <= head_dim, so a score (log2 units, scale 1/sqrt(hd)
 // folded in) is at most sqrt(128) * log2(e) = 16.3 in magnitude: every weight
@@ -81,8 +80,8 @@ static_assert(kTmemResident + kMaxResidentGroups * kTok <= kTmemCols, "TMEM colu
 
 enum Phase : int { PH_QKV = 0, PH_ATTN = 1, PH_O = 2, PH_FC = 3, PH_PROJ = 4 };
 // Activation sources of a projection: fp32 x (+ sum of squares), fp32 FC sums
-// (scaled, ReLU^2), the attention phase's partial softmax records (merged while
-// staged), or an image already in the B-chunk layout (final norm).
+// (scaled, ReLU^2), the attention phase's summed numerators and denominators
+// (divided while staged), or an image already in the B-chunk layout (final norm).
 enum ActKind : int { ACT_X32 = 0, ACT_H32 = 1, ACT_ATT = 2, ACT_IMG = 3 };
 
 // ---------------------------------------------------------------- primitives
@@ -169,18 +168,13 @@ __host__ __device__ __forceinline__ void share(int total, int c, int P, int& lo,
     hi = (int)((unsigned)(total * (c + 1)) / (unsigned)P);
   }
 }
-// The CTA whose share contains item f.
-__host__ __device__ __forceinline__ int owner_of(int total, int f, int P) {
-  return total < P ? f : (int)((unsigned)((f + 1) * P - 1) / (unsigned)total);
-}
 
 // Attention work: tiles of kKeys positions over (sequence, KV head) pairs bg =
 // b * Hkv + g; sequence b attends over positions 0..pos[b], so each of its pairs
 // has tiles_of(b) tiles. Tiles are numbered pair after pair (f). With per-pair
 // CTA blocks every CTA holds one contiguous tile range of one pair (one partial
 // state per CTA); otherwise CTA c holds an even share of all tiles.
-// attn_work gives CTA c's range [f0, f1); attn_group the CTAs holding tiles of
-// pair bg: c_first, c_first + 1, ... (ns of them).
+// attn_work gives CTA c's range [f0, f1).
 __host__ __device__ __forceinline__ int tiles_of(const Params& p, int b) {
   return (p.pos[b] + kKeys) / kKeys;
 }
@@ -218,19 +212,6 @@ __host__ __device__ __forceinline__ void attn_work(const Params& p, int c, int P
     f1 = t0 + j1;
   } else {
     share(p.attn_total, c, P, f0, f1);
-  }
-}
-__host__ __device__ __forceinline__ void attn_group(const Params& p, int bg, int P, int& c_first,
-                                                    int& ns) {
-  const int nt = tiles_of(p, (int)((unsigned)bg / (unsigned)p.Hkv));
-  if (p.attn_blocks) {
-    c_first = p.pair_c0[bg];
-    const int n = p.pair_c0[bg + 1] - c_first;
-    ns = n < nt ? n : nt;
-  } else {
-    const int t0 = tile0_of(p, bg);
-    c_first = owner_of(p.attn_total, t0, P);
-    ns = owner_of(p.attn_total, t0 + nt - 1, P) - c_first + 1;
   }
 }
 
@@ -377,6 +358,7 @@ struct Gemv {
   int act_ld;          // row pitch (elements) of an fp32 source
   const float* ss_in;  // ACT_H32: sums of squares giving the per-token scale
   float* ss_out;       // ACT_X32: sums of squares of x accumulated here (or null)
+  const float* den;    // ACT_ATT: softmax denominators [kMaxTok][H]
   int whole;           // 1: CTAs take whole row groups (LM head, sampling mode)
 };
 
@@ -405,7 +387,9 @@ __device__ __forceinline__ Gemv gemv_of(const Params& p, int l, int ph) {
       g.ldo = d;
       g.n_valid = d;
       g.act_kind = ACT_ATT;
-      g.act = p.attn_part;
+      g.act = p.att_num + (int64_t)(l & 1) * kMaxTok * qd;
+      g.act_ld = qd;
+      g.den = p.att_den + (l & 1) * kMaxTok * p.H;
       break;
     case PH_FC:
       g.w = lw + p.off_fc;
@@ -655,59 +639,39 @@ __device__ void stage_b(const Params& p, const Shared& sh, const Gemv& g, const 
       }
     }
   } else if (g.act_kind == ACT_ATT) {
-    // token tok, 16-byte chunk j of every slot: the (sequence, KV head) pair's
-    // partial softmax states, combined against kScoreRef in one pass
+    // token tok, 16-byte chunk j of every slot: eight values of head c / 2's
+    // attention output (values 64 (c % 2) + 8 j ..), the summed numerators over
+    // the head's summed denominator; the loads of up to eight slots in flight
     const int tok = tid >> 3, j = tid & 7;
     const bool tok_ok = tok < p.B;
-    const int G = p.H / p.Hkv;
+    const float* src = static_cast<const float*>(g.act) + (int64_t)tok * g.act_ld + 8 * j;
+    const float* den = g.den + tok * p.H;
     uint8_t* dst = sh.act + bchunk_off(tok, j);
-    for (int s = 0; s < rg.nslots; ++s) {
-      const int c = rg.chunk(s, g.nch);
-      const int h = c >> 1, half = c & 1;   // head and 64-value half of the chunk
-      float L = 0.f, O[8];
+    for (int s0 = 0; s0 < rg.nslots; s0 += 8) {
+      float4 a[8], b[8];
+      float dn[8];
 #pragma unroll
-      for (int e = 0; e < 8; ++e) O[e] = 0.f;
-      if (tok_ok) {
-        const int bg = tok * p.Hkv + h / G;
-        int c_first, ns;
-        attn_group(p, bg, gridDim.x, c_first, ns);
-        const float* rec = static_cast<const float*>(g.act) +
-                           (int64_t)bg * p.attn_slots * p.rec_stride + (h % G) * kRecHead;
-        for (int s0 = 0; s0 < ns; s0 += 8) {
-          float2 ml[8];
-          float4 oa[8], ob[8];
-#pragma unroll
-          for (int q = 0; q < 8; ++q) {
-            ml[q] = make_float2(-INFINITY, 0.f);
-            oa[q] = ob[q] = make_float4(0.f, 0.f, 0.f, 0.f);
-            if (s0 + q < ns) {
-              const float* r = rec + (int64_t)(s0 + q) * p.rec_stride;
-              ml[q] = __ldcg(reinterpret_cast<const float2*>(r));
-              oa[q] = __ldcg(reinterpret_cast<const float4*>(r + 4 + 64 * half + 8 * j));
-              ob[q] = __ldcg(reinterpret_cast<const float4*>(r + 8 + 64 * half + 8 * j));
-            }
-          }
-#pragma unroll
-          for (int q = 0; q < 8; ++q) {
-            const float w = ex2_approx(ml[q].x - kScoreRef);
-            L = fmaf(w, ml[q].y, L);
-            O[0] = fmaf(w, oa[q].x, O[0]);
-            O[1] = fmaf(w, oa[q].y, O[1]);
-            O[2] = fmaf(w, oa[q].z, O[2]);
-            O[3] = fmaf(w, oa[q].w, O[3]);
-            O[4] = fmaf(w, ob[q].x, O[4]);
-            O[5] = fmaf(w, ob[q].y, O[5]);
-            O[6] = fmaf(w, ob[q].z, O[6]);
-            O[7] = fmaf(w, ob[q].w, O[7]);
-          }
+      for (int q = 0; q < 8; ++q) {
+        const int s = s0 + q;
+        a[q] = b[q] = make_float4(0.f, 0.f, 0.f, 0.f);
+        dn[q] = 1.f;
+        if (s < rg.nslots && tok_ok) {
+          const int c = rg.chunk(s, g.nch);
+          const float* sp = src + c * kUnitCols;
+          a[q] = __ldcg(reinterpret_cast<const float4*>(sp));
+          b[q] = __ldcg(reinterpret_cast<const float4*>(sp + 4));
+          dn[q] = __ldcg(den + (c >> 1));
         }
-        const float inv = 1.f / L;
-#pragma unroll
-        for (int e = 0; e < 8; ++e) O[e] *= inv;
       }
-      *reinterpret_cast<uint4*>(dst + (size_t)s * kChunkBytes) =
-          make_uint4(pack2<T16>(O[0], O[1]), pack2<T16>(O[2], O[3]), pack2<T16>(O[4], O[5]),
-                     pack2<T16>(O[6], O[7]));
+#pragma unroll
+      for (int q = 0; q < 8; ++q) {
+        const int s = s0 + q;
+        if (s >= rg.nslots) continue;
+        const float inv = 1.f / dn[q];
+        *reinterpret_cast<uint4*>(dst + (size_t)s * kChunkBytes) =
+            make_uint4(pack2<T16>(a[q].x * inv, a[q].y * inv), pack2<T16>(a[q].z * inv, a[q].w * inv),
+                       pack2<T16>(b[q].x * inv, b[q].y * inv), pack2<T16>(b[q].z * inv, b[q].w * inv));
+      }
     }
   } else {
     // thread: token tok = tid / 8, 16-byte chunk j = tid % 8 of every slot; the
@@ -1049,71 +1013,57 @@ __device__ bool consume_attn(const Params& p, Shared& sh, int l, int k) {
     }
     r.skip(j1 - j0);
     trace_mark(p, k, 1);
-    // ---- merge the warps' states: row sums over the quad, then through smem
+    // ---- the warps' states against the fixed reference: row sums over the quad,
+    // each row's output and sum scaled by 2^(m - kScoreRef) (0 for a warp without
+    // keys of the row), summed over the warps through shared memory, then added
+    // into the accumulators that all CTAs of the pair share
+    float w_r[2];
 #pragma unroll
     for (int h = 0; h < 2; ++h) {
       l_r[h] += __shfl_xor_sync(0xffffffffu, l_r[h], 1);
       l_r[h] += __shfl_xor_sync(0xffffffffu, l_r[h], 2);
+      w_r[h] = ex2_approx(m_r[h] - kScoreRef);
     }
-    float* mw = reinterpret_cast<float*>(sh.act) + warp * (16 * kMergeStride + 32);
+    constexpr int kWs = 16 * kMergeStride + 32;   // floats per warp's merge area
+    float* mw = reinterpret_cast<float*>(sh.act) + warp * kWs;
     float* ow = mw + 32;
     if (tq == 0) {
-      mw[gq] = m_r[0];
-      mw[gq + 8] = m_r[1];
-      mw[16 + gq] = l_r[0];
-      mw[16 + gq + 8] = l_r[1];
+      mw[16 + gq] = l_r[0] * w_r[0];
+      mw[16 + gq + 8] = l_r[1] * w_r[1];
     }
 #pragma unroll
     for (int i = 0; i < 16; ++i) {
       const int c = i * 8 + 2 * tq;
-      ow[gq * kMergeStride + c] = o[i][0];
-      ow[gq * kMergeStride + c + 1] = o[i][1];
-      ow[(gq + 8) * kMergeStride + c] = o[i][2];
-      ow[(gq + 8) * kMergeStride + c + 1] = o[i][3];
+      *reinterpret_cast<float2*>(ow + gq * kMergeStride + c) =
+          make_float2(o[i][0] * w_r[0], o[i][1] * w_r[0]);
+      *reinterpret_cast<float2*>(ow + (gq + 8) * kMergeStride + c) =
+          make_float2(o[i][2] * w_r[1], o[i][3] * w_r[1]);
     }
     bar_consumers();
-    // partial record of this CTA for (b, g): per head [m, l, -, -, o[128]]; the
-    // O projection's staging combines the records of all CTAs of the pair
-    int c_first, n_slots;
-    attn_group(p, bg, gridDim.x, c_first, n_slots);
-    const int slot = blockIdx.x - c_first;
-    float* rec = p.attn_part + ((int64_t)bg * p.attn_slots + slot) * p.rec_stride;
-    float* const mall = reinterpret_cast<float*>(sh.act);
-    constexpr int kWs = 16 * kMergeStride + 32;   // floats per warp's merge area
-    // one thread per head: the CTA's max M and sum L, and each warp's weight
-    // 2^(m_w - M), which replaces m_w in place (only this thread touches column h)
-    if (tid < G) {
-      const int h = tid;
-      float mwv[kCons];
-      float M = -INFINITY;
+    {
+      const float* const mall = reinterpret_cast<const float*>(sh.act);
+      const int sl = l & 1;
+      float* num = p.att_num + ((int64_t)sl * kMaxTok + b) * qd + g * G * kHd;
+      float* den = p.att_den + (sl * kMaxTok + b) * p.H + g * G;
+      for (int e = tid; e < G * kHd / 4; e += 256) {
+        const int h = e / (kHd / 4), i = (e % (kHd / 4)) * 4;
+        float4 v = make_float4(0.f, 0.f, 0.f, 0.f);
 #pragma unroll
-      for (int w = 0; w < kCons; ++w) {
-        mwv[w] = mall[w * kWs + h];
-        M = fmaxf(M, mwv[w]);
+        for (int w = 0; w < kCons; ++w) {
+          const float4 ov = *reinterpret_cast<const float4*>(mall + w * kWs + 32 + h * kMergeStride + i);
+          v.x += ov.x;
+          v.y += ov.y;
+          v.z += ov.z;
+          v.w += ov.w;
+        }
+        red_add_f32x4(num + h * kHd + i, v);
       }
-      float L = 0.f;
+      if (tid < G) {
+        float L = 0.f;
 #pragma unroll
-      for (int w = 0; w < kCons; ++w) {
-        const float sc = ex2_approx(mwv[w] - M);
-        L = fmaf(sc, mall[w * kWs + 16 + h], L);
-        mall[w * kWs + h] = sc;
+        for (int w = 0; w < kCons; ++w) L += mall[w * kWs + 16 + tid];
+        red_add_f32(den + tid, L);
       }
-      *reinterpret_cast<float2*>(rec + h * kRecHead) = make_float2(M, L);
-    }
-    bar_consumers();
-    for (int e = tid; e < G * kHd / 4; e += 256) {
-      const int h = e / (kHd / 4), i = (e % (kHd / 4)) * 4;
-      float4 v = make_float4(0.f, 0.f, 0.f, 0.f);
-#pragma unroll
-      for (int w = 0; w < kCons; ++w) {
-        const float sc = mall[w * kWs + h];
-        const float* ov = mall + w * kWs + 32 + h * kMergeStride + i;
-        v.x = fmaf(sc, ov[0], v.x);
-        v.y = fmaf(sc, ov[1], v.y);
-        v.z = fmaf(sc, ov[2], v.z);
-        v.w = fmaf(sc, ov[3], v.w);
-      }
-      *reinterpret_cast<float4*>(rec + h * kRecHead + 4 + i) = v;
     }
     trace_mark(p, k, 2);
     bar_consumers();
@@ -1490,6 +1440,8 @@ __device__ void consumers(const Params& p, Shared& sh, uint32_t tmem_base) {
   phase_embed<TW>(p);
   zero_f32(p.qkv_acc, p.B * p.nqkv_pad);
   zero_f32(p.ss, 2 * p.L * kMaxTok);
+  zero_f32(p.att_num, kMaxTok * p.H * kHd);   // layer 0's buffer
+  zero_f32(p.att_den, kMaxTok * p.H);
   if (!p.sample) zero_f32(p.logits, p.B * p.V);   // sampling mode stores whole rows
   {
     const int tid = threadIdx.x - 64;
@@ -1507,6 +1459,12 @@ __device__ void consumers(const Params& p, Shared& sh, uint32_t tmem_base) {
     if (l + 1 < p.L) zero_f32(p.qkv_acc + ((l + 1) & 1) * kMaxTok * p.nqkv_pad, p.B * p.nqkv_pad);
     const bool b = consume_attn<T16>(p, sh, l, nbar + 1);
     if (!grid_barrier(p, sh, ++nbar) || !b) return;
+    if (l + 1 < p.L) {
+      // the next layer's buffer: last read by this layer's predecessor's O phase
+      const int sl = (l + 1) & 1;
+      zero_f32(p.att_num + (int64_t)sl * kMaxTok * p.H * kHd, p.B * p.H * kHd);
+      zero_f32(p.att_den + sl * kMaxTok * p.H, p.B * p.H);
+    }
     const bool c = consume_gemv<T16>(p, sh, gemv_of(p, l, PH_O), nbar + 1, tmem_base, run);
     if (!grid_barrier(p, sh, ++nbar) || !c) return;
     const bool d = consume_gemv<T16>(p, sh, gemv_of(p, l, PH_FC), nbar + 1, tmem_base, run);
@@ -1757,13 +1715,7 @@ int plan_attention(Params& p, int P) {
       p.pair_c0[bg] = (unsigned short)(bg + (int64_t)(P - pairs) * t0 / total);
     }
   }
-  int best = 1;
-  for (int bg = 0; bg < pairs; ++bg) {
-    int c_first, ns;
-    attn_group(p, bg, P, c_first, ns);
-    best = std::max(best, ns);
-  }
-  return best;
+  return 1;
 }
 
 template <class T16, class TW>

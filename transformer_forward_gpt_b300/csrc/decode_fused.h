@@ -45,8 +45,7 @@ struct Params {
   int attn_blocks;            // 1: per-pair CTA blocks (pair_c0); 0: tiles shared evenly
   unsigned short pair_c0[kMaxAttnBlocks + 1];
   int L, d, H, Hkv, F, V, vpad, nqkv, nqkv_pad;
-  int stages, act_bytes, attn_slots;
-  int rec_stride;             // floats per partial record: G heads x [m, l, -, -, o[128]]
+  int stages, act_bytes;
   float eps, scale_log2;
   int64_t layer_bytes, off_o, off_fc, off_proj;
   const int32_t* tokens;      // [B]
@@ -71,7 +70,13 @@ struct Params {
   float temp_k;               // log2(e) / temperature, 0 for the greedy index
   const float* u;             // [B] uniforms in [0, 1), one per sequence
   float4* lm_part;            // [gridDim][kMaxTok] per CTA: max, exp-sum, best value, best index
-  float* attn_part;           // partial softmax states
+  // Attention output of a layer as sums over the CTAs that share a (sequence, KV
+  // head) pair: numerators sum_c 2^(m_c - ref) o_c and denominators
+  // sum_c 2^(m_c - ref) l_c of each CTA's softmax state (max m_c, sum l_c,
+  // unnormalised output o_c) against one fixed reference. Two buffers, by layer
+  // parity; each is zeroed a layer ahead of its use.
+  float* att_num;             // [2][kMaxTok][H * 128]
+  float* att_den;             // [2][kMaxTok][H]
   unsigned long long* argmax_key;   // [kMaxTok]
   unsigned int* argmax_count;       // [kMaxTok]
   unsigned long long* bar_counter;  // grid barrier arrivals (monotonic)
@@ -89,9 +94,8 @@ int64_t packed_bytes(int N, int K);
 // Whether the persistent step has a configuration for this shape on P SMs.
 bool supported(int d, int H, int Hkv, int F, int hd, int V, int P);
 nc_status pack_weights(const PackSrc& src, bool half, uint8_t* out, cudaStream_t s);
-// Fills p.attn_total, p.attn_blocks and p.pair_c0 from p.pos, p.B, p.Hkv for
-// P CTAs; returns the largest number of CTAs that share one pair's tiles (the
-// partial states to merge), or -1 if the work is too large for 32-bit indices.
+// Fills p.tile_pre, p.attn_total, p.attn_blocks and p.pair_c0 from p.pos, p.B,
+// p.Hkv for P CTAs; returns 1, or -1 if the work is too large for 32-bit indices.
 int plan_attention(Params& p, int P);
 // TMA view of a KV array (all layers) as [rows, 128] 16-bit values.
 bool make_cache_map(CUtensorMap* map, void* base, uint64_t rows, bool half);
