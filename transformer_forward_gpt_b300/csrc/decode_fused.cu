@@ -57,7 +57,7 @@ namespace nc {
 namespace dec {
 
 constexpr int kCons = 8;                    // consumer warps (CTA warps 2..9)
-constexpr int kThreads = 32 * (2 + kCons);  // producer, MMA, consumers
+constexpr int kThreads = 32 * (3 + kCons);  // producer, MMA issuer 0, consumers, MMA issuer 1
 constexpr int kStage = 16384;               // bytes of one ring stage
 constexpr int kUnitRows = 128;              // weight rows of one unit (MMA M)
 constexpr int kUnitCols = 64;               // weight columns of one unit (128 bytes)
@@ -72,8 +72,10 @@ constexpr int kMergeStride = 132;           // floats per row of a warp's merge 
 // lies in [2^-37, 2^-3.6], far inside fp32, and no maximum has to be found first.
 constexpr float kScoreRef = 20.f;
 constexpr int kMergeBytes = kCons * (16 * kMergeStride + 32) * 4;
-// Tensor memory: two alternating accumulators, then (sampling mode) one per
-// vocabulary row group of the LM head that the CTA keeps until the draw.
+// Tensor memory: per MMA issuer two alternating accumulators (issuer i, run
+// parity a at column (a + 2 i) kTok); in sampling mode the LM head's row groups
+// that the CTA keeps until the draw take one accumulator each from column
+// kTmemResident on (issuer 1 is idle then, so they may cover its columns).
 constexpr int kTmemResident = 2 * kTok;
 constexpr int kTmemCols = 256;
 static_assert(kTmemResident + kMaxResidentGroups * kTok <= kTmemCols, "TMEM columns");
@@ -306,7 +308,9 @@ __device__ bool grid_barrier(const Params& p, const Shared& sh, int k) {
   bar_consumers();
   const int tid = threadIdx.x - 64;
   if (tid == 0) {
-    bool ok = !aborted(p);
+    // an aborted step is noticed in the wait below (its slow path): a read of the
+    // abort word here would hold up the release by a round trip to L2
+    bool ok = true;
     const bool tr = p.trace && blockIdx.x == 0;
     uint64_t t_arr = 0;
     if (p.trace) t_arr = global_timer_ns();
@@ -433,6 +437,16 @@ __device__ __forceinline__ Gemv gemv_lm(const Params& p) {
   return g;
 }
 
+// The step as one sequence of phases q = 5 l + ph (ph a Phase of layer l), then
+// q = 5 L (final norm) and q = 5 L + 1 (LM head). Every role walks it in one
+// loop with one call site per kind of phase: the kernel's code stays small
+// enough that the phases share their instructions in the instruction cache.
+__device__ __forceinline__ int phase_layer(int q, int& ph) {
+  const int l = (int)((unsigned)q / 5u);
+  ph = q - 5 * l;
+  return l;
+}
+
 // The CTA's unit range of a projection and the B chunk slot of each unit: a
 // range shorter than a row group holds distinct chunks, staged in range order;
 // a longer one needs every chunk, staged in chunk order.
@@ -512,21 +526,19 @@ __device__ void produce_attn(const Params& p, Ring& r, const CUtensorMap* tk, co
 __device__ void producer(const Params& p, Ring r, const CUtensorMap* tk, const CUtensorMap* tv) {
   const uint64_t pol = l2_policy_evict_first();
   bool ok = true;
-  for (int l = 0; l < p.L && ok; ++l) {
-    const int k = 2 + 5 * l;   // grid barrier that ends this layer's QKV phase
-    trace_producer(p, k);
-    produce_gemv(p, r, gemv_of(p, l, PH_QKV), pol, ok);
-    trace_producer(p, k + 1);
-    produce_attn(p, r, tk, tv, l, pol, ok);
-    trace_producer(p, k + 2);
-    produce_gemv(p, r, gemv_of(p, l, PH_O), pol, ok);
-    trace_producer(p, k + 3);
-    produce_gemv(p, r, gemv_of(p, l, PH_FC), pol, ok);
-    trace_producer(p, k + 4);
-    produce_gemv(p, r, gemv_of(p, l, PH_PROJ), pol, ok);
+  // phase q ends at grid barrier q + 2 (barrier 1 ends the embedding); the final
+  // norm streams nothing
+#pragma unroll 1
+  for (int q = 0; q < 5 * p.L + 2 && ok; ++q) {
+    int ph;
+    const int l = phase_layer(q, ph);
+    if (l == p.L && ph == 0) continue;
+    trace_producer(p, q + 2);
+    if (l < p.L && ph == PH_ATTN)
+      produce_attn(p, r, tk, tv, l, pol, ok);
+    else
+      produce_gemv(p, r, l < p.L ? gemv_of(p, l, ph) : gemv_lm(p), pol, ok);
   }
-  trace_producer(p, 5 * p.L + 3);
-  if (ok) produce_gemv(p, r, gemv_lm(p), pol, ok);
   if (!ok) {
     // Let every copy already issued land before the CTA's shared memory goes
     // away: the latest fill of each stage completes its full barrier's phase.
@@ -543,10 +555,17 @@ __device__ void producer(const Params& p, Ring r, const CUtensorMap* tk, const C
 
 // ==================================================================== MMA
 // Issues the MMAs of one projection phase: per row group of the CTA's range one
-// accumulator (alternating between the two), per unit four K = 16 steps.
+// run of units, per unit four K = 16 steps. Two issuer threads share a phase
+// (one tcgen05.mma takes about as long to issue as to run at N = 32, so two
+// issuers nearly double the rate): with an even number of ring stages, issuer i
+// takes the units at ring positions of parity i, so every stage has one issuer,
+// and sums them in its own accumulator of the run. In whole-group mode (sampling)
+// issuer 0 takes every unit into the run's resident accumulator. Both commit
+// every run's accumulator barrier (an issuer without units of the run commits
+// at once).
 template <class T16>
 __device__ bool mma_gemv(const Params& p, const Shared& sh, Ring& r, const Gemv& g,
-                         uint32_t tmem_base, int& run, uint32_t& bphase) {
+                         uint32_t tmem_base, int& run, uint32_t& bphase, int issuer) {
   const Range rg = range_of(g);
   if (rg.u0 >= rg.u1) return true;
   if (!bwait(sh.b_full, bphase & 1u, p)) return false;
@@ -554,26 +573,30 @@ __device__ bool mma_gemv(const Params& p, const Shared& sh, Ring& r, const Gemv&
   tc_fence_after();
   constexpr uint32_t kIdesc = idesc_f32acc(Fmt16<T16>::code, kUnitRows, kTok);
   const uint32_t act = smem_u32(sh.act);
-  // runs: one per row group of the range; slots in range order (or by chunk).
-  // Whole-group ranges (sampling mode) give run r of the phase its own
-  // accumulator, kept until the draw.
+  // runs: one per row group of the range; slots in range order (or by chunk)
   int u = rg.u0, kp = rg.c0, sl = 0, rr = 0;
   while (u < rg.u1) {
     const int n = min(g.nch - kp, rg.u1 - u);
     const int a = run & 1;
     if (!bwait(&sh.acc_empty[a], ((run >> 1) & 1) ^ 1u, p)) return false;
     tc_fence_after();
-    const uint32_t d = g.whole ? tmem_base + kTmemResident + (rr++) * kTok : tmem_base + a * kTok;
+    const uint32_t d = g.whole ? tmem_base + kTmemResident + (rr++) * kTok
+                               : tmem_base + (uint32_t)(a + 2 * issuer) * kTok;
+    int mine = 0;
     for (int i = 0; i < n; ++i, ++sl) {
-      if (!bwait(&r.full[r.stage], r.parity, p)) return false;
-      tc_fence_after();
-      const uint64_t wd = sdesc_kmajor_sw128(smem_u32(r.base + (size_t)r.stage * kStage));
-      const uint64_t bd = sdesc_kmajor_sw128(act + (rg.all ? kp + i : sl) * kChunkBytes);
-      // +32 bytes along K per step: +2 in the descriptor's address field
+      const bool own = g.whole ? issuer == 0 : (r.stage & 1) == issuer;
+      if (own) {
+        if (!bwait(&r.full[r.stage], r.parity, p)) return false;
+        tc_fence_after();
+        const uint64_t wd = sdesc_kmajor_sw128(smem_u32(r.base + (size_t)r.stage * kStage));
+        const uint64_t bd = sdesc_kmajor_sw128(act + (rg.all ? kp + i : sl) * kChunkBytes);
+        // +32 bytes along K per step: +2 in the descriptor's address field
 #pragma unroll
-      for (int k = 0; k < 4; ++k)
-        mma_f16kind_ss(d, wd + 2 * k, bd + 2 * k, kIdesc, (i > 0 || k > 0) ? 1u : 0u);
-      mma_commit(&r.empty[r.stage]);
+        for (int k = 0; k < 4; ++k)
+          mma_f16kind_ss(d, wd + 2 * k, bd + 2 * k, kIdesc, (mine > 0 || k > 0) ? 1u : 0u);
+        mma_commit(&r.empty[r.stage]);
+        ++mine;
+      }
       r.advance();
     }
     mma_commit(&sh.acc_full[a]);
@@ -585,22 +608,24 @@ __device__ bool mma_gemv(const Params& p, const Shared& sh, Ring& r, const Gemv&
 }
 
 template <class T16>
-__device__ void mma_role(const Params& p, const Shared& sh, Ring r, uint32_t tmem_base) {
+__device__ void mma_role(const Params& p, const Shared& sh, Ring r, uint32_t tmem_base, int issuer) {
   int run = 0;
   uint32_t bphase = 0;
   bool ok = true;
   int f0, f1;   // the attention phase's stages belong to the consumers
   attn_work(p, blockIdx.x, gridDim.x, f0, f1);
-  for (int l = 0; l < p.L && ok; ++l) {
-    ok = mma_gemv<T16>(p, sh, r, gemv_of(p, l, PH_QKV), tmem_base, run, bphase);
-    if (!ok) break;
-    r.skip(f1 - f0);
-    ok = mma_gemv<T16>(p, sh, r, gemv_of(p, l, PH_O), tmem_base, run, bphase) &&
-         mma_gemv<T16>(p, sh, r, gemv_of(p, l, PH_FC), tmem_base, run, bphase) &&
-         mma_gemv<T16>(p, sh, r, gemv_of(p, l, PH_PROJ), tmem_base, run, bphase);
+#pragma unroll 1
+  for (int q = 0; q < 5 * p.L + 2 && ok; ++q) {
+    int ph;
+    const int l = phase_layer(q, ph);
+    if (l == p.L && ph == 0) continue;
+    if (l < p.L && ph == PH_ATTN)
+      r.skip(f1 - f0);
+    else
+      ok = mma_gemv<T16>(p, sh, r, l < p.L ? gemv_of(p, l, ph) : gemv_lm(p), tmem_base, run, bphase,
+                         issuer);
   }
-  if (ok) mma_gemv<T16>(p, sh, r, gemv_lm(p), tmem_base, run, bphase);
-  // every MMA issued so far has completed once this commit arrives
+  // every MMA of both issuers has completed once both commits have arrived
   mma_commit(sh.fin);
   const uint64_t t0 = global_timer_ns();
   while (!mbar_try_wait(sh.fin, 0)) {
@@ -751,16 +776,26 @@ __device__ bool consume_gemv(const Params& p, Shared& sh, const Gemv& g, int k, 
   trace_mark(p, k, 0);
   bool ok = true;
   int u = rg.u0, grp = rg.g0, kp = rg.c0;
+  int par = sh.ring.stage & 1;   // ring position parity of the unit u (even ring)
   while (u < rg.u1) {
     const int n = min(g.nch - kp, rg.u1 - u);
     const int a = run & 1;
+    const int n0 = (n + 1 - par) >> 1;   // units of the run at even positions: issuer 0's
+    par = (par + n) & 1;
     float v[16];
 #pragma unroll
     for (int i = 0; i < 16; ++i) v[i] = 0.f;
     ok = ok && __all_sync(0xffffffffu, bwait(&sh.acc_full[a], (run >> 1) & 1, p));
     if (ok) {
       tc_fence_after();
-      tmem_ld16_sync(tmem_base + ((uint32_t)(quarter * 32) << 16) + a * kTok + half * 16, v);
+      const uint32_t t = tmem_base + ((uint32_t)(quarter * 32) << 16) + half * 16;
+      if (n0 > 0) tmem_ld16_sync(t + a * kTok, v);
+      if (n0 < n) {
+        float w[16];
+        tmem_ld16_sync(t + (a + 2) * kTok, w);
+#pragma unroll
+        for (int i = 0; i < 16; ++i) v[i] += w[i];
+      }
     }
     tc_fence_before();
     __syncwarp();
@@ -1091,6 +1126,7 @@ __device__ void phase_embed(const Params& p) {
   }
 }
 
+// a[0, n) = 0 over the consumer threads of all CTAs (a 16-byte aligned)
 __device__ void zero_f32(float* a, int n) {
   const int tid = threadIdx.x - 64;
   const int gt = blockIdx.x * 256 + tid, gs = gridDim.x * 256;
@@ -1452,31 +1488,31 @@ __device__ void consumers(const Params& p, Shared& sh, uint32_t tmem_base) {
     }
   }
   if (!grid_barrier(p, sh, ++nbar)) return;
-  for (int l = 0; l < p.L; ++l) {
-    zero_f32(p.hacc, p.B * p.F);
-    const bool a = consume_gemv<T16>(p, sh, gemv_of(p, l, PH_QKV), nbar + 1, tmem_base, run);
-    if (!grid_barrier(p, sh, ++nbar) || !a) return;
-    if (l + 1 < p.L) zero_f32(p.qkv_acc + ((l + 1) & 1) * kMaxTok * p.nqkv_pad, p.B * p.nqkv_pad);
-    const bool b = consume_attn<T16>(p, sh, l, nbar + 1);
-    if (!grid_barrier(p, sh, ++nbar) || !b) return;
-    if (l + 1 < p.L) {
+#pragma unroll 1
+  for (int q = 0; q < 5 * p.L + 2; ++q) {
+    int ph;
+    const int l = phase_layer(q, ph);
+    bool ok = true;
+    if (l == p.L && ph == 0) {
+      phase_final_norm<T16>(p);
+    } else if (l < p.L && ph == PH_ATTN) {
+      ok = consume_attn<T16>(p, sh, l, nbar + 1);
+    } else if (l == p.L && p.sample) {
+      ok = consume_lm_sample<T16>(p, sh, gemv_lm(p), nbar + 1, tmem_base, run);
+    } else {
+      if (l < p.L && ph == PH_QKV) zero_f32(p.hacc, p.B * p.F);
+      ok = consume_gemv<T16>(p, sh, l < p.L ? gemv_of(p, l, ph) : gemv_lm(p), nbar + 1, tmem_base, run);
+    }
+    if (!grid_barrier(p, sh, ++nbar) || !ok) return;
+    if (l + 1 < p.L && ph == PH_QKV)
+      zero_f32(p.qkv_acc + ((l + 1) & 1) * kMaxTok * p.nqkv_pad, p.B * p.nqkv_pad);
+    if (l + 1 < p.L && ph == PH_ATTN) {
       // the next layer's buffer: last read by this layer's predecessor's O phase
       const int sl = (l + 1) & 1;
       zero_f32(p.att_num + (int64_t)sl * kMaxTok * p.H * kHd, p.B * p.H * kHd);
       zero_f32(p.att_den + sl * kMaxTok * p.H, p.B * p.H);
     }
-    const bool c = consume_gemv<T16>(p, sh, gemv_of(p, l, PH_O), nbar + 1, tmem_base, run);
-    if (!grid_barrier(p, sh, ++nbar) || !c) return;
-    const bool d = consume_gemv<T16>(p, sh, gemv_of(p, l, PH_FC), nbar + 1, tmem_base, run);
-    if (!grid_barrier(p, sh, ++nbar) || !d) return;
-    const bool e = consume_gemv<T16>(p, sh, gemv_of(p, l, PH_PROJ), nbar + 1, tmem_base, run);
-    if (!grid_barrier(p, sh, ++nbar) || !e) return;
   }
-  phase_final_norm<T16>(p);
-  if (!grid_barrier(p, sh, ++nbar)) return;
-  const bool lm = p.sample ? consume_lm_sample<T16>(p, sh, gemv_lm(p), nbar + 1, tmem_base, run)
-                          : consume_gemv<T16>(p, sh, gemv_lm(p), nbar + 1, tmem_base, run);
-  if (!grid_barrier(p, sh, ++nbar) || !lm) return;
   if (p.sample)
     phase_sample(p, sh, tmem_base);
   else
@@ -1525,11 +1561,11 @@ __global__ void __launch_bounds__(kThreads, 1)
       mbar_init(&sh.ring.empty[s], 1);
     }
     for (int a = 0; a < 2; ++a) {
-      mbar_init(&sh.acc_full[a], 1);
+      mbar_init(&sh.acc_full[a], 2);   // one commit per MMA issuer
       mbar_init(&sh.acc_empty[a], kCons);
     }
     mbar_init(sh.b_full, kCons);
-    mbar_init(sh.fin, 1);
+    mbar_init(sh.fin, 2);
     sh.flag[2] = 1;
     fence_mbar_init();
   }
@@ -1548,8 +1584,8 @@ __global__ void __launch_bounds__(kThreads, 1)
       tma_prefetch_desc(&tmV);
       producer(p, sh.ring, &tmK, &tmV);
     }
-  } else if (warp == 1) {
-    if (lane == 0) mma_role<T16>(p, sh, sh.ring, tmem_base);
+  } else if (warp == 1 || warp == 2 + kCons) {
+    if (lane == 0) mma_role<T16>(p, sh, sh.ring, tmem_base, warp == 1 ? 0 : 1);
   } else {
     consumers<T16, TW>(p, sh, tmem_base);
   }
@@ -1674,6 +1710,7 @@ static size_t smem_bytes(int act, int* stages) {
   const int limit = 232448 - 1024;   // dynamic part; static shared memory is small
   int st = (limit - fixed - act) / (kStage + 16);
   if (st > 16) st = 16;
+  st &= ~1;   // even: each stage belongs to one of the two MMA issuers
   *stages = st;
   return (size_t)st * kStage + act + fixed + 16 * st;
 }
