@@ -47,6 +47,7 @@ struct GemmArgs {
   QkvDst qkv;
   uint32_t* status;
   int stream_k;            // 1: CTAs take equal contiguous ranges of (tile, k block)
+  int sk_groups;           // > 1 (stream-K): one group of CTAs per n block, see Sched
 };
 
 // Work schedule shared by the three roles of a CTA: a sequence of segments
@@ -56,16 +57,30 @@ struct GemmArgs {
 //               every CTA does the same number of k blocks; a tile cut between
 //               CTAs is finished by more than one of them (EPI_RESID adds).
 //               Tiles are ordered n block fastest.
+//   grouped stream-K (sk_groups = n blocks = G): CTA c works on n block c % G
+//               and takes share c / G of the (m block, k block) pairs, the same
+//               share in every group; the G CTAs that need one k block of A then
+//               read it at about the same time, so L2 serves it to all but the
+//               first. CTAs past the last full group of G stay idle.
 struct Seg {
   int mb, nb, kb0, kb1, ks;
 };
 struct Sched {
   int64_t pos, end;   // stream-K position / end, or persistent unit / units
   int step;
+  int nbf;            // grouped stream-K: this CTA's n block (else -1)
   bool sk;
   __device__ __forceinline__ void init(const GemmArgs& p) {
     sk = p.stream_k != 0;
-    if (sk) {
+    nbf = -1;
+    if (sk && p.sk_groups > 1) {
+      const int G = p.sk_groups, P = (int)gridDim.x / G, c = (int)blockIdx.x;
+      const int64_t total = (int64_t)p.num_m_blk * p.num_k_blk;
+      nbf = c % G;
+      pos = c < G * P ? total * (c / G) / P : 0;
+      end = c < G * P ? total * (c / G + 1) / P : 0;
+      step = 0;
+    } else if (sk) {
       const int64_t total = (int64_t)p.num_m_blk * p.num_n_blk * p.num_k_blk;
       pos = total * blockIdx.x / gridDim.x;
       end = total * (blockIdx.x + 1) / gridDim.x;
@@ -78,7 +93,14 @@ struct Sched {
   }
   __device__ __forceinline__ bool next(const GemmArgs& p, Seg& g) {
     if (pos >= end) return false;
-    if (sk) {
+    if (sk && nbf >= 0) {
+      g.kb0 = (int)(pos % p.num_k_blk);
+      { const int64_t e = g.kb0 + (end - pos); g.kb1 = (int)(e < p.num_k_blk ? e : p.num_k_blk); }
+      g.nb = nbf;
+      g.mb = (int)(pos / p.num_k_blk);
+      g.ks = 0;
+      pos += g.kb1 - g.kb0;
+    } else if (sk) {
       // tiles n-block fastest: the n tiles of one 128-row block of A follow one
       // another, so that block is read from DRAM once and from L2 after (A of
       // the PROJ projection, 84 MB at d20, does not stay in L2 across a sweep)
@@ -730,6 +752,12 @@ static nc_status proj_impl(TcModel* t, int l, int64_t M, float* x, float* part, 
   args.out_f32 = x;
   args.ldo = d;
   args.stream_k = 1;
+  // A (M x F, 16-bit) larger than about half of L2: group the CTAs by n block
+  // when at most 3% of the SMs would stay idle
+  const int G = args.num_n_blk;
+  if ((int64_t)M * F * 2 > (int64_t)48 << 20 && G > 1 && G <= t->sm_count &&
+      (t->sm_count % G) * 100 <= 3 * t->sm_count)
+    args.sk_groups = G;
   return tile_gemm<EPI_RESID, T16>(a, w.wproj, w.wproj, w.wproj, args, BN, t->sm_count, s);
 }
 
