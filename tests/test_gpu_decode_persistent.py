@@ -78,6 +78,15 @@ def test_long_context_spans_ctas(cuda_device):
     _run(_small(synth.D20_MQA, n_layer=2, vocab=1000), 2, 1000, 3)
 
 
+def test_shares_spanning_two_pairs(cuda_device):
+    """20 sequences x 32 tiles = 640 tiles over the SMs: shares of 4-5 tiles, many
+    of them ending in one (sequence, KV head) pair and starting in the next. Those
+    CTAs prepare and compute both pairs in one round, one tile per warp, and add each
+    pair's sums to its own accumulators; the new k / v rows land in whichever CTA
+    holds a pair's last tile."""
+    _run(_small(synth.D20_MQA, n_layer=2, vocab=512), 20, 1000, 2, seqs=[0, 7, 13, 19])
+
+
 def test_tiles_shared_evenly_over_many_laps(cuda_device):
     """More (sequence, KV head) pairs than CTAs: the tiles of all pairs are shared
     evenly, about 50 per CTA, so the ring of stages turns over many times within

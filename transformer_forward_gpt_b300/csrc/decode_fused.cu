@@ -248,8 +248,8 @@ struct Ring {
 struct Shared {
   Ring ring;
   uint8_t* act;          // B chunks of the projection phases / attention merge area
-  uint8_t* sq;           // Q tile (16 x 128, swizzled)
-  uint16_t* kvnew;       // new K row, new V row (16-bit)
+  uint8_t* sq;           // Q tiles of up to two pairs (16 x 128 each, swizzled)
+  uint16_t* kvnew;       // new K row, new V row of up to two pairs (16-bit)
   uint64_t* acc_full;    // [2] accumulator ready (tcgen05.commit)
   uint64_t* acc_empty;   // [2] accumulator read by the consumers (8 arrivals)
   uint64_t* b_full;      // B chunks staged (8 arrivals)
@@ -912,6 +912,12 @@ __device__ __forceinline__ void attn_tile(const Params& p, uint32_t sq_base, uin
   }
 }
 
+// The attention phase of layer l for the CTA's share [f0, f1) of all tiles, in
+// rounds. A round takes the rest of the share when that is at most kCons tiles
+// (and at most the ring's stages) and touches at most two pairs; then tile t of the
+// round goes to warp t, and the two pairs are prepared, computed and combined
+// together. Otherwise a round is the rest of the current pair, its tiles taken by
+// ring stage (stage index mod kCons).
 template <class T16>
 __device__ bool consume_attn(const Params& p, Shared& sh, int l, int k) {
   const int warp = threadIdx.x / 32 - 2, lane = threadIdx.x % 32;
@@ -924,134 +930,185 @@ __device__ bool consume_attn(const Params& p, Shared& sh, int l, int k) {
   const int qd = p.H * kHd, kvd = p.Hkv * kHd;
   const float* acc_l = p.qkv_acc + (int64_t)(l & 1) * kMaxTok * p.nqkv_pad;
   const float* ss_l = p.ss + (2 * l) * kMaxTok;
+  const int npairs = p.B * p.Hkv;
   bool ok = true;
   int f = f0;
   int j0 = 0;
   int bg = f0 < f1 ? pair_at(p, f0, j0) : 0;
   while (f < f1) {
-    const int b = (int)((unsigned)bg / (unsigned)p.Hkv), g = bg - b * p.Hkv;
-    const int pos = p.pos[b];
-    const int nt = tiles_of(p, b);
-    const int len = pos + 1;
-    const int last_tile = nt - 1;
-    const int rp = pos - kKeys * last_tile;   // row of pos in the last tile
-    const int j1 = min(nt, j0 + (f1 - f));
-    const float ssb = __ldcg(ss_l + b);   // used after the q/k/v loads are issued
-    const float* accb = acc_l + (int64_t)b * p.nqkv_pad;
-    // ---- Q tile of the group's query heads (rows >= G zero) and, in the CTA that
-    // holds position pos, the new k / v row. Warp w prepares query rows w and w + 8;
-    // warps 0 and 1 also the new k and v. All loads are issued before any use.
-    const bool has_last = j1 == nt;
+    // ---- the round: pieces (pair, tiles [ja, jb)) of one or two pairs
+    int pbg[2], pja[2], pjb[2];
+    const int rest = f1 - f;
+    pbg[0] = bg;
+    pja[0] = j0;
+    pjb[0] = min(tiles_of(p, (int)((unsigned)bg / (unsigned)p.Hkv)), j0 + rest);
+    const int n0 = pjb[0] - pja[0];
+    const bool by_tile = rest <= kCons && rest <= r.n;
+    int npc = 1;
+    if (by_tile && n0 < rest && bg + 1 < npairs &&
+        rest - n0 <= tiles_of(p, (int)((unsigned)(bg + 1) / (unsigned)p.Hkv))) {
+      npc = 2;
+      pbg[1] = bg + 1;
+      pja[1] = 0;
+      pjb[1] = rest - n0;
+    }
+    const int n = npc == 2 ? rest : n0;
+    // ---- per piece: the Q tile of the group's query heads (rows >= G zero) and,
+    // in the CTA that holds position pos, the new k / v row. Warp w prepares query
+    // rows w and w + 8 of each piece; warps 2 pc and 2 pc + 1 also the new k and v
+    // of piece pc. All loads of both pieces are issued before any use.
     {
-      const int nrow = (has_last && warp < 2) ? 3 : 2;
-      float av[3][4];
-      const float* cs = p.cos_tab + (int64_t)pos * (kHd / 2);
-      const float* sn = p.sin_tab + (int64_t)pos * (kHd / 2);
-      float cv[2], sv[2];
+      float av[2][3][4], cv[2][2], sv[2][2], ssb[2];
 #pragma unroll
-      for (int jj = 0; jj < 2; ++jj) {
-        cv[jj] = cs[lane + 32 * jj];
-        sv[jj] = sn[lane + 32 * jj];
-      }
+      for (int pc = 0; pc < 2; ++pc) {
+        ssb[pc] = 0.f;
 #pragma unroll
-      for (int rr = 0; rr < 3; ++rr) {
-        const int hh = warp + 8 * rr;
-        const float* src = nullptr;
-        if (rr < 2 && hh < G) src = accb + (g * G + hh) * kHd;
-        if (rr == 2 && nrow == 3) src = accb + qd + (warp == 0 ? g * kHd : kvd + g * kHd);
+        for (int rr = 0; rr < 3; ++rr)
 #pragma unroll
-        for (int jj = 0; jj < 4; ++jj) av[rr][jj] = src ? __ldcg(src + lane + 32 * jj) : 0.f;
-      }
-      const float rb = rsqrtf(ssb / (float)p.d + p.eps);
+          for (int jj = 0; jj < 4; ++jj) av[pc][rr][jj] = 0.f;
+        cv[pc][0] = cv[pc][1] = sv[pc][0] = sv[pc][1] = 0.f;
+        if (pc >= npc) continue;
+        const int b = (int)((unsigned)pbg[pc] / (unsigned)p.Hkv), g = pbg[pc] - b * p.Hkv;
+        const int pos = p.pos[b];
+        const bool kv_here = pjb[pc] == tiles_of(p, b) && (warp >> 1) == pc;
+        const float* accb = acc_l + (int64_t)b * p.nqkv_pad;
+        ssb[pc] = __ldcg(ss_l + b);
+        const float* cs = p.cos_tab + (int64_t)pos * (kHd / 2);
+        const float* sn = p.sin_tab + (int64_t)pos * (kHd / 2);
 #pragma unroll
-      for (int rr = 0; rr < 3; ++rr)
-#pragma unroll
-        for (int jj = 0; jj < 4; ++jj) av[rr][jj] *= rb;
-#pragma unroll
-      for (int rr = 0; rr < 3; ++rr) {
-        if (rr == 2 && nrow < 3) continue;
-        const bool is_v = rr == 2 && warp == 1;
-        float o[4];
-        if (is_v) {
-#pragma unroll
-          for (int jj = 0; jj < 4; ++jj) o[jj] = av[rr][jj];
-        } else {
-          float sq = 0.f;
-#pragma unroll
-          for (int jj = 0; jj < 4; ++jj) sq += av[rr][jj] * av[rr][jj];
-          sq = warp_sum(sq);
-          const float rn = rsqrtf(sq * (1.f / kHd) + p.eps);
-#pragma unroll
-          for (int jj = 0; jj < 2; ++jj) {
-            const float lo = av[rr][jj], hi = av[rr][jj + 2];
-            o[jj] = (lo * cv[jj] - hi * sv[jj]) * rn;
-            o[jj + 2] = (lo * sv[jj] + hi * cv[jj]) * rn;
-          }
+        for (int jj = 0; jj < 2; ++jj) {
+          cv[pc][jj] = cs[lane + 32 * jj];
+          sv[pc][jj] = sn[lane + 32 * jj];
         }
-        if (rr < 2) {
 #pragma unroll
-          for (int jj = 0; jj < 4; ++jj) st16<T16>(sh.sq, warp + 8 * rr, lane + 32 * jj, o[jj]);
-        } else {
-          const int64_t crow =
-              (((int64_t)l * p.cache_batch + p.b_off + b) * p.Hkv + g) * p.t_max + pos;
-          T16* dstc = static_cast<T16*>(is_v ? p.v_cache : p.k_cache) + crow * kHd;
+        for (int rr = 0; rr < 3; ++rr) {
+          const int hh = warp + 8 * rr;
+          const float* src = nullptr;
+          if (rr < 2 && hh < G) src = accb + (g * G + hh) * kHd;
+          if (rr == 2 && kv_here) src = accb + qd + ((warp & 1) == 0 ? g * kHd : kvd + g * kHd);
 #pragma unroll
-          for (int jj = 0; jj < 4; ++jj) {
-            const T16 v = from_f32<T16>(o[jj]);
-            dstc[lane + 32 * jj] = v;
-            reinterpret_cast<T16*>(sh.kvnew)[(is_v ? kHd : 0) + lane + 32 * jj] = v;
+          for (int jj = 0; jj < 4; ++jj) av[pc][rr][jj] = src ? __ldcg(src + lane + 32 * jj) : 0.f;
+        }
+      }
+#pragma unroll
+      for (int pc = 0; pc < 2; ++pc) {
+        if (pc >= npc) continue;
+        const int b = (int)((unsigned)pbg[pc] / (unsigned)p.Hkv), g = pbg[pc] - b * p.Hkv;
+        const int pos = p.pos[b];
+        const bool kv_here = pjb[pc] == tiles_of(p, b) && (warp >> 1) == pc;
+        const float rb = rsqrtf(ssb[pc] / (float)p.d + p.eps);
+        uint8_t* sq = sh.sq + pc * 4096;
+        uint16_t* kvn = sh.kvnew + pc * 2 * kHd;
+#pragma unroll
+        for (int rr = 0; rr < 3; ++rr) {
+          if (rr == 2 && !kv_here) continue;
+          const bool is_v = rr == 2 && (warp & 1) == 1;
+          float a4[4], o[4];
+#pragma unroll
+          for (int jj = 0; jj < 4; ++jj) a4[jj] = av[pc][rr][jj] * rb;
+          if (is_v) {
+#pragma unroll
+            for (int jj = 0; jj < 4; ++jj) o[jj] = a4[jj];
+          } else {
+            float sq2 = 0.f;
+#pragma unroll
+            for (int jj = 0; jj < 4; ++jj) sq2 += a4[jj] * a4[jj];
+            sq2 = warp_sum(sq2);
+            const float rn = rsqrtf(sq2 * (1.f / kHd) + p.eps);
+#pragma unroll
+            for (int jj = 0; jj < 2; ++jj) {
+              const float lo = a4[jj], hi = a4[jj + 2];
+              o[jj] = (lo * cv[pc][jj] - hi * sv[pc][jj]) * rn;
+              o[jj + 2] = (lo * sv[pc][jj] + hi * cv[pc][jj]) * rn;
+            }
+          }
+          if (rr < 2) {
+#pragma unroll
+            for (int jj = 0; jj < 4; ++jj) st16<T16>(sq, warp + 8 * rr, lane + 32 * jj, o[jj]);
+          } else {
+            const int64_t crow =
+                (((int64_t)l * p.cache_batch + p.b_off + b) * p.Hkv + g) * p.t_max + pos;
+            T16* dstc = static_cast<T16*>(is_v ? p.v_cache : p.k_cache) + crow * kHd;
+#pragma unroll
+            for (int jj = 0; jj < 4; ++jj) {
+              const T16 v = from_f32<T16>(o[jj]);
+              dstc[lane + 32 * jj] = v;
+              reinterpret_cast<T16*>(kvn)[(is_v ? kHd : 0) + lane + 32 * jj] = v;
+            }
           }
         }
       }
     }
     bar_consumers();
     trace_mark(p, k, 0);
-    const uint32_t sq_base = smem_u32(sh.sq);
     float m_r[2] = {-INFINITY, -INFINITY}, l_r[2] = {0.f, 0.f};
     float o[16][4];
 #pragma unroll
     for (int i = 0; i < 16; ++i) o[i][0] = o[i][1] = o[i][2] = o[i][3] = 0.f;
-    // Every ring stage belongs to one warp (stage index mod 8), which takes the
-    // tiles landing there in order. A warp thus waits on each of its stages'
-    // fills one after another and can never reach a fill two ahead of the
-    // producer, where the barrier's parity would match an older, completed fill.
-    for (int j = j0; j < j1; ++j) {
-      int st_i;
-      uint32_t par;
-      r.ahead(j - j0, st_i, par);
-      if (st_i % kCons != warp) continue;
+    // One tile of piece pc: wait for its stage, patch the new row into the last
+    // tile of the pair, accumulate, release the stage.
+    int my_pc = 0;
+    auto run_tile = [&](int pc, int j, int st_i, uint32_t par) {
+      const int b = (int)((unsigned)pbg[pc] / (unsigned)p.Hkv);
+      const int pos = p.pos[b];
+      const int last_tile = tiles_of(p, b) - 1;
       ok = ok && __all_sync(0xffffffffu, bwait(&r.full[st_i], par, p));
       uint8_t* st = r.base + (size_t)st_i * kStage;
       if (ok) {
         if (j == last_tile) {
-          // the new row from registers; V rows past pos zeroed (their p is 0, but
-          // a NaN there would still poison the product)
+          // the new row from shared memory; V rows past pos zeroed (their p is 0,
+          // but a NaN there would still poison the product)
+          const int rp = pos - kKeys * last_tile;
+          const uint16_t* kvn = sh.kvnew + pc * 2 * kHd;
           for (int i = lane; i < kKeys * 16; i += 32) {
             const int rr = i / 16, c16 = i % 16;
             uint4* kd = reinterpret_cast<uint4*>(st + sw_off<kKeys>(rr, c16));
             uint4* vd = reinterpret_cast<uint4*>(st + 8192 + sw_off<kKeys>(rr, c16));
             if (rr == rp) {
-              *kd = reinterpret_cast<const uint4*>(sh.kvnew)[c16];
-              *vd = reinterpret_cast<const uint4*>(sh.kvnew + kHd)[c16];
+              *kd = reinterpret_cast<const uint4*>(kvn)[c16];
+              *vd = reinterpret_cast<const uint4*>(kvn + kHd)[c16];
             } else if (rr > rp) {
               *vd = make_uint4(0u, 0u, 0u, 0u);
             }
           }
           __syncwarp();
         }
-        attn_tile<T16>(p, sq_base, st, j, len, m_r, l_r, o);
+        attn_tile<T16>(p, smem_u32(sh.sq + pc * 4096), st, j, pos + 1, m_r, l_r, o);
         // generic writes into the stage are ordered before the next TMA fill
         if (j == last_tile) fence_proxy_async_smem();
       }
       __syncwarp();
       if (lane == 0) mbar_arrive(&r.empty[st_i]);
+    };
+    if (by_tile) {
+      // tile t of the round to warp t: the round's tiles lie in distinct stages,
+      // and every earlier position of the ring was consumed before the round
+      if (warp < n) {
+        int st_i;
+        uint32_t par;
+        r.ahead(warp, st_i, par);
+        my_pc = warp < n0 ? 0 : 1;
+        run_tile(my_pc, warp < n0 ? pja[0] + warp : warp - n0, st_i, par);
+      }
+    } else {
+      // Every ring stage belongs to one warp (stage index mod 8), which takes the
+      // tiles landing there in order. A warp thus waits on each of its stages'
+      // fills one after another and can never reach a fill two ahead of the
+      // producer, where the barrier's parity would match an older, completed fill.
+      for (int t = 0; t < n; ++t) {
+        int st_i;
+        uint32_t par;
+        r.ahead(t, st_i, par);
+        if (st_i % kCons != warp) continue;
+        run_tile(0, pja[0] + t, st_i, par);
+      }
     }
-    r.skip(j1 - j0);
+    r.skip(n);
     trace_mark(p, k, 1);
     // ---- the warps' states against the fixed reference: row sums over the quad,
     // each row's output and sum scaled by 2^(m - kScoreRef) (0 for a warp without
-    // keys of the row), summed over the warps through shared memory, then added
-    // into the accumulators that all CTAs of the pair share
+    // keys of the row), summed per piece over its warps through shared memory,
+    // then added into the accumulators that all CTAs of the pair share
     float w_r[2];
 #pragma unroll
     for (int h = 0; h < 2; ++h) {
@@ -1062,6 +1119,7 @@ __device__ bool consume_attn(const Params& p, Shared& sh, int l, int k) {
     constexpr int kWs = 16 * kMergeStride + 32;   // floats per warp's merge area
     float* mw = reinterpret_cast<float*>(sh.act) + warp * kWs;
     float* ow = mw + 32;
+    if (lane == 0) mw[0] = (float)my_pc;
     if (tq == 0) {
       mw[16 + gq] = l_r[0] * w_r[0];
       mw[16 + gq + 8] = l_r[1] * w_r[1];
@@ -1078,33 +1136,38 @@ __device__ bool consume_attn(const Params& p, Shared& sh, int l, int k) {
     {
       const float* const mall = reinterpret_cast<const float*>(sh.act);
       const int sl = l & 1;
-      float* num = p.att_num + ((int64_t)sl * kMaxTok + b) * qd + g * G * kHd;
-      float* den = p.att_den + (sl * kMaxTok + b) * p.H + g * G;
-      for (int e = tid; e < G * kHd / 4; e += 256) {
-        const int h = e / (kHd / 4), i = (e % (kHd / 4)) * 4;
+      for (int e = tid; e < npc * G * (kHd / 4); e += 256) {
+        const int pc = e >= G * (kHd / 4) ? 1 : 0;
+        const int e1 = e - pc * G * (kHd / 4);
+        const int h = e1 / (kHd / 4), i = (e1 % (kHd / 4)) * 4;
+        const int b = (int)((unsigned)pbg[pc] / (unsigned)p.Hkv), g = pbg[pc] - b * p.Hkv;
         float4 v = make_float4(0.f, 0.f, 0.f, 0.f);
 #pragma unroll
         for (int w = 0; w < kCons; ++w) {
+          if (mall[w * kWs] != (float)pc) continue;
           const float4 ov = *reinterpret_cast<const float4*>(mall + w * kWs + 32 + h * kMergeStride + i);
           v.x += ov.x;
           v.y += ov.y;
           v.z += ov.z;
           v.w += ov.w;
         }
-        red_add_f32x4(num + h * kHd + i, v);
+        red_add_f32x4(p.att_num + ((int64_t)sl * kMaxTok + b) * qd + (g * G + h) * kHd + i, v);
       }
-      if (tid < G) {
+      if (tid < npc * G) {
+        const int pc = tid >= G ? 1 : 0, h = tid - pc * G;
+        const int b = (int)((unsigned)pbg[pc] / (unsigned)p.Hkv), g = pbg[pc] - b * p.Hkv;
         float L = 0.f;
 #pragma unroll
-        for (int w = 0; w < kCons; ++w) L += mall[w * kWs + 16 + tid];
-        red_add_f32(den + tid, L);
+        for (int w = 0; w < kCons; ++w)
+          if (mall[w * kWs] == (float)pc) L += mall[w * kWs + 16 + h];
+        red_add_f32(p.att_den + (sl * kMaxTok + b) * p.H + g * G + h, L);
       }
     }
     trace_mark(p, k, 2);
     bar_consumers();
     trace_mark(p, k, 3);
-    f += j1 - j0;
-    ++bg;
+    f += n;
+    bg = pbg[npc - 1] + 1;
     j0 = 0;
   }
   return ok;
@@ -1542,9 +1605,9 @@ __global__ void __launch_bounds__(kThreads, 1)
   sh.act = q;
   q += p.act_bytes;
   sh.sq = q;
-  q += 4096;
+  q += 8192;   // Q tiles of up to two pairs
   sh.kvnew = reinterpret_cast<uint16_t*>(q);
-  q += 512;
+  q += 1024;   // new K and V rows of up to two pairs
   sh.ring.full = reinterpret_cast<uint64_t*>(q);
   sh.ring.empty = sh.ring.full + p.stages;
   sh.acc_full = sh.ring.empty + p.stages;
@@ -1706,7 +1769,7 @@ static int b_slots_needed(int d, int H, int F, int nqkv_pad, int vpad, int P) {
 }
 
 static size_t smem_bytes(int act, int* stages) {
-  const int fixed = 1024 /*align*/ + 4096 + 512 + 256;
+  const int fixed = 1024 /*align*/ + 8192 + 1024 + 256;
   const int limit = 232448 - 1024;   // dynamic part; static shared memory is small
   int st = (limit - fixed - act) / (kStage + 16);
   if (st > 16) st = 16;
@@ -1744,7 +1807,15 @@ int plan_attention(Params& p, int P) {
   if (total * (P + 1) >= (int64_t(1) << 31)) return -1;
   p.tile_pre[p.B] = (int)total;
   p.attn_total = (int)total;
-  p.attn_blocks = (pairs <= P && P <= kMaxAttnBlocks) ? 1 : 0;
+  // Even shares of all tiles when no share exceeds kCons tiles and none can span
+  // more than two pairs (every pair at least the largest share minus one tiles):
+  // each CTA then computes its tiles in one round, one per warp. Otherwise, with
+  // no more pairs than CTAs, per-pair CTA blocks (one pair per CTA).
+  int min_tiles = INT_MAX;
+  for (int b = 0; b < p.B; ++b) min_tiles = std::min(min_tiles, tiles_of(p, b));
+  const int64_t largest = (total + P - 1) / P;
+  const bool even = largest <= kCons && min_tiles >= largest - 1;
+  p.attn_blocks = (!even && pairs <= P && P <= kMaxAttnBlocks) ? 1 : 0;
   if (p.attn_blocks) {
     // every pair one CTA, the other P - pairs CTAs in proportion to its tiles
     for (int bg = 0; bg <= pairs; ++bg) {
