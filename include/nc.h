@@ -55,8 +55,12 @@ typedef enum {
     NC_ERR_OOM = 3,             /* device allocation failed */
     NC_ERR_CUDA = 4,            /* a CUDA runtime/driver call failed */
     NC_ERR_DEVICE_TIMEOUT = 5,  /* a kernel's bounded wait ran out (device status word) */
-    NC_ERR_BOUNDS = 6           /* a token id outside [0, vocab) was seen (device status word);
+    NC_ERR_BOUNDS = 6,          /* a token id outside [0, vocab) was seen (device status word);
                                    the kernel used row 0 in its place */
+    NC_ERR_RANGE = 7            /* a value stored in fp16 (act_dtype NC_F16) was too large for
+                                   it and became +-inf (device status word): the V rows of the
+                                   KV cache, the ReLU^2 activations, or the decode step's
+                                   un-normalised residual; NC_BF16 has fp32's range */
 } nc_status;
 
 typedef enum { NC_F32 = 0, NC_BF16 = 1, NC_F16 = 2 } nc_dtype;
@@ -280,7 +284,8 @@ NC_API nc_status nc_decode_step_ragged(nc_model* m, const int32_t* tokens, const
                                        nc_kv_cache* c, void* stream);
 
 /* Synchronises `stream`, reads and clears the device status word. Returns NC_OK,
- * NC_ERR_BOUNDS or NC_ERR_DEVICE_TIMEOUT (or NC_ERR_CUDA). */
+ * NC_ERR_DEVICE_TIMEOUT, NC_ERR_BOUNDS or NC_ERR_RANGE, in that order of
+ * precedence (or NC_ERR_CUDA). */
 NC_API nc_status nc_model_check(nc_model* m, void* stream);
 
 /* ------------------------------------------------------------------------

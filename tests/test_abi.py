@@ -71,6 +71,7 @@ def test_create_rejects_bad_config_without_touching_the_device(lib):
 def test_status_strings(lib):
     assert lib.nc_status_string(0) == b"ok"
     assert lib.nc_status_string(binding.NC_ERR_BOUNDS) == b"token id out of range"
+    assert lib.nc_status_string(binding.NC_ERR_RANGE) == b"value out of fp16 range"
     assert binding.nc_version().startswith("nc-b300")
 
 

@@ -112,6 +112,54 @@ def test_bad_token_is_flagged_not_faulted(cuda_device):
     assert nc.nc_model_check(model.handle) == nc.NC_OK    # cleared after reading
 
 
+def _scale_pow2(W, name, k):
+    """Multiplies one matrix of W by 2^k (exact, also for its bf16 bits)."""
+    if name == "wte":
+        W.wte = W.wte * np.float32(2.0 ** k)
+        arr = W.wte
+    else:
+        l, n = name.split(".")[1], name.split(".")[2]
+        mats = list(W.layers[int(l)])
+        i = synth.LAYER_MATRIX_NAMES.index(n)
+        mats[i] = mats[i] * np.float32(2.0 ** k)
+        W.layers[int(l)] = tuple(mats)
+        arr = mats[i]
+    if W.bits is not None:
+        W.bits[name] = synth.round_to_bf16_bits(arr)
+
+
+@pytest.mark.parametrize("act", ["f16", "bf16"])
+@pytest.mark.parametrize("case", ["relu2", "residual"])
+def test_fp16_overflow_is_flagged(cuda_device, act, case):
+    """Values stored in fp16 that exceed its range latch NC_ERR_RANGE instead of
+    silently becoming inf. 'relu2': W_fc x 2^9 puts the ReLU^2 activations near
+    2^18 (the prefill's FC epilogue and the decode step's PROJ staging). 'residual':
+    wte x 2^20 puts the residual near 3e4 RMS, which only the decode step stages
+    un-normalised. bf16 has fp32's range: no flag."""
+    import torch
+    shape = synth.with_changes(synth.D20_MQA, name="range", n_layer=1, vocab=512)
+    W = synth.make_weights(shape)
+    if case == "relu2":
+        _scale_pow2(W, "layers.0.w_fc", 9)
+    else:
+        _scale_pow2(W, "wte", 20)
+    adt = nc.NC_F16 if act == "f16" else nc.NC_BF16
+    model = nc.Model(W, max_seq=48, max_batch=2, act_dtype=adt)
+    nc.nc_model_set_decode_path(model.handle, nc.NC_DECODE_PERSISTENT)
+    cache = model.cache(2, 48)
+    toks = torch.from_numpy(synth.make_tokens(shape, 2, 33)).cuda()
+    am = torch.empty(2, dtype=torch.int32, device="cuda")
+    nc.nc_prefill_last(model.handle, toks[:, :32].contiguous(), 2, 32, None, am, cache.handle)
+    want_prefill = nc.NC_ERR_RANGE if (act == "f16" and case == "relu2") else nc.NC_OK
+    assert nc.nc_model_check(model.handle) == want_prefill
+    nc.nc_decode_step(model.handle, toks[:, 32].contiguous(), 2, 32, None, am, cache.handle)
+    want_decode = nc.NC_ERR_RANGE if act == "f16" else nc.NC_OK
+    assert nc.nc_model_check(model.handle) == want_decode
+    assert nc.nc_model_check(model.handle) == nc.NC_OK   # cleared after reading
+    cache.close()
+    model.close()
+
+
 def test_host_argument_errors(cuda_device):
     import torch
     shape = synth.TINY

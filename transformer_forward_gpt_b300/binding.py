@@ -14,7 +14,7 @@ PKG = os.path.dirname(os.path.abspath(__file__))
 LIB_PATH = os.path.join(PKG, "libnc.so")
 
 NC_OK, NC_ERR_INVALID_ARG, NC_ERR_UNSUPPORTED, NC_ERR_OOM, NC_ERR_CUDA, \
-    NC_ERR_DEVICE_TIMEOUT, NC_ERR_BOUNDS = range(7)
+    NC_ERR_DEVICE_TIMEOUT, NC_ERR_BOUNDS, NC_ERR_RANGE = range(8)
 NC_F32, NC_BF16, NC_F16 = 0, 1, 2
 
 EXPORTS = (

@@ -210,6 +210,7 @@ const char* nc_status_string(nc_status s) {
     case NC_ERR_CUDA: return "CUDA error";
     case NC_ERR_DEVICE_TIMEOUT: return "device wait timed out";
     case NC_ERR_BOUNDS: return "token id out of range";
+    case NC_ERR_RANGE: return "value out of fp16 range";
   }
   return "unknown status";
 }
@@ -515,7 +516,7 @@ nc_status run_blocks(nc_model* m, nc_kv_cache* c, int B, int rows_per_seq, int p
   for (int l = 0; l < cfg.n_layer; ++l) {
     QkvDst dst{m->q, layer_ptr(c->k, c->layer_elems, l, dt), layer_ptr(c->v, c->layer_elems, l, dt),
                H, Hkv, hd, c->t_max, m->cos_tab, m->sin_tab, cfg.rms_eps,
-               m->cos_t, m->sin_t, cfg.max_seq};
+               m->cos_t, m->sin_t, cfg.max_seq, m->status};
     // Q/K/V projections + RoPE + QK norm + cache write
     {
     ProfScope ps(m, NC_K_QKV, s);
@@ -583,7 +584,7 @@ nc_status run_blocks(nc_model* m, nc_kv_cache* c, int B, int rows_per_seq, int p
       nc::launch_gemm_simt(m->att, m->wo[l], m->part, M, d, H * hd, d, dt, s);
       nc::launch_residual_finish(m->part, 1, m->x, M, d, m->xn, dt, cfg.rms_eps, s);
       nc::launch_gemm_simt(m->xn, m->w_fc[l], m->part, M, F, d, F, dt, s);
-      nc::launch_relu2_finish(m->part, 1, m->h, M, F, dt, s);
+      nc::launch_relu2_finish(m->part, 1, m->h, M, F, dt, m->status, s);
       nc::launch_gemm_simt(m->h, m->w_proj[l], m->part, M, d, F, d, dt, s);
       nc::launch_residual_finish(m->part, 1, m->x, M, d, m->xn, dt, cfg.rms_eps, s);
     }
@@ -1108,6 +1109,11 @@ nc_status nc_model_check(nc_model* m, void* stream) {
   if (word & nc::ST_BAD_TOKEN) {
     set_err("a token id was outside [0, vocab); row 0 was used");
     return NC_ERR_BOUNDS;
+  }
+  if (word & nc::ST_RANGE) {
+    set_err("a value stored in fp16 exceeded its range (|v| >= 65520) and became inf; "
+            "act_dtype NC_BF16 has fp32's range");
+    return NC_ERR_RANGE;
   }
   return NC_OK;
 }

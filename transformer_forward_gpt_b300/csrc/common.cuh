@@ -16,7 +16,25 @@ typedef __half f16;
 enum : uint32_t {
   ST_BAD_TOKEN = 1u,   // a token id outside [0, vocab): row 0 was used instead
   ST_TIMEOUT = 2u,     // a bounded wait gave up
+  ST_RANGE = 4u,       // a value stored in fp16 was too large for it (became +-inf)
 };
+
+// Whether T16 is fp16, whose largest finite value is 65504: a float at or above
+// 65520 in magnitude rounds to infinity when stored. bf16 has fp32's range.
+template <class T>
+struct IsF16 {
+  static constexpr bool value = false;
+};
+template <>
+struct IsF16<__half> {
+  static constexpr bool value = true;
+};
+// Latches ST_RANGE when amax, the largest magnitude a thread is about to store in
+// T16, overflows fp16 (unbounded values only: V rows, ReLU^2, the raw residual).
+template <class T16>
+__device__ __forceinline__ void note_range(float amax, uint32_t* status) {
+  if (IsF16<T16>::value && amax >= 65520.f && status) atomicOr(status, ST_RANGE);
+}
 
 // Upper bound of any single wait inside a kernel (nanoseconds of %globaltimer).
 constexpr uint64_t kWaitLimitNs = 1000ull * 1000ull * 1000ull;   // 1 s

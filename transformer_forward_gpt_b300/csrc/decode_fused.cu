@@ -707,7 +707,7 @@ __device__ void stage_b(const Params& p, const Shared& sh, const Gemv& g, const 
     const bool want_ss = g.act_kind == ACT_X32 && g.ss_out != nullptr;
     float rscale = 0.f;
     if (g.act_kind == ACT_H32 && tok_ok) rscale = rsqrtf(__ldcg(g.ss_in + tok) / (float)p.d + p.eps);
-    float ssum = 0.f;
+    float ssum = 0.f, amax = 0.f;
     uint8_t* dst = sh.act + bchunk_off(tok, j);
     for (int s0 = 0; s0 < rg.nslots; s0 += 8) {
       float4 a[8], b[8];
@@ -741,11 +741,14 @@ __device__ void stage_b(const Params& p, const Shared& sh, const Gemv& g, const 
             v[e] = t * t;
           }
         }
+#pragma unroll
+        for (int e = 0; e < 8; ++e) amax = fmaxf(amax, fabsf(v[e]));
         *reinterpret_cast<uint4*>(dst + (size_t)s * kChunkBytes) =
             make_uint4(pack2<T16>(v[0], v[1]), pack2<T16>(v[2], v[3]), pack2<T16>(v[4], v[5]),
                        pack2<T16>(v[6], v[7]));
       }
     }
+    note_range<T16>(amax, p.status);   // x is staged un-normalised
     if (want_ss) {
       // the eight lanes of a token are adjacent
       ssum += __shfl_xor_sync(0xffffffffu, ssum, 1);
@@ -1007,8 +1010,13 @@ __device__ bool consume_attn(const Params& p, Shared& sh, int l, int k) {
 #pragma unroll
           for (int jj = 0; jj < 4; ++jj) a4[jj] = av[pc][rr][jj] * rb;
           if (is_v) {
+            float amax = 0.f;
 #pragma unroll
-            for (int jj = 0; jj < 4; ++jj) o[jj] = a4[jj];
+            for (int jj = 0; jj < 4; ++jj) {
+              o[jj] = a4[jj];
+              amax = fmaxf(amax, fabsf(o[jj]));
+            }
+            note_range<T16>(amax, p.status);
           } else {
             float sq2 = 0.f;
 #pragma unroll

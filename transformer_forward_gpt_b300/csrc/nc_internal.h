@@ -38,6 +38,7 @@ struct QkvDst {
   const float* cos_t;     // the same tables position-minor: [hd/2, max_seq]
   const float* sin_t;
   int32_t tab_ld;         // max_seq
+  uint32_t* status;       // device status word (fp16 range of the V rows), or NULL
 };
 
 // ---- CUDA-core kernels (simt.cu)
@@ -55,7 +56,7 @@ void launch_qkv_post(const float* part, int n_split, int64_t M, const RowMap& rm
 void launch_residual_finish(const float* part, int n_split, float* x, int64_t M, int N,
                             void* xn_out, nc_dtype dt, float eps, cudaStream_t s);
 void launch_relu2_finish(const float* part, int n_split, void* h, int64_t M, int N, nc_dtype dt,
-                         cudaStream_t s);
+                         uint32_t* status, cudaStream_t s);
 void launch_sum_splits(const float* part, int n_split, float* out, int64_t M, int N, int64_t ldo,
                        cudaStream_t s);
 void launch_attention_prefill_simt(const void* q, const void* k, const void* v, void* o, int B,

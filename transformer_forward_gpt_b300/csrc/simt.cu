@@ -165,10 +165,13 @@ __global__ void qkv_post_kernel(const float* __restrict__ part, int n_split, int
     const int g = j - dst.H - dst.Hkv;
     T* out = reinterpret_cast<T*>(dst.v_cache) + (((int64_t)b * dst.Hkv + g) * dst.t_max + t) * hd;
     cnt = 0;
+    float amax = 0.f;
     for (int i = lane; i < half; i += 32, ++cnt) {
       out[i] = from_f32<T>(lo[cnt]);
       out[i + half] = from_f32<T>(hi[cnt]);
+      amax = fmaxf(amax, fmaxf(fabsf(lo[cnt]), fabsf(hi[cnt])));
     }
+    note_range<T>(amax, dst.status);
     return;
   }
   cnt = 0;
@@ -228,14 +231,17 @@ __global__ void residual_finish_kernel(const float* __restrict__ part, int n_spl
 // h = relu(sum of partials)^2, elementwise.
 template <class T>
 __global__ void relu2_finish_kernel(const float* __restrict__ part, int n_split,
-                                    T* __restrict__ h, int64_t total) {
+                                    T* __restrict__ h, int64_t total, uint32_t* status) {
+  float amax = 0.f;
   for (int64_t i = (int64_t)blockIdx.x * blockDim.x + threadIdx.x; i < total;
        i += (int64_t)gridDim.x * blockDim.x) {
     float a = 0.f;
     for (int s = 0; s < n_split; ++s) a += part[s * total + i];
     a = fmaxf(a, 0.f);
+    amax = fmaxf(amax, a * a);
     h[i] = from_f32<T>(a * a);
   }
+  note_range<T>(amax, status);
 }
 
 __global__ void sum_splits_kernel(const float* __restrict__ part, int n_split,
@@ -484,11 +490,11 @@ void launch_residual_finish(const float* part, int n_split, float* x, int64_t M,
 }
 
 void launch_relu2_finish(const float* part, int n_split, void* h, int64_t M, int N, nc_dtype dt,
-                         cudaStream_t s) {
+                         uint32_t* status, cudaStream_t s) {
   count_launches(1);
   const int64_t total = M * N;
   const unsigned grid = (unsigned)std::min<int64_t>((total + 255) / 256, 148 * 16);
-  NC_DISPATCH(dt, T, (relu2_finish_kernel<T><<<grid, 256, 0, s>>>(part, n_split, (T*)h, total)));
+  NC_DISPATCH(dt, T, (relu2_finish_kernel<T><<<grid, 256, 0, s>>>(part, n_split, (T*)h, total, status)));
 }
 
 void launch_sum_splits(const float* part, int n_split, float* out, int64_t M, int N, int64_t ldo,

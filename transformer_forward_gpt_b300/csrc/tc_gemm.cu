@@ -173,11 +173,14 @@ __device__ __forceinline__ void epi_store_rows(const GemmArgs& p, uint32_t taddr
     const int n0 = nb * BN + c * 32;
     if (n0 >= p.N) continue;   // uniform across the warp
     if (mode == EPI_RELU2) {
+      float amax = 0.f;
 #pragma unroll
       for (int j = 0; j < 32; ++j) {
         const float r = fmaxf(v[j], 0.f);
         v[j] = r * r;
+        amax = fmaxf(amax, v[j]);
       }
+      note_range<T16>(amax, p.status);
     }
 #pragma unroll
     for (int i = 0; i < 8; ++i)
@@ -247,6 +250,10 @@ __device__ __forceinline__ void epi_qkv(const GemmArgs& p, uint32_t taddr, int r
         float v[32];
         tmem_ld32_sync(base + c * 32, v);
         if (valid) {
+          float amax = 0.f;
+#pragma unroll
+          for (int i = 0; i < 32; ++i) amax = fmaxf(amax, fabsf(v[i]));
+          note_range<T16>(amax, p.status);
 #pragma unroll
           for (int i = 0; i < 4; ++i)
             *reinterpret_cast<uint4*>(out + c * 32 + 8 * i) = make_uint4(
@@ -720,7 +727,7 @@ static nc_status fc_impl(TcModel* t, int l, int64_t M, float* part, cudaStream_t
     nc_status st = swap_partials<T16>(t, w.wfc, w.wfc, w.wfc, INT_MAX, INT_MAX, F, d, t->xn, M,
                                       part, &ns, s);
     if (st != NC_OK) return st;
-    launch_relu2_finish(part, ns, t->h, M, F, act_of(t), s);
+    launch_relu2_finish(part, ns, t->h, M, F, act_of(t), t->status, s);
     return cudaGetLastError() == cudaSuccess ? NC_OK : NC_ERR_CUDA;
   }
   CUtensorMap a;
