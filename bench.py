@@ -354,7 +354,9 @@ def run_ours(args):
                     "tflops": round(pre_tflops, 1), "algorithmic_tflop": round((g_flops + a_flops) / 1e12, 3),
                     "frac_of_peak": round(pre_tflops / bf16_peak, 4),
                     "peak": bf16_peak, "peak_source": f"{peak_src} bf16",
-                    "frac_of_nominal_peak": round(pre_tflops / NOMINAL["bf16_tflops"], 4)},
+                    "frac_of_nominal_peak": round(pre_tflops / NOMINAL["bf16_tflops"], 4),
+                    "operands": "fp16 GEMM operands, activations and KV cache on bf16 weights "
+                                "(report.d20_prefill_bf16_mode times bf16 activations)"},
         "decode": {"value": round(dec_value, 1), "unit": "tok/s", "ms_per_token_step": round(dec_ms / K / steps, 4),
                    "gbs": round(dec_gbs, 1), "algorithmic_mb_per_step": round(dec_bytes / steps / 1e6, 1),
                    "frac_of_peak": round(dec_gbs / peaks["hbm_gbs"], 4),
