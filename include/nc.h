@@ -51,7 +51,7 @@ extern "C" {
 typedef enum {
     NC_OK = 0,
     NC_ERR_INVALID_ARG = 1,     /* null/misaligned pointer, size or position out of range */
-    NC_ERR_UNSUPPORTED = 2,     /* shape this build has no kernel for */
+    NC_ERR_UNSUPPORTED = 2,     /* shape the library has no kernel for */
     NC_ERR_OOM = 3,             /* device allocation failed */
     NC_ERR_CUDA = 4,            /* a CUDA runtime/driver call failed */
     NC_ERR_DEVICE_TIMEOUT = 5,  /* a kernel's bounded wait ran out (device status word) */
