@@ -366,6 +366,41 @@ NC_API nc_status nc_op_sample(const float* logits, int32_t rows, int32_t n, floa
                               const float* u, int32_t* out, void* stream);
 
 /* ------------------------------------------------------------------------
+ * fp8 projection variant. The pages name fp8 only as a current topic of the
+ * project (一天一个开源项目（第22篇）：nanochat, m.alixixi.com, section 项目简介, the
+ * "版本" bullet) and define no format or scaling; the readings here: E4M3 without
+ * infinities (1 sign, 4 exponent bits with bias 7, 3 mantissa bits, largest
+ * finite value 448), rounding to nearest with ties to the even mantissa,
+ * saturating; a matrix is scaled per row by max|row| / 448 (1 for a zero row),
+ * computed in fp32. The product runs on the tensor cores (tcgen05, kind::f8f6f4)
+ * with fp32 accumulation: half the weight bytes of the 16-bit path.
+ * ---------------------------------------------------------------------- */
+
+/* scale[r] = max_c |x[r, c]| / 448 (1 if the row is zero) and q[r, c] =
+ * E4M3(x[r, c] / scale[r]) (one byte each, nearest-even, saturating; the division
+ * is IEEE fp32). x dev [rows, cols] in dtype (NC_F32, NC_BF16 or NC_F16); q dev
+ * uint8 [rows, cols]; scale dev fp32 [rows]. cols % 16 == 0. Errors:
+ * NC_ERR_INVALID_ARG for NULL or misaligned pointers or bad sizes. */
+NC_API nc_status nc_op_quantize_e4m3(const void* x, nc_dtype dtype, int64_t rows, int32_t cols,
+                                     uint8_t* q, float* scale, void* stream);
+
+/* Device scratch that nc_op_gemv_e4m3 needs for N features, K inputs, B tokens. */
+NC_API size_t nc_op_gemv_e4m3_scratch_bytes(int32_t N, int32_t K, int32_t B);
+
+/* y[t, n] = w_scale[n] * s_t * sum_k wq[n, k] * E4M3(x[t, k] / s_t), the
+ * activations scaled per token as nc_op_quantize_e4m3 does: a decode step's
+ * projection with fp8 weights (wq, w_scale from nc_op_quantize_e4m3 on W [N, K]).
+ * wq dev [N, K] E4M3 codes, w_scale dev fp32 [N], x dev fp32 [B, K], y dev fp32
+ * [B, N]; 1 <= B <= 128, K % 128 == 0, pointers 16-byte aligned; scratch dev of
+ * at least nc_op_gemv_e4m3_scratch_bytes(N, K, B) bytes, owned by the caller
+ * (not used by two calls at once). Nothing is allocated. Errors:
+ * NC_ERR_INVALID_ARG for NULL or misaligned pointers, bad sizes or a small
+ * scratch; NC_ERR_CUDA if a launch fails. */
+NC_API nc_status nc_op_gemv_e4m3(const uint8_t* wq, const float* w_scale, int32_t N, int32_t K,
+                                 const float* x, int32_t B, float* y, void* scratch,
+                                 size_t scratch_bytes, void* stream);
+
+/* ------------------------------------------------------------------------
  * Measurement: per-kernel-class device time and a launch counter. Host-side
  * bookkeeping only; results are unchanged.
  * ---------------------------------------------------------------------- */

@@ -27,7 +27,8 @@ EXPORTS = (
     "nc_op_attention_decode_noalloc", "nc_model_set_decode_path", "nc_decode_trace",
     "nc_decode_trace_entries", "nc_op_sample", "nc_prefill_continue",
     "nc_decode_step_ragged", "nc_kv_cache_set_lengths", "nc_kv_cache_lengths",
-    "nc_decode_step_sample", "nc_generate_host_sample",
+    "nc_decode_step_sample", "nc_generate_host_sample", "nc_op_quantize_e4m3",
+    "nc_op_gemv_e4m3_scratch_bytes", "nc_op_gemv_e4m3",
 )
 
 KERNEL_KINDS = ("embed", "norm", "qkv", "attn_prefill", "attn_decode", "oproj", "fc", "proj",
@@ -93,6 +94,9 @@ def load(path: str = LIB_PATH):
                                              C.c_int, vp, sz, vp]),
         "nc_op_argmax": (C.c_int, [vp, i32, i32, vp, vp]),
         "nc_op_sample": (C.c_int, [vp, i32, i32, C.c_float, vp, vp, vp]),
+        "nc_op_quantize_e4m3": (C.c_int, [vp, C.c_int, i64, i32, vp, vp, vp]),
+        "nc_op_gemv_e4m3_scratch_bytes": (sz, [i32, i32, i32]),
+        "nc_op_gemv_e4m3": (C.c_int, [vp, vp, i32, i32, vp, i32, vp, vp, sz, vp]),
         "nc_kv_cache_set_length": (C.c_int, [vp, i32]),
         "nc_profile_begin": (C.c_int, [vp]),
         "nc_profile_end": (C.c_int, [vp, vp, C.POINTER(NcKernelTime)]),
@@ -284,6 +288,20 @@ def nc_op_argmax(x, rows, n, out, stream=None):
 def nc_op_sample(logits, rows, n, temperature, u, out, stream=None):
     _check(load().nc_op_sample(_ptr(logits), rows, n, float(temperature), _ptr(u), _ptr(out),
                                _stream(stream)), "nc_op_sample")
+
+
+def nc_op_quantize_e4m3(x, dtype, rows, cols, q, scale, stream=None):
+    _check(load().nc_op_quantize_e4m3(_ptr(x), dtype, rows, cols, _ptr(q), _ptr(scale),
+                                      _stream(stream)), "nc_op_quantize_e4m3")
+
+
+def nc_op_gemv_e4m3_scratch_bytes(N, K, B):
+    return load().nc_op_gemv_e4m3_scratch_bytes(N, K, B)
+
+
+def nc_op_gemv_e4m3(wq, w_scale, N, K, x, B, y, scratch, scratch_bytes, stream=None):
+    _check(load().nc_op_gemv_e4m3(_ptr(wq), _ptr(w_scale), N, K, _ptr(x), B, _ptr(y), _ptr(scratch),
+                                  scratch_bytes, _stream(stream)), "nc_op_gemv_e4m3")
 
 
 def nc_op_attention_decode_noalloc(q, k, v, o, B, H, Hkv, length, t_max, hd, dtype, stream=None):

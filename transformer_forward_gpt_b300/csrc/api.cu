@@ -1146,6 +1146,32 @@ nc_status nc_op_gemm(const void* A, const void* B, float* C, int32_t M, int32_t 
   return check_launch();
 }
 
+nc_status nc_op_quantize_e4m3(const void* x, nc_dtype dtype, int64_t rows, int32_t cols, uint8_t* q,
+                              float* scale, void* stream) {
+  NC_CHECK(x && q && scale && aligned16(x) && aligned16(q), NC_ERR_INVALID_ARG, "NULL/misaligned");
+  NC_CHECK(rows >= 0 && rows <= INT32_MAX && cols > 0 && cols % 16 == 0, NC_ERR_INVALID_ARG,
+           "bad sizes");
+  NC_CHECK(dtype == NC_F32 || dtype == NC_BF16 || dtype == NC_F16, NC_ERR_INVALID_ARG, "bad dtype");
+  return nc::quantize_e4m3(x, dtype, rows, cols, q, scale, static_cast<cudaStream_t>(stream));
+}
+
+size_t nc_op_gemv_e4m3_scratch_bytes(int32_t N, int32_t K, int32_t B) {
+  if (N <= 0 || K <= 0 || B <= 0 || B > 128) return 0;
+  return nc::gemv_e4m3_scratch_bytes(N, K, B);
+}
+
+nc_status nc_op_gemv_e4m3(const uint8_t* wq, const float* w_scale, int32_t N, int32_t K,
+                          const float* x, int32_t B, float* y, void* scratch, size_t scratch_bytes,
+                          void* stream) {
+  NC_CHECK(wq && w_scale && x && y && scratch && aligned16(wq) && aligned16(x) && aligned16(y) &&
+               aligned16(scratch),
+           NC_ERR_INVALID_ARG, "NULL/misaligned");
+  NC_CHECK(N > 0 && K > 0 && K % 128 == 0 && B >= 1 && B <= 128, NC_ERR_INVALID_ARG, "bad sizes");
+  NC_CHECK(scratch_bytes >= nc::gemv_e4m3_scratch_bytes(N, K, B), NC_ERR_INVALID_ARG,
+           "scratch too small");
+  return nc::gemv_e4m3(wq, w_scale, N, K, x, B, y, scratch, static_cast<cudaStream_t>(stream));
+}
+
 nc_status nc_op_attention_prefill(const void* q, const void* k, const void* v, void* o, int32_t B,
                                   int32_t H, int32_t Hkv, int32_t T, int32_t t_max, int32_t hd,
                                   nc_dtype dtype, void* stream) {

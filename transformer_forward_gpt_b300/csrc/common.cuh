@@ -4,6 +4,7 @@
 #include <cuda.h>
 #include <cuda_bf16.h>
 #include <cuda_fp16.h>
+#include <cuda_fp8.h>
 #include <cuda_runtime.h>
 #include <stdint.h>
 
@@ -77,9 +78,17 @@ template <> __device__ __forceinline__ float2 unpack2<f16>(uint32_t u) {
   return __half22float2(*reinterpret_cast<__half2*>(&u));
 }
 // tcgen05 / mma operand format code of a 16-bit type (kind::f16: F16 = 0, BF16 = 1).
+// 8-bit E4M3 operand element (tag type; stored as bytes)
+struct e4m3 {
+  uint8_t bits;
+};
+
+// Operand type code of the MMA instruction descriptor: f16 / bf16 for kind::f16,
+// E4M3 for kind::f8f6f4.
 template <class T> struct Fmt16;
 template <> struct Fmt16<bf16> { static constexpr uint32_t code = 1; };
 template <> struct Fmt16<f16> { static constexpr uint32_t code = 0; };
+template <> struct Fmt16<e4m3> { static constexpr uint32_t code = 0; };
 
 // 2^x with the hardware's approximate exp2 (flush-to-zero; 2^-inf = 0).
 __device__ __forceinline__ float ex2_approx(float x) {
@@ -229,6 +238,25 @@ __device__ __forceinline__ void mma_f16kind_ss(uint32_t d_tmem, uint64_t a_desc,
       " tcgen05.mma.cta_group::1.kind::f16 [%0], %1, %2, %3, p;\n}\n" ::"r"(d_tmem),
       "l"(a_desc), "l"(b_desc), "r"(idesc), "r"(accumulate)
       : "memory");
+}
+// D (+)= A * B^T with 8-bit operands (both E4M3 here), fp32 accumulation: K = 32
+// per instruction, 32 bytes of a K-major row, as a kind::f16 step covers.
+__device__ __forceinline__ void mma_f8kind_ss(uint32_t d_tmem, uint64_t a_desc, uint64_t b_desc,
+                                           uint32_t idesc, uint32_t accumulate) {
+  asm volatile(
+      "{\n .reg .pred p;\n setp.ne.b32 p, %4, 0;\n"
+      " tcgen05.mma.cta_group::1.kind::f8f6f4 [%0], %1, %2, %3, p;\n}\n" ::"r"(d_tmem),
+      "l"(a_desc), "l"(b_desc), "r"(idesc), "r"(accumulate)
+      : "memory");
+}
+// The MMA of an operand type: kind::f8f6f4 for E4M3, kind::f16 otherwise.
+template <class T>
+__device__ __forceinline__ void mma_ss(uint32_t d_tmem, uint64_t a_desc, uint64_t b_desc,
+                                       uint32_t idesc, uint32_t accumulate) {
+  if constexpr (sizeof(T) == 1)
+    mma_f8kind_ss(d_tmem, a_desc, b_desc, idesc, accumulate);
+  else
+    mma_f16kind_ss(d_tmem, a_desc, b_desc, idesc, accumulate);
 }
 // Arrives once on the mbarrier when all previously issued MMAs of this thread finish.
 __device__ __forceinline__ void mma_commit(uint64_t* bar) {

@@ -44,6 +44,12 @@ nc_status tc_attention_prefill_tc(const void* q, const void* k, const void* v, v
                                   int64_t layer_stride, int layer, nc_dtype dt, uint32_t* status,
                                   cudaStream_t s);
 // C[M, N] = A[M, K] B[N, K]^T, fp32 out (single-step entry point).
+// fp8 (E4M3) projection variant: row-wise quantisation and the scaled product
+nc_status quantize_e4m3(const void* x, nc_dtype dt, int64_t rows, int cols, uint8_t* q, float* scale,
+                        cudaStream_t s);
+size_t gemv_e4m3_scratch_bytes(int N, int K, int B);
+nc_status gemv_e4m3(const uint8_t* wq, const float* w_scale, int N, int K, const float* x, int B,
+                    float* y, void* scratch, cudaStream_t s);
 nc_status tc_gemm_f32out(const void* A, const void* B, float* C, int M, int N, int K, nc_dtype dt,
                          cudaStream_t s);
 

@@ -48,6 +48,8 @@ struct GemmArgs {
   uint32_t* status;
   int stream_k;            // 1: CTAs take equal contiguous ranges of (tile, k block)
   int sk_groups;           // > 1 (stream-K): one group of CTAs per n block, see Sched
+  const float* row_scale;  // EPI_SWAP with 8-bit operands: scale of each A row (feature)
+  const float* tok_scale;  // and of each B row (token); NULL for 16-bit operands
 };
 
 // Work schedule shared by the three roles of a CTA: a sequence of segments
@@ -312,6 +314,8 @@ template <int BN>
 __device__ __forceinline__ void epi_swap(const GemmArgs& p, uint32_t taddr, int f, int nb, int ks) {
   const bool valid = f < p.M;
   float* base = p.out_f32 + (int64_t)ks * p.split_stride + f;
+  // 8-bit operands: the codes' product times the feature's and the token's scale
+  const float rs = (p.row_scale && valid) ? p.row_scale[f] : 1.f;
 #pragma unroll 1
   for (int c = 0; c < BN / 16; ++c) {
     float v[16];
@@ -319,7 +323,7 @@ __device__ __forceinline__ void epi_swap(const GemmArgs& p, uint32_t taddr, int 
 #pragma unroll
     for (int i = 0; i < 16; ++i) {
       const int tok = nb * BN + c * 16 + i;
-      if (valid && tok < p.N) base[(int64_t)tok * p.ldo] = v[i];
+      if (valid && tok < p.N) base[(int64_t)tok * p.ldo] = p.tok_scale ? v[i] * rs * p.tok_scale[tok] : v[i];
     }
   }
 }
@@ -390,12 +394,13 @@ __global__ void __launch_bounds__(192, 1)
           mbar_arrive_expect_tx(&full[stage], C::kStageBytes);
           int local;
           const CUtensorMap* ma = pick_map(&tmA0, &tmA1, &tmA2, mb * 128, p.a_split0, p.a_split1, local);
-          tma_load_2d(sa, ma, &full[stage], kb * 64, local);
+          constexpr int kElemsPerRow = 128 / (int)sizeof(T16);   // one 128-byte swizzle row
+          tma_load_2d(sa, ma, &full[stage], kb * kElemsPerRow, local);
 #pragma unroll
           for (int h = 0; h < BN / C::kBoxRowsB; ++h) {
             const CUtensorMap* mb_ = pick_map(&tmB0, &tmB1, &tmB2, nb * BN + h * C::kBoxRowsB,
                                               p.b_split0, p.b_split1, local);
-            tma_load_2d(sb + h * C::kBoxRowsB * 128, mb_, &full[stage], kb * 64, local);
+            tma_load_2d(sb + h * C::kBoxRowsB * 128, mb_, &full[stage], kb * kElemsPerRow, local);
           }
           if (++stage == S) {
             stage = 0;
@@ -444,7 +449,7 @@ __global__ void __launch_bounds__(192, 1)
           const uint32_t b_addr = a_addr + C::kABytes;
 #pragma unroll
           for (int k = 0; k < 4; ++k) {
-            mma_f16kind_ss(d_tmem, sdesc_kmajor_sw128(a_addr + k * 32),
+            mma_ss<T16>(d_tmem, sdesc_kmajor_sw128(a_addr + k * 32),
                         sdesc_kmajor_sw128(b_addr + k * 32), kIdesc, (kb > kb0 || k > 0) ? 1u : 0u);
           }
           mma_commit(&empty[stage]);
@@ -480,10 +485,10 @@ __global__ void __launch_bounds__(192, 1)
       tc_fence_after();
       const int row = mb * 128 + quarter * 32 + lane;
       const uint32_t taddr = tmem_base + ((uint32_t)(quarter * 32) << 16) + acc * BN;
-      if (EPI == EPI_QKV)
-        epi_qkv<BN, T16>(p, taddr, row, nb);
-      else if (EPI == EPI_SWAP)
+      if constexpr (EPI == EPI_SWAP)
         epi_swap<BN>(p, taddr, row, nb, ks);
+      else if constexpr (EPI == EPI_QKV)
+        epi_qkv<BN, T16>(p, taddr, row, nb);
       else
         epi_store_rows<BN, T16>(p, taddr, epi_stage + quarter * 32 * C::kEpiStride,
                                 mb * 128 + quarter * 32, nb, EPI);
@@ -530,17 +535,19 @@ static EncodeTiledFn encode_fn() {
 template <class T16> struct MapType;
 template <> struct MapType<bf16> { static constexpr CUtensorMapDataType v = CU_TENSOR_MAP_DATA_TYPE_BFLOAT16; };
 template <> struct MapType<f16> { static constexpr CUtensorMapDataType v = CU_TENSOR_MAP_DATA_TYPE_FLOAT16; };
+template <> struct MapType<e4m3> { static constexpr CUtensorMapDataType v = CU_TENSOR_MAP_DATA_TYPE_UINT8; };
 
-// Row-major 16-bit matrix [rows, cols] viewed as 2D (x = column, y = row); box of
-// 64 columns (128 bytes, the swizzle width) by box_rows rows.
+// Row-major matrix [rows, cols] of 16- or 8-bit elements viewed as 2D (x =
+// column, y = row); box of 128 bytes of columns (the swizzle width: 64 16-bit or
+// 128 8-bit elements) by box_rows rows.
 template <class T16>
 static bool make_map(CUtensorMap* map, const void* base, uint64_t rows, uint64_t cols,
                      uint32_t box_rows) {
   EncodeTiledFn fn = encode_fn();
   if (!fn) return false;
   cuuint64_t dims[2] = {cols, rows};
-  cuuint64_t strides[1] = {cols * 2};
-  cuuint32_t box[2] = {64, box_rows};
+  cuuint64_t strides[1] = {cols * sizeof(T16)};
+  cuuint32_t box[2] = {128 / (uint32_t)sizeof(T16), box_rows};
   cuuint32_t estr[2] = {1, 1};
   return fn(map, MapType<T16>::v, 2, const_cast<void*>(base), dims, strides, box, estr,
             CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B,
@@ -849,6 +856,107 @@ nc_status tc_lm_head(TcModel* t, const void* xn, int64_t M, float* logits, float
                      cudaStream_t s) {
   (void)part;
   return t->f16 ? lm_impl<f16>(t, xn, M, logits, s) : lm_impl<bf16>(t, xn, M, logits, s);
+}
+
+// ------------------------------------------------- fp8 (E4M3) projections
+static size_t align256(size_t x) { return (x + 255) / 256 * 256; }
+
+// One CTA per row: scale = max|x[r, :]| / 448 (1 for a zero row) and the codes
+// E4M3(x / scale), rounded to nearest even and saturating, two per conversion.
+// The division is IEEE (the rounding decision matches a float32 reference).
+template <class TI>
+__global__ void quantize_e4m3_kernel(const TI* __restrict__ x, int64_t rows, int cols,
+                                     uint8_t* __restrict__ q, float* __restrict__ scale) {
+  __shared__ float red[32];
+  const int64_t r = blockIdx.x;
+  if (r >= rows) return;
+  const TI* xr = x + r * cols;
+  float amax = 0.f;
+  for (int c = threadIdx.x; c < cols; c += blockDim.x) amax = fmaxf(amax, fabsf(to_f32(xr[c])));
+#pragma unroll
+  for (int o = 16; o > 0; o >>= 1) amax = fmaxf(amax, __shfl_xor_sync(0xffffffffu, amax, o));
+  if (threadIdx.x % 32 == 0) red[threadIdx.x / 32] = amax;
+  __syncthreads();
+  if (threadIdx.x < 32) {
+    float m = threadIdx.x < blockDim.x / 32 ? red[threadIdx.x] : 0.f;
+#pragma unroll
+    for (int o = 16; o > 0; o >>= 1) m = fmaxf(m, __shfl_xor_sync(0xffffffffu, m, o));
+    if (threadIdx.x == 0) red[0] = m;
+  }
+  __syncthreads();
+  amax = red[0];
+  const float s = amax > 0.f ? __fdiv_rn(amax, 448.f) : 1.f;
+  if (threadIdx.x == 0) scale[r] = s;
+  uint8_t* qr = q + r * cols;
+  for (int c = 2 * threadIdx.x; c < cols; c += 2 * blockDim.x) {
+    const float a = __fdiv_rn(to_f32(xr[c]), s), b = __fdiv_rn(to_f32(xr[c + 1]), s);
+    *reinterpret_cast<__nv_fp8x2_storage_t*>(qr + c) =
+        __nv_cvt_float2_to_fp8x2(make_float2(a, b), __NV_SATFINITE, __NV_E4M3);
+  }
+}
+
+nc_status quantize_e4m3(const void* x, nc_dtype dt, int64_t rows, int cols, uint8_t* q, float* scale,
+                        cudaStream_t s) {
+  if (rows == 0) return NC_OK;
+  const dim3 grid((unsigned)rows), block(256);
+  if (dt == NC_F32)
+    quantize_e4m3_kernel<float><<<grid, block, 0, s>>>((const float*)x, rows, cols, q, scale);
+  else if (dt == NC_BF16)
+    quantize_e4m3_kernel<bf16><<<grid, block, 0, s>>>((const bf16*)x, rows, cols, q, scale);
+  else
+    quantize_e4m3_kernel<f16><<<grid, block, 0, s>>>((const f16*)x, rows, cols, q, scale);
+  count_launches(1);
+  return cudaGetLastError() == cudaSuccess ? NC_OK : NC_ERR_CUDA;
+}
+
+size_t gemv_e4m3_scratch_bytes(int N, int K, int B) {
+  const int BN = swap_bn(B);
+  const size_t xq = align256((size_t)BN * K), xs = 512;
+  const size_t part = (size_t)kMaxSplits * B * N * 4;
+  return xq + xs + part;
+}
+
+// y[t, n] = w_scale[n] * s_t * sum_k wq[n, k] * E4M3(x[t, k] / s_t): the activations
+// are quantised per token into the scratch, then the swap-mode tcgen05 GEMM
+// (kind::f8f6f4, features as M, tokens as N, split over K) writes scaled partial
+// sums that one pass adds.
+nc_status gemv_e4m3(const uint8_t* wq, const float* w_scale, int N, int K, const float* x, int B,
+                    float* y, void* scratch, cudaStream_t s) {
+  const int BN = swap_bn(B);
+  uint8_t* xq = static_cast<uint8_t*>(scratch);
+  float* xs = reinterpret_cast<float*>(xq + align256((size_t)BN * K));
+  float* part = xs + 128;
+  // token rows past B are read by the tile: zero codes
+  if (BN > B && cudaMemsetAsync(xq + (size_t)B * K, 0, (size_t)(BN - B) * K, s) != cudaSuccess)
+    return NC_ERR_CUDA;
+  nc_status st = quantize_e4m3(x, NC_F32, B, K, xq, xs, s);
+  if (st != NC_OK) return st;
+  CUtensorMap a, b;
+  if (!make_map<e4m3>(&a, wq, (uint64_t)N, (uint64_t)K, 128) ||
+      !make_map<e4m3>(&b, xq, (uint64_t)BN, (uint64_t)K, BN))
+    return NC_ERR_CUDA;
+  const int sm = sm_count_now();
+  GemmArgs args = base_args(N, B, K, BN, nullptr);
+  if (cudaGetSymbolAddress(reinterpret_cast<void**>(&args.status), g_op_status) != cudaSuccess)
+    return NC_ERR_CUDA;
+  args.num_k_blk = K / 128;   // 128 one-byte elements per 128-byte row of a stage
+  args.k_per_split = args.num_k_blk;
+  plan_splits(args, sm);
+  args.num_n_blk = 1;
+  args.out_f32 = part;
+  args.ldo = N;
+  args.split_stride = (int64_t)B * N;
+  args.row_scale = w_scale;
+  args.tok_scale = xs;
+  if (BN == 32)
+    st = launch_gemm<32, EPI_SWAP, e4m3>(a, a, a, b, b, b, args, sm, s);
+  else if (BN == 64)
+    st = launch_gemm<64, EPI_SWAP, e4m3>(a, a, a, b, b, b, args, sm, s);
+  else
+    st = launch_gemm<128, EPI_SWAP, e4m3>(a, a, a, b, b, b, args, sm, s);
+  if (st != NC_OK) return st;
+  launch_sum_splits(part, args.k_splits, y, B, N, N, s);
+  return cudaGetLastError() == cudaSuccess ? NC_OK : NC_ERR_CUDA;
 }
 
 nc_status tc_gemm_f32out(const void* A, const void* B, float* C, int M, int N, int K,
