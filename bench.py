@@ -653,6 +653,47 @@ def run_op_attention(args):
           f"{flop / (ms / 1e3) / 1e12:.0f} TFLOP/s", flush=True)
 
 
+def run_op_gemv_fp8(args):
+    """Profiling aid: the fp8 (E4M3) projection variant alone, through the C ABI, at
+    the d20 decode shapes with 32 tokens: FC (5120 x 1280), PROJ (1280 x 5120) and
+    the LM head (65536 x 1280). Seeded N(0, 1/sqrt(K)) weights quantised once, N(0, 1)
+    activations. Each call quantises the activations, runs the tcgen05 kind::f8f6f4
+    product and adds the split-K partials. Prints the time per call and the rate of
+    its bytes (1-byte weights, fp32 activations and output) against the measured HBM
+    bandwidth."""
+    import numpy as np
+    import torch
+    from transformer_forward_gpt_b300 import binding as nc
+    peaks, src = load_peaks()
+    B = 32
+    rng = np.random.default_rng(0)
+    for name, N, K in (("FC", 5120, 1280), ("PROJ", 1280, 5120), ("LM head", 65536, 1280)):
+        w = torch.from_numpy((rng.standard_normal((N, K)) / np.sqrt(K)).astype(np.float32)).cuda()
+        wq = torch.empty(N, K, dtype=torch.uint8, device="cuda")
+        ws = torch.empty(N, dtype=torch.float32, device="cuda")
+        nc.nc_op_quantize_e4m3(w, nc.NC_F32, N, K, wq, ws)
+        del w
+        x = torch.randn(B, K, device="cuda")
+        y = torch.empty(B, N, device="cuda")
+        nbytes = nc.nc_op_gemv_e4m3_scratch_bytes(N, K, B)
+        scratch = torch.empty(nbytes, dtype=torch.uint8, device="cuda")
+        for _ in range(max(3, args.warmup)):
+            nc.nc_op_gemv_e4m3(wq, ws, N, K, x, B, y, scratch, nbytes)
+        torch.cuda.synchronize()
+        e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+        e0.record()
+        for _ in range(args.steps):
+            nc.nc_op_gemv_e4m3(wq, ws, N, K, x, B, y, scratch, nbytes)
+        e1.record()
+        torch.cuda.synchronize()
+        us = e0.elapsed_time(e1) / args.steps * 1e3
+        byts = N * K + 4 * N + 4 * B * K + 4 * B * N
+        gbs = byts / (us / 1e6) / 1e9
+        print(f"profiling aid: fp8 GEMV {name} {N}x{K}, {B} tokens: {us:.1f} us per call, "
+              f"{gbs:.0f} GB/s = {gbs / peaks['hbm_gbs']:.2f} of {src} HBM "
+              f"(16-bit weights would be {2 * N * K / 1e6:.1f} MB, fp8 {N * K / 1e6:.1f} MB)", flush=True)
+
+
 def main():
     ap = argparse.ArgumentParser(description=__doc__.splitlines()[0])
     ap.add_argument("--gpus", type=int, default=1)
@@ -669,7 +710,7 @@ def main():
                     help="profiling aid: smaller prefill batch (no JSON line)")
     ap.add_argument("--decode-steps", type=int, default=None,
                     help="profiling aid: fewer decode steps per step (no JSON line)")
-    ap.add_argument("--op", choices=("attention",), default=None,
+    ap.add_argument("--op", choices=("attention", "gemv-fp8"), default=None,
                     help="profiling aid: time one kernel on its own (no JSON line)")
     ap.add_argument("--cpu-budget", type=float, default=30.0)
     args = ap.parse_args()
@@ -679,6 +720,8 @@ def main():
         run_reference(args)
     elif args.op == "attention":
         run_op_attention(args)
+    elif args.op == "gemv-fp8":
+        run_op_gemv_fp8(args)
     else:
         run_ours(args)
 
