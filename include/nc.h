@@ -201,8 +201,8 @@ NC_API nc_status nc_decode_step(nc_model* m, const int32_t* tokens, int32_t B, i
  * The persistent kernel runs a whole decode step for up to 32 sequences as one
  * cooperative launch with one CTA per SM: a producer warp streams every weight
  * matrix (packed once, on first use, into a model-owned copy of 16 KB units in
- * the tensor core's swizzled layout) and the KV cache through shared memory, an
- * MMA warp runs the projections on tcgen05, and the other warps compute the
+ * the tensor core's swizzled layout) and the KV cache through shared memory, two
+ * MMA threads run the projections on tcgen05, and eight warps compute the
  * phases of the step between grid-wide barriers. Larger batches run as
  * several launches of up to 32 sequences. Projection partial sums are added in
  * fp32 in a run-dependent order. The fp32 path always uses kernels. */
@@ -435,9 +435,9 @@ NC_API int64_t nc_launch_count(void);
  * the activations, 0 when that is done, 1 when an accumulator has been read from
  * tensor memory and 2 after adding its partial sums (per row group; the last one
  * stays); attention records m = 0 after preparing q, 1 after the key tiles, 2
- * after writing its partial state and 3 at the end, for each (sequence, KV
- * head) it covers (later segments overwrite earlier ones; unused marks stay as
- * they were); m = 4 is when CTA 0's producer started loading the phase's weights
+ * after adding its weighted softmax sums and 3 at the end, for each round of
+ * (sequence, KV head) pairs it covers (later rounds overwrite earlier ones;
+ * unused marks stay as they were); m = 4 is when CTA 0's producer started loading the phase's weights
  * or K/V tiles; m = 5 is unused. After those 8 * nbar + 2 entries, every CTA c < 256 of the launch
  * records, for barrier k, its arrival and exit time at 8 * nbar + 2 + 2 * (256 * (k - 1) + c)
  * (+ 1). capacity must be at least nc_decode_trace_entries(cfg), else nothing is

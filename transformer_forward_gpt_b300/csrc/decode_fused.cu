@@ -5,7 +5,7 @@
 // cached K/V row once, and each of them is used by only B <= 32 tokens. With one
 // kernel per projection the step pays a launch, a ramp and a tail per kernel
 // (about 180 of them for a 20-layer model), which costs more than the streaming
-// itself. Here one CTA per SM runs the whole step with three roles:
+// itself. Here one CTA per SM runs the whole step with four roles:
 //
 //   warp 0 (producer)   one thread streams the CTA's share of every weight
 //                       matrix (pre-swizzled 16 KB units, 1-D bulk copies) and of
@@ -13,12 +13,13 @@
 //                       swizzle) into a ring of 16 KB stages. Nothing it loads
 //                       depends on the step's activations, so it runs ahead
 //                       across the grid barriers of the phases.
-//   warp 1 (MMA)        allocates 64 TMEM columns (two 128 x 32 fp32
-//                       accumulators); one thread issues tcgen05.mma for every
-//                       weight unit of the projection phases: the unit's 128
-//                       weight rows are the A operand (M = 128), the 32 token rows
-//                       staged by the consumers the B operand (N = 32), fp32
-//                       accumulation in TMEM over the CTA's K range.
+//   warps 1 and 10      the MMA issuers (one thread each; warp 1 allocates the
+//                       TMEM): tcgen05.mma for every weight unit of the
+//                       projection phases, the unit's 128 weight rows the A
+//                       operand (M = 128), the 32 token rows staged by the
+//                       consumers the B operand (N = 32), fp32 accumulation in
+//                       TMEM over the CTA's K range. Issuer i takes the units at
+//                       ring positions of parity i (see mma_gemv).
 //   warps 2..9          consumers, phase by phase, separated by grid barriers:
 //     P0       embedding x = wte[token]; zero the accumulators of the step
 //     per layer:
@@ -27,9 +28,10 @@
 //              that cover feature group 0 also sum x^2 for that scale
 //       ATTN   RoPE + QK norm of q and of the new k, cache write of the new
 //              k / v, split-KV attention over positions 0..pos (all query heads
-//              of a KV head share one pass over K/V); each CTA writes one
-//              partial softmax state per (sequence, query head) it covers
-//       O      x += att Wo^T, the partial states merged while staging att
+//              of a KV head share one pass over K/V); each CTA adds its
+//              softmax sums, weighted against a fixed reference, into
+//              accumulators that the CTAs of a (sequence, KV head) share
+//       O      x += att Wo^T, att = numerators / denominators while staging
 //       FC     hacc = x Wfc^T (un-normalised, sum of x^2 as in QKV)
 //       PROJ   x += relu(r hacc)^2 Wproj^T
 //     FNORM    xn = RMSNorm(x), written as the B operand image of the LM head
@@ -41,8 +43,8 @@
 // reads). Units are ordered row-group-major and each CTA takes an equal
 // contiguous range of them, so every CTA streams the same number of bytes. The
 // consumers first stage the 64-column chunks of the activations the range needs
-// (32 token rows, 16-bit, same swizzle); the MMA thread then runs the range,
-// one accumulator per row group it touches; the consumers read each finished
+// (32 token rows, 16-bit, same swizzle); the MMA issuers then run the range,
+// one accumulator per issuer and row group it touches; the consumers read each finished
 // accumulator from TMEM and add it into the fp32 output with reductions.
 // Projection outputs therefore sum in a run-dependent order (fp32).
 #include <math.h>
@@ -253,7 +255,7 @@ struct Shared {
   uint64_t* acc_full;    // [2] accumulator ready (tcgen05.commit)
   uint64_t* acc_empty;   // [2] accumulator read by the consumers (8 arrivals)
   uint64_t* b_full;      // B chunks staged (8 arrivals)
-  uint64_t* fin;         // the MMA thread's last commit
+  uint64_t* fin;         // the MMA issuers' last commits (2 arrivals)
   uint32_t* tmem_slot;
   volatile int* flag;    // [2] barrier ok
 };
@@ -764,7 +766,7 @@ __device__ void stage_b(const Params& p, const Shared& sh, const Gemv& g, const 
 }
 
 // Consumer side of a projection phase: stage the B chunks, then read every
-// accumulator the MMA thread finishes and add it into the output. Warp w of the
+// accumulator the MMA issuers finish and add it into the output. Warp w of the
 // consumers reads TMEM lane quarter (w + 2) % 4 (the quarter its CTA warp index
 // may access) and token columns 16 * (w / 4) .. + 15.
 template <class T16>
