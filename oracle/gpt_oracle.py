@@ -31,7 +31,9 @@ What it computes, in the order the pages give it:
   (jxzklqfsx.com, the KV cache paragraph; CSDN nanochat article,
   wap.jaobe.com, the Engine paragraph with prefill and decode);
 * greedy next token: argmax of the logits, lowest index on ties (Microgpt
-  summary, 推理 section; greedy is the zero-temperature limit).
+  summary, 推理 section; greedy is the zero-temperature limit);
+* the training step's loss: the cross-entropy between each position's predicted
+  distribution and the true next token (Microgpt summary, 训练过程 item 2).
 
 Readings where the pages are silent: eps = cfg["rms_eps"] (1e-5 in the
 workloads); attention scale 1/sqrt(head_dim); RoPE rotates the pair
@@ -267,3 +269,28 @@ def sample_temperature(logits, temperature, u):
         k = int(np.searchsorted(cdf[b], u[b], side="right"))
         out[b] = min(k, logits.shape[1] - 1)
     return out
+
+
+def cross_entropy(logits, targets):
+    """Next-token loss of each row and their mean (Microgpt summary, 训练过程
+    item 2: the cross-entropy between the model's prediction and the true token,
+    a measure of how surprised the model is).
+
+    loss[r] = -log p_r[targets[r]] with p_r = softmax(logits[r]) (核心架构 item 2),
+    written as log(sum_v exp(z[r, v] - m_r)) + m_r - z[r, targets[r]] with m_r the
+    row max, so that no exponential overflows. Reading where the pages are
+    silent: a row whose target is negative is ignored (loss 0, not counted in the
+    mean). Returns (loss [R], mean over counted rows; NaN if none counts).
+    """
+    z = np.asarray(logits, dtype=F64)
+    t = np.asarray(targets).reshape(-1)
+    assert z.ndim == 2 and z.shape[0] == t.shape[0]
+    keep = t >= 0
+    assert np.all(t[keep] < z.shape[1])
+    m = z.max(axis=1)
+    lse = np.log(np.sum(np.exp(z - m[:, None]), axis=1)) + m
+    loss = np.zeros(z.shape[0], dtype=F64)
+    rows = np.nonzero(keep)[0]
+    loss[rows] = lse[rows] - z[rows, t[rows]]
+    mean = float(np.sum(loss[rows]) / len(rows)) if len(rows) else float("nan")
+    return loss, mean

@@ -337,3 +337,56 @@ def test_prefill_in_chunks_equals_one_prefill():
         np.testing.assert_allclose(cache.k[l], fcache.k[l], rtol=0, atol=1e-12)
         np.testing.assert_allclose(cache.v[l], fcache.v[l], rtol=0, atol=1e-12)
     assert cache.length == 9
+
+
+# ----------------------------------------------------------- cross-entropy loss
+def test_cross_entropy_two_classes_by_hand():
+    """z = (0, ln 3): p = (1/4, 3/4), so the loss is ln 4 for target 0 and
+    ln(4/3) for target 1."""
+    z = np.array([[0.0, math.log(3.0)], [0.0, math.log(3.0)]])
+    loss, mean = O.cross_entropy(z, np.array([0, 1]))
+    assert abs(loss[0] - math.log(4.0)) < 1e-15
+    assert abs(loss[1] - math.log(4.0 / 3.0)) < 1e-15
+    assert abs(mean - (math.log(4.0) + math.log(4.0 / 3.0)) / 2) < 1e-15
+
+
+def test_cross_entropy_of_uniform_logits_is_ln_v():
+    for V in (2, 27, 1000, 65536):
+        z = np.full((3, V), 1.7)
+        loss, _ = O.cross_entropy(z, np.array([0, V // 2, V - 1]))
+        assert np.allclose(loss, math.log(V), rtol=0, atol=1e-12)
+
+
+def test_cross_entropy_matches_minus_log_probability_brute_force():
+    """Pure-Python loops: p = exp(z_t) / sum exp(z_v), loss = -log p."""
+    rng = np.random.default_rng(31)
+    z = rng.standard_normal((6, 9)) * 3
+    t = rng.integers(0, 9, size=6)
+    loss, mean = O.cross_entropy(z, t)
+    want = []
+    for r in range(6):
+        den = sum(math.exp(float(v)) for v in z[r])
+        want.append(-math.log(math.exp(float(z[r, t[r]])) / den))
+    assert np.allclose(loss, want, rtol=1e-13, atol=0)
+    assert abs(mean - sum(want) / 6) < 1e-13
+
+
+def test_cross_entropy_shift_invariance_and_no_overflow():
+    rng = np.random.default_rng(32)
+    z = rng.standard_normal((4, 50))
+    t = rng.integers(0, 50, size=4)
+    a, _ = O.cross_entropy(z, t)
+    b, _ = O.cross_entropy(z + np.array([[1000.0], [-1000.0], [3.5], [0.0]]), t)
+    assert np.allclose(a, b, rtol=0, atol=1e-10)
+    # a dominant logit: about 0 for its own target, about the gap for another
+    big, _ = O.cross_entropy(np.array([[1000.0, 0.0], [1000.0, 0.0]]), np.array([0, 1]))
+    assert big[0] == 0.0 and big[1] == 1000.0
+
+
+def test_cross_entropy_ignores_negative_targets():
+    z = np.array([[0.0, math.log(3.0)], [5.0, -2.0], [1.0, 1.0]])
+    loss, mean = O.cross_entropy(z, np.array([1, -1, 0]))
+    assert loss[1] == 0.0
+    assert abs(mean - (math.log(4.0 / 3.0) + math.log(2.0)) / 2) < 1e-15
+    _, none = O.cross_entropy(z, np.array([-1, -1, -1]))
+    assert math.isnan(none)
