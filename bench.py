@@ -381,8 +381,11 @@ def report_configs(nc, synth, peaks, peak_src, dev, stream, reps=5):
     the headline step (CUDA events on the launching stream, warm-up first):
     d12 and d26 prefill (all logits) with their tensor-roofline fractions, d26
     KV-cache decode (B64, 64 steps at context 2048..2111) with its HBM fraction,
-    and the headline d20 prefill with literal bf16 activations and KV cache
-    (act_dtype bf16) beside the default fp16 operands. Inputs are larger than L2."""
+    the headline d20 prefill with literal bf16 activations and KV cache
+    (act_dtype bf16) beside the default fp16 operands, and the d20 prefill with
+    the training step's next-token loss in place of the logits. Inputs are larger
+    than L2."""
+    import numpy as np
     import torch
     out = {}
 
@@ -415,6 +418,37 @@ def report_configs(nc, synth, peaks, peak_src, dev, stream, reps=5):
                     "frac_of_peak": round(tf / peaks["bf16_tflops"], 4),
                     "peak": peaks["bf16_tflops"], "peak_source": f"{peak_src} bf16", "operands": note}
         del logits, tok
+        c.close()
+        m.close()
+        torch.cuda.empty_cache()
+
+    def loss_case():
+        # the training step's forward pass and loss: the prefill with the LM head
+        # reduced to per-position cross-entropy in its epilogue (no logits stored)
+        wl = synth.WORKLOADS["d20_prefill"]
+        sh, B, T = wl.shape, wl.batch, wl.seq
+        W = synth.make_weights(sh)
+        m = nc.Model(W, max_seq=T, max_batch=B)
+        del W
+        c = m.cache(B, T)
+        toks = synth.make_tokens(sh, B, T)
+        tgt = np.concatenate([toks[:, 1:], toks[:, :1]], axis=1)
+        tok = torch.from_numpy(toks).to(dev)
+        tgt_d = torch.from_numpy(np.ascontiguousarray(tgt)).to(dev)
+        loss = torch.empty(B * T, device=dev)
+        mean = torch.empty(1, device=dev)
+        ms = timed(lambda: nc.nc_prefill_loss(m.handle, tok, tgt_d, B, T, loss, mean, c.handle, stream),
+                   reps)
+        g, a = prefill_flops(sh, B, T)
+        tf = (g + a) / (ms / 1e3) / 1e12
+        out["d20_prefill_loss"] = {"workload": f"{sh.name} prefill + next-token loss B{B}xT{T}",
+                                   "tok_s": round(B * T / (ms / 1e3), 1), "ms": round(ms, 3),
+                                   "tflops": round(tf, 1), "frac_of_peak": round(tf / peaks["bf16_tflops"], 4),
+                                   "peak": peaks["bf16_tflops"], "peak_source": f"{peak_src} bf16",
+                                   "mean_loss": round(float(mean.item()), 4),
+                                   "logits_stored": False}
+        if nc.nc_model_check(m.handle) != nc.NC_OK:
+            raise RuntimeError("device status set during the loss configuration")
         c.close()
         m.close()
         torch.cuda.empty_cache()
@@ -464,6 +498,7 @@ def report_configs(nc, synth, peaks, peak_src, dev, stream, reps=5):
     guarded("d26_prefill", prefill_case, "d26_prefill", "d26_prefill", nc.NC_F16, "fp16 (bf16 weights)")
     guarded("d20_prefill_bf16_mode", prefill_case, "d20_prefill_bf16_mode", "d20_prefill", nc.NC_BF16,
             "bf16 activations and KV cache")
+    guarded("d20_prefill_loss", loss_case)
     guarded("d26_decode", decode_case)
     return out
 

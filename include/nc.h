@@ -56,7 +56,8 @@ typedef enum {
     NC_ERR_CUDA = 4,            /* a CUDA runtime/driver call failed */
     NC_ERR_DEVICE_TIMEOUT = 5,  /* a kernel's bounded wait ran out (device status word) */
     NC_ERR_BOUNDS = 6,          /* a token id outside [0, vocab) was seen (device status word);
-                                   the kernel used row 0 in its place */
+                                   the kernel used row 0 in its place (an input token) or
+                                   left the row out (a loss target >= vocab) */
     NC_ERR_RANGE = 7            /* a value stored in fp16 (act_dtype NC_F16) was too large for
                                    it and became +-inf (device status word): the V rows of the
                                    KV cache, the ReLU^2 activations, or the decode step's
@@ -180,6 +181,28 @@ NC_API nc_status nc_prefill_continue(nc_model* m, const int32_t* tokens, int32_t
  * may be NULL; the greedy next token, lowest index on ties). */
 NC_API nc_status nc_prefill_last(nc_model* m, const int32_t* tokens, int32_t B, int32_t T,
                                  float* logits_last, int32_t* argmax_out, nc_kv_cache* c,
+                                 void* stream);
+
+/* Loss of a training step's forward pass (Microgpt summary, section 训练过程,
+ * item 2: every position predicts the next token, and the loss is the
+ * cross-entropy between that prediction and the true token). Runs the prefill of
+ * nc_prefill over tokens (dev int32 [B, T]) and, per position r = b * T + t,
+ *   loss[r] = log(sum_v exp(z[r, v])) - z[r, targets[r]],  z = that position's logits,
+ * with the mean over the counted positions in *mean (dev fp32 [1]; NaN if none
+ * counts). targets (dev int32 [B, T]): the true next token of each position; a
+ * negative target leaves the position out (loss 0, not counted); a target >=
+ * vocab does the same and sets NC_ERR_BOUNDS in the status word (nc_model_check).
+ * loss (dev fp32 [B, T]) may be NULL. The logits are never stored: the LM-head
+ * GEMM's epilogue reduces each row's 256-column blocks to (max, sum of exp) and
+ * keeps the target's logit. The cache is written as by nc_prefill and is the
+ * caller's. A model-owned scratch of B*T*(8*ceil(vocab/256) + 8) bytes is
+ * allocated on the first call (and again for a larger B*T). The mean is summed in a
+ * fixed order; the losses follow the projections' fp32 sums. Bounds as
+ * nc_prefill; NC_ERR_INVALID_ARG for NULL targets or mean or pointers that are not
+ * 4-byte aligned; NC_ERR_UNSUPPORTED for an fp32 model; NC_ERR_OOM if the scratch
+ * cannot be allocated. */
+NC_API nc_status nc_prefill_loss(nc_model* m, const int32_t* tokens, const int32_t* targets,
+                                 int32_t B, int32_t T, float* loss, float* mean, nc_kv_cache* c,
                                  void* stream);
 
 /* One decode step: token (dev int32 [B]) of each sequence at position pos, which
@@ -383,6 +406,29 @@ NC_API nc_status nc_op_sample(const float* logits, int32_t rows, int32_t n, floa
  * NC_ERR_INVALID_ARG for NULL or misaligned pointers or bad sizes. */
 NC_API nc_status nc_op_quantize_e4m3(const void* x, nc_dtype dtype, int64_t rows, int32_t cols,
                                      uint8_t* q, float* scale, void* stream);
+
+/* ------------------------------------------------------------------------
+ * Next-token loss of a matrix product (the LM head of nc_prefill_loss as a
+ * single step). Microgpt summary, section 训练过程, item 2.
+ * ---------------------------------------------------------------------- */
+
+/* Device scratch that nc_op_cross_entropy needs for M rows and N columns. */
+NC_API size_t nc_op_cross_entropy_scratch_bytes(int32_t M, int32_t N);
+
+/* loss[r] = log(sum_n exp(z[r, n])) - z[r, targets[r]] for z = A B^T (A dev
+ * [M, K], B dev [N, K], both dtype NC_BF16 or NC_F16, row-major, fp32
+ * accumulation on tcgen05), and *mean the mean over the rows counted. A row whose
+ * target (dev int32 [M]) is outside [0, N) is left out (loss 0). The product is
+ * reduced in the GEMM's epilogue per row and block of 256 columns; z is never
+ * stored. loss dev fp32 [M] or NULL; mean dev fp32 [1] (NaN if no row counts);
+ * scratch dev of at least nc_op_cross_entropy_scratch_bytes(M, N) bytes, owned by
+ * the caller. K % 64 == 0 (N is free); A, B and scratch 16-byte aligned.
+ * Errors: NC_ERR_INVALID_ARG for NULL or misaligned pointers, bad sizes or dtype,
+ * or a small scratch; NC_ERR_UNSUPPORTED for K not a multiple of 64. */
+NC_API nc_status nc_op_cross_entropy(const void* A, const void* B, const int32_t* targets,
+                                     int32_t M, int32_t N, int32_t K, nc_dtype dtype, float* loss,
+                                     float* mean, void* scratch, size_t scratch_bytes,
+                                     void* stream);
 
 /* Device scratch that nc_op_gemv_e4m3 needs for N features, K inputs, B tokens. */
 NC_API size_t nc_op_gemv_e4m3_scratch_bytes(int32_t N, int32_t K, int32_t B);

@@ -28,6 +28,7 @@ EXPORTS = (
     "nc_decode_trace_entries", "nc_op_sample", "nc_prefill_continue",
     "nc_decode_step_ragged", "nc_kv_cache_set_lengths", "nc_kv_cache_lengths",
     "nc_decode_step_sample", "nc_generate_host_sample", "nc_op_quantize_e4m3",
+    "nc_prefill_loss", "nc_op_cross_entropy_scratch_bytes", "nc_op_cross_entropy",
     "nc_op_gemv_e4m3_scratch_bytes", "nc_op_gemv_e4m3",
 )
 
@@ -82,6 +83,10 @@ def load(path: str = LIB_PATH):
         "nc_prefill": (C.c_int, [vp, vp, i32, i32, vp, vp, vp]),
         "nc_prefill_continue": (C.c_int, [vp, vp, i32, i32, vp, vp, vp]),
         "nc_prefill_last": (C.c_int, [vp, vp, i32, i32, vp, vp, vp, vp]),
+        "nc_prefill_loss": (C.c_int, [vp, vp, vp, i32, i32, vp, vp, vp, vp]),
+        "nc_op_cross_entropy_scratch_bytes": (C.c_size_t, [i32, i32]),
+        "nc_op_cross_entropy": (C.c_int, [vp, vp, vp, i32, i32, i32, C.c_int, vp, vp, vp,
+                                          C.c_size_t, vp]),
         "nc_decode_step": (C.c_int, [vp, vp, i32, i32, vp, vp, vp, vp]),
         "nc_generate_host": (C.c_int, [vp, vp, i32, i32, i32, vp, vp, vp]),
         "nc_model_check": (C.c_int, [vp, vp]),
@@ -220,6 +225,22 @@ def nc_prefill_continue(model, tokens, B, T, logits, cache, stream=None):
 def nc_prefill_last(model, tokens, B, T, logits_last, argmax_out, cache, stream=None):
     _check(load().nc_prefill_last(model, _ptr(tokens), B, T, _ptr(logits_last), _ptr(argmax_out),
                                   cache, _stream(stream)), "nc_prefill_last")
+
+
+def nc_op_cross_entropy_scratch_bytes(M, N):
+    return load().nc_op_cross_entropy_scratch_bytes(M, N)
+
+
+def nc_op_cross_entropy(A, B, targets, M, N, K, dtype, loss, mean, scratch, scratch_bytes,
+                        stream=None):
+    _check(load().nc_op_cross_entropy(_ptr(A), _ptr(B), _ptr(targets), M, N, K, dtype, _ptr(loss),
+                                      _ptr(mean), _ptr(scratch), scratch_bytes, _stream(stream)),
+           "nc_op_cross_entropy")
+
+
+def nc_prefill_loss(model, tokens, targets, B, T, loss, mean, cache, stream=None):
+    _check(load().nc_prefill_loss(model, _ptr(tokens), _ptr(targets), B, T, _ptr(loss), _ptr(mean),
+                                  cache, _stream(stream)), "nc_prefill_loss")
 
 
 def nc_decode_step(model, tokens, B, pos, logits, argmax_out, cache, stream=None):

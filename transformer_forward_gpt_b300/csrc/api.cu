@@ -142,6 +142,9 @@ struct nc_model {
   float4* d_lm_part = nullptr;  // per-CTA softmax partials of the sampling mode
   float* d_att_num = nullptr;   // attention numerators [2][kMaxTok][H * head_dim]
   float* d_att_den = nullptr;   // and denominators [2][kMaxTok][H]
+  // next-token loss (nc_prefill_loss), allocated on first use for the largest M
+  void* ce_ws = nullptr;
+  size_t ce_ws_bytes = 0;
   unsigned long long bar_base = 0;
   unsigned long long* dec_trace = nullptr;   // caller's buffer (nc_decode_trace)
   int32_t dec_trace_cap = 0;
@@ -262,6 +265,7 @@ void nc_model_destroy(nc_model* m) {
   for (auto e : m->event_pool) cudaEventDestroy(e);
   cudaFree(m->wcopy);
   cudaFree(m->dpack);
+  cudaFree(m->ce_ws);
   cudaFree(m->dws);
   cudaFree(m->ws);
   cudaFree(m->cos_tab);
@@ -862,6 +866,49 @@ nc_status nc_prefill_last(nc_model* m, const int32_t* tokens, int32_t B, int32_t
   return check_launch();
 }
 
+nc_status nc_prefill_loss(nc_model* m, const int32_t* tokens, const int32_t* targets, int32_t B,
+                          int32_t T, float* loss, float* mean, nc_kv_cache* c, void* stream) {
+  nc_status st = check_prefill_args(m, tokens, B, T, c);
+  if (st != NC_OK) return st;
+  NC_CHECK(targets && mean, NC_ERR_INVALID_ARG, "NULL targets or mean");
+  NC_CHECK((reinterpret_cast<uintptr_t>(targets) & 3u) == 0 &&
+               (!loss || (reinterpret_cast<uintptr_t>(loss) & 3u) == 0) &&
+               (reinterpret_cast<uintptr_t>(mean) & 3u) == 0,
+           NC_ERR_INVALID_ARG, "targets, loss and mean must be 4-byte aligned");
+  NC_CHECK(m->adt != NC_F32, NC_ERR_UNSUPPORTED,
+           "the fused loss runs on the tensor-core path (16-bit activations)");
+  const int64_t M = (int64_t)B * T;
+  const int nblk = nc::lm_loss_blocks(m->cfg.vocab);
+  const size_t b_part = round_up((size_t)M * nblk * sizeof(float2), 256),
+               b_row = round_up((size_t)M * sizeof(float), 256);
+  if (b_part + 2 * b_row > m->ce_ws_bytes) {
+    cudaFree(m->ce_ws);
+    m->ce_ws = nullptr;
+    m->ce_ws_bytes = 0;
+    if (cudaMalloc(&m->ce_ws, b_part + 2 * b_row) != cudaSuccess) {
+      cudaGetLastError();
+      m->ce_ws = nullptr;
+      set_err("loss scratch allocation of %zu bytes failed", b_part + 2 * b_row);
+      return NC_ERR_OOM;
+    }
+    m->ce_ws_bytes = b_part + 2 * b_row;
+  }
+  char* ws = static_cast<char*>(m->ce_ws);
+  float2* part = reinterpret_cast<float2*>(ws);
+  float* zt = reinterpret_cast<float*>(ws + b_part);
+  float* rows = loss ? loss : reinterpret_cast<float*>(ws + b_part + b_row);
+  cudaStream_t s = static_cast<cudaStream_t>(stream);
+  st = prefill_common(m, tokens, B, T, c, s);
+  if (st != NC_OK) return st;
+  {
+    ProfScope ps(m, NC_K_LM_HEAD, s);
+    st = nc::tc_lm_loss(m->tc, m->xn, M, targets, part, zt, s);
+    if (st != NC_OK) return st;
+    nc::launch_ce_finish(part, nblk, zt, targets, m->cfg.vocab, M, rows, mean, m->status, s);
+  }
+  return check_launch();
+}
+
 nc_status nc_decode_step(nc_model* m, const int32_t* tokens, int32_t B, int32_t pos,
                          float* logits, int32_t* argmax_out, nc_kv_cache* c, void* stream) {
   NC_CHECK(m && c && tokens, NC_ERR_INVALID_ARG, "NULL model, cache or tokens");
@@ -1107,7 +1154,8 @@ nc_status nc_model_check(nc_model* m, void* stream) {
     return NC_ERR_DEVICE_TIMEOUT;
   }
   if (word & nc::ST_BAD_TOKEN) {
-    set_err("a token id was outside [0, vocab); row 0 was used");
+    set_err("a token id was outside [0, vocab) (an input token: row 0 was used; a loss "
+            "target: the row was left out)");
     return NC_ERR_BOUNDS;
   }
   if (word & nc::ST_RANGE) {
@@ -1153,6 +1201,40 @@ nc_status nc_op_quantize_e4m3(const void* x, nc_dtype dtype, int64_t rows, int32
            "bad sizes");
   NC_CHECK(dtype == NC_F32 || dtype == NC_BF16 || dtype == NC_F16, NC_ERR_INVALID_ARG, "bad dtype");
   return nc::quantize_e4m3(x, dtype, rows, cols, q, scale, static_cast<cudaStream_t>(stream));
+}
+
+size_t nc_op_cross_entropy_scratch_bytes(int32_t M, int32_t N) {
+  if (M < 0 || N <= 0) return 0;
+  return round_up((size_t)M * nc::lm_loss_blocks(N) * sizeof(float2), 256) +
+         2 * round_up((size_t)M * sizeof(float), 256);
+}
+
+nc_status nc_op_cross_entropy(const void* A, const void* B, const int32_t* targets, int32_t M,
+                              int32_t N, int32_t K, nc_dtype dtype, float* loss, float* mean,
+                              void* scratch, size_t scratch_bytes, void* stream) {
+  NC_CHECK(A && B && targets && mean && scratch && aligned16(A) && aligned16(B) &&
+               aligned16(scratch) && (reinterpret_cast<uintptr_t>(targets) & 3u) == 0 &&
+               (!loss || (reinterpret_cast<uintptr_t>(loss) & 3u) == 0) &&
+               (reinterpret_cast<uintptr_t>(mean) & 3u) == 0,
+           NC_ERR_INVALID_ARG, "NULL/misaligned");
+  NC_CHECK(M >= 0 && N > 0 && K > 0, NC_ERR_INVALID_ARG, "bad sizes");
+  NC_CHECK(dtype == NC_BF16 || dtype == NC_F16, NC_ERR_INVALID_ARG, "dtype must be NC_BF16 or NC_F16");
+  NC_CHECK(K % 64 == 0, NC_ERR_UNSUPPORTED, "needs K%%64==0");
+  NC_CHECK(scratch_bytes >= nc_op_cross_entropy_scratch_bytes(M, N), NC_ERR_INVALID_ARG,
+           "scratch too small");
+  cudaStream_t s = static_cast<cudaStream_t>(stream);
+  const size_t b_part = round_up((size_t)M * nc::lm_loss_blocks(N) * sizeof(float2), 256),
+               b_row = round_up((size_t)M * sizeof(float), 256);
+  char* ws = static_cast<char*>(scratch);
+  float2* part = reinterpret_cast<float2*>(ws);
+  float* zt = reinterpret_cast<float*>(ws + b_part);
+  float* rows = loss ? loss : reinterpret_cast<float*>(ws + b_part + b_row);
+  if (M > 0) {
+    nc_status st = nc::tc_cross_entropy(A, B, targets, M, N, K, dtype, part, zt, s);
+    if (st != NC_OK) return st;
+  }
+  nc::launch_ce_finish(part, nc::lm_loss_blocks(N), zt, targets, N, M, rows, mean, nullptr, s);
+  return check_launch();
 }
 
 size_t nc_op_gemv_e4m3_scratch_bytes(int32_t N, int32_t K, int32_t B) {

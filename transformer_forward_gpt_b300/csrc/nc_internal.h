@@ -84,6 +84,15 @@ void launch_attention_combine(const float* scratch, void* o, int BH, int hd, int
 void launch_convert16(const void* src, nc_dtype from, void* dst, nc_dtype to, int64_t n,
                       cudaStream_t s);
 void launch_argmax(const float* x, int rows, int n, int32_t* out, cudaStream_t s);
+// ---- next-token loss (loss.cu): loss[r] = log sum_nb s_nb exp(m_nb - M_r) + M_r
+// - zt[r] from the LM head's per-block softmax partials part[nb * M + r]; rows
+// whose target is outside [0, V) get 0 and are not counted (targets >= V also set
+// ST_BAD_TOKEN in status, if not NULL); mean = sum of the counted losses / their number
+// (NaN if none), summed in a fixed order.
+void launch_ce_finish(const float2* part, int nblk, const float* zt, const int32_t* targets,
+                      int V, int64_t M, float* loss, float* mean, uint32_t* status,
+                      cudaStream_t s);
+
 // ---- temperature sampling (sample.cu)
 void launch_sample(const float* logits, int B, int V, float temperature, const float* u,
                    int32_t* out, cudaStream_t s);

@@ -30,6 +30,13 @@ nc_status tc_proj(TcModel* t, int layer, int64_t M, float* x, float* part, cudaS
 // logits[M, V] = xn lm_head^T (xn is the model's xn or xnl buffer)
 nc_status tc_lm_head(TcModel* t, const void* xn, int64_t M, float* logits, float* part,
                      cudaStream_t s);
+// The same product reduced per row and block of 256 columns, no logits stored:
+// part[nb * M + r] = (max, sum exp(z - max)) over block nb of row r's logits, and
+// zt[r] = the logit of column targets[r] (written where 0 <= targets[r] < V).
+// part holds lm_loss_blocks(V) * M pairs.
+int lm_loss_blocks(int vocab);
+nc_status tc_lm_loss(TcModel* t, const void* xn, int64_t M, const int32_t* targets, float2* part,
+                     float* zt, cudaStream_t s);
 // Causal attention over q [B, H, T, 128], cache k/v [B, Hkv, t_max, 128] -> o [B, T, H*128].
 nc_status tc_attention_prefill(const void* q, const void* k, const void* v, void* o, int B, int H,
                                int Hkv, int T, int t_max, nc_dtype dt, cudaStream_t s);
@@ -43,13 +50,17 @@ nc_status tc_attention_prefill_tc(const void* q, const void* k, const void* v, v
                                   int H, int Hkv, int T, int pos0, int t_max, int n_layers,
                                   int64_t layer_stride, int layer, nc_dtype dt, uint32_t* status,
                                   cudaStream_t s);
-// C[M, N] = A[M, K] B[N, K]^T, fp32 out (single-step entry point).
 // fp8 (E4M3) projection variant: row-wise quantisation and the scaled product
 nc_status quantize_e4m3(const void* x, nc_dtype dt, int64_t rows, int cols, uint8_t* q, float* scale,
                         cudaStream_t s);
 size_t gemv_e4m3_scratch_bytes(int N, int K, int B);
 nc_status gemv_e4m3(const uint8_t* wq, const float* w_scale, int N, int K, const float* x, int B,
                     float* y, void* scratch, cudaStream_t s);
+// The cross-entropy reduction of C = A B^T against targets (single-step entry
+// point): part and zt as tc_lm_loss, for lm_loss_blocks(N) blocks.
+nc_status tc_cross_entropy(const void* A, const void* B, const int32_t* targets, int M, int N,
+                           int K, nc_dtype dt, float2* part, float* zt, cudaStream_t s);
+// C[M, N] = A[M, K] B[N, K]^T, fp32 out (single-step entry point).
 nc_status tc_gemm_f32out(const void* A, const void* B, float* C, int M, int N, int K, nc_dtype dt,
                          cudaStream_t s);
 

@@ -30,7 +30,7 @@
 
 namespace nc {
 
-enum Epi : int { EPI_F32 = 0, EPI_RESID = 1, EPI_RELU2 = 2, EPI_QKV = 3, EPI_SWAP = 4 };
+enum Epi : int { EPI_F32 = 0, EPI_RESID = 1, EPI_RELU2 = 2, EPI_QKV = 3, EPI_SWAP = 4, EPI_CE = 5 };
 
 struct GemmArgs {
   int M;                  // rows of the A operand
@@ -50,6 +50,8 @@ struct GemmArgs {
   int sk_groups;           // > 1 (stream-K): one group of CTAs per n block, see Sched
   const float* row_scale;  // EPI_SWAP with 8-bit operands: scale of each A row (feature)
   const float* tok_scale;  // and of each B row (token); NULL for 16-bit operands
+  const int32_t* targets;  // EPI_CE: target column of each row (out_f32: float2 partials)
+  float* ce_zt;            // EPI_CE: the target column's value of each row
 };
 
 // Work schedule shared by the three roles of a CTA: a sequence of segments
@@ -328,6 +330,50 @@ __device__ __forceinline__ void epi_swap(const GemmArgs& p, uint32_t taddr, int 
   }
 }
 
+// Cross-entropy epilogue: the thread's row of the tile's BN logits becomes the
+// pair (m, s) = (max z, sum exp(z - m)) over the columns below N, stored at
+// part[nb][row] (lanes of a warp write consecutive rows); the value of the
+// row's target column goes to ce_zt[row]. No logit leaves the SM.
+template <int BN>
+__device__ __forceinline__ void epi_ce(const GemmArgs& p, uint32_t taddr, int row, int nb) {
+  constexpr float kLog2e = 1.4426950408889634f;
+  const bool valid = row < p.M;
+  const int tgt = valid ? __ldg(p.targets + row) : -1;
+  float m = -INFINITY, s = 0.f;
+#pragma unroll 1
+  for (int c = 0; c < BN / 32; ++c) {
+    float v[32];
+    tmem_ld32_sync(taddr + c * 32, v);
+    const int n0 = nb * BN + c * 32;
+    if (n0 >= p.N) continue;   // uniform across the warp
+    const int nv = min(32, p.N - n0);
+    float cm = -INFINITY;
+#pragma unroll
+    for (int j = 0; j < 32; ++j)
+      if (j < nv) cm = fmaxf(cm, v[j]);
+    if (cm > m) {
+      s *= exp2f((m - cm) * kLog2e);   // 0 while m is -inf (s is 0 then)
+      m = cm;
+    }
+    // exp(z - m) = 2^(z log2 e - m log2 e), four independent partial sums
+    const float ml = m * kLog2e;
+    float s4[4] = {0.f, 0.f, 0.f, 0.f};
+#pragma unroll
+    for (int j = 0; j < 32; ++j)
+      if (j < nv) s4[j & 3] += exp2f(fmaf(v[j], kLog2e, -ml));
+    s += (s4[0] + s4[1]) + (s4[2] + s4[3]);
+    if (tgt >= n0 && tgt < n0 + nv) {
+      float z = 0.f;
+#pragma unroll
+      for (int j = 0; j < 32; ++j)
+        if (n0 + j == tgt) z = v[j];
+      p.ce_zt[row] = z;
+    }
+  }
+  if (valid)
+    reinterpret_cast<float2*>(p.out_f32)[(int64_t)nb * p.M + row] = make_float2(m, s);
+}
+
 // --------------------------------------------------------------------- kernel
 template <int BN, int EPI, class T16>
 __global__ void __launch_bounds__(192, 1)
@@ -489,6 +535,8 @@ __global__ void __launch_bounds__(192, 1)
         epi_swap<BN>(p, taddr, row, nb, ks);
       else if constexpr (EPI == EPI_QKV)
         epi_qkv<BN, T16>(p, taddr, row, nb);
+      else if constexpr (EPI == EPI_CE)
+        epi_ce<BN>(p, taddr, row, nb);
       else
         epi_store_rows<BN, T16>(p, taddr, epi_stage + quarter * 32 * C::kEpiStride,
                                 mb * 128 + quarter * 32, nb, EPI);
@@ -858,6 +906,29 @@ nc_status tc_lm_head(TcModel* t, const void* xn, int64_t M, float* logits, float
   return t->f16 ? lm_impl<f16>(t, xn, M, logits, s) : lm_impl<bf16>(t, xn, M, logits, s);
 }
 
+// The LM head's 128 x 256 tiles reduced in the epilogue to the softmax partials
+// of each (row, n block) and the target logits; tile mode for every M.
+template <class T16>
+static nc_status lm_loss_impl(TcModel* t, const void* xn, int64_t M, const int32_t* targets,
+                              float2* part, float* zt, cudaStream_t s) {
+  const nc_config& c = t->cfg;
+  CUtensorMap a;
+  if (!make_map<T16>(&a, xn, (uint64_t)M, c.d_model, 128)) return NC_ERR_CUDA;
+  GemmArgs args = base_args((int)M, c.vocab, c.d_model, 256, t->status);
+  args.out_f32 = reinterpret_cast<float*>(part);
+  args.targets = targets;
+  args.ce_zt = zt;
+  return tile_gemm<EPI_CE, T16>(a, t->lm, t->lm, t->lm, args, 256, t->sm_count, s);
+}
+
+int lm_loss_blocks(int vocab) { return (vocab + 255) / 256; }
+
+nc_status tc_lm_loss(TcModel* t, const void* xn, int64_t M, const int32_t* targets, float2* part,
+                     float* zt, cudaStream_t s) {
+  return t->f16 ? lm_loss_impl<f16>(t, xn, M, targets, part, zt, s)
+                : lm_loss_impl<bf16>(t, xn, M, targets, part, zt, s);
+}
+
 // ------------------------------------------------- fp8 (E4M3) projections
 static size_t align256(size_t x) { return (x + 255) / 256 * 256; }
 
@@ -957,6 +1028,24 @@ nc_status gemv_e4m3(const uint8_t* wq, const float* w_scale, int N, int K, const
   if (st != NC_OK) return st;
   launch_sum_splits(part, args.k_splits, y, B, N, N, s);
   return cudaGetLastError() == cudaSuccess ? NC_OK : NC_ERR_CUDA;
+}
+
+nc_status tc_cross_entropy(const void* A, const void* B, const int32_t* targets, int M, int N,
+                           int K, nc_dtype dt, float2* part, float* zt, cudaStream_t s) {
+  CUtensorMap a, b;
+  const bool h = dt == NC_F16;
+  const bool ok = h ? (make_map<f16>(&a, A, M, K, 128) && make_map<f16>(&b, B, N, K, 128))
+                    : (make_map<bf16>(&a, A, M, K, 128) && make_map<bf16>(&b, B, N, K, 128));
+  if (!ok) return NC_ERR_CUDA;
+  const int sm = sm_count_now();
+  GemmArgs args = base_args(M, N, K, 256, nullptr);
+  if (cudaGetSymbolAddress(reinterpret_cast<void**>(&args.status), g_op_status) != cudaSuccess)
+    return NC_ERR_CUDA;
+  args.out_f32 = reinterpret_cast<float*>(part);
+  args.targets = targets;
+  args.ce_zt = zt;
+  return h ? tile_gemm<EPI_CE, f16>(a, b, b, b, args, 256, sm, s)
+           : tile_gemm<EPI_CE, bf16>(a, b, b, b, args, 256, sm, s);
 }
 
 nc_status tc_gemm_f32out(const void* A, const void* B, float* C, int M, int N, int K,
