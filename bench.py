@@ -729,6 +729,45 @@ def run_op_gemv_fp8(args):
               f"(16-bit weights would be {2 * N * K / 1e6:.1f} MB, fp8 {N * K / 1e6:.1f} MB)", flush=True)
 
 
+def run_op_lm_loss(args):
+    """Profiling aid: the d20 LM head of B4 x T2048 (8192 x 65536 x 1280, fp16
+    operands, seeded N(0, 1) rows and N(0, 1/sqrt(K)) weights) through the C ABI,
+    first with its fp32 logits stored (nc_op_gemm), then reduced to the next-token
+    cross-entropy in the epilogue (nc_op_cross_entropy). Each is warmed up
+    max(3, --warmup) times and timed over --steps calls; prints the time per call and
+    the rate against the measured bf16 peak."""
+    import torch
+    from transformer_forward_gpt_b300 import binding as nc
+    peaks, src = load_peaks()
+    M, N, K = 8192, 65536, 1280
+    g = torch.Generator().manual_seed(0)
+    A = torch.randn(M, K, generator=g).to(torch.float16).cuda()
+    W = (torch.randn(N, K, generator=g) / K ** 0.5).to(torch.float16).cuda()
+    tgt = torch.randint(0, N, (M,), generator=g, dtype=torch.int32).cuda()
+    C = torch.empty(M, N, device="cuda")
+    loss = torch.empty(M, device="cuda")
+    mean = torch.empty(1, device="cuda")
+    nbytes = nc.nc_op_cross_entropy_scratch_bytes(M, N)
+    scratch = torch.empty(nbytes, dtype=torch.uint8, device="cuda")
+    calls = (("logits stored", lambda: nc.nc_op_gemm(A, W, C, M, N, K, nc.NC_F16)),
+             ("cross-entropy", lambda: nc.nc_op_cross_entropy(A, W, tgt, M, N, K, nc.NC_F16, loss,
+                                                              mean, scratch, nbytes)))
+    for name, fn in calls:
+        for _ in range(max(3, args.warmup)):
+            fn()
+        torch.cuda.synchronize()
+        e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+        e0.record()
+        for _ in range(args.steps):
+            fn()
+        e1.record()
+        torch.cuda.synchronize()
+        ms = e0.elapsed_time(e1) / args.steps
+        tf = 2.0 * M * N * K / (ms / 1e3) / 1e12
+        print(f"profiling aid: LM head {M}x{N}x{K}, {name}: {ms:.3f} ms per call, {tf:.0f} TFLOP/s "
+              f"= {tf / peaks['bf16_tflops']:.3f} of {src} bf16", flush=True)
+
+
 def main():
     ap = argparse.ArgumentParser(description=__doc__.splitlines()[0])
     ap.add_argument("--gpus", type=int, default=1)
@@ -745,7 +784,7 @@ def main():
                     help="profiling aid: smaller prefill batch (no JSON line)")
     ap.add_argument("--decode-steps", type=int, default=None,
                     help="profiling aid: fewer decode steps per step (no JSON line)")
-    ap.add_argument("--op", choices=("attention", "gemv-fp8"), default=None,
+    ap.add_argument("--op", choices=("attention", "gemv-fp8", "lm-loss"), default=None,
                     help="profiling aid: time one kernel on its own (no JSON line)")
     ap.add_argument("--cpu-budget", type=float, default=30.0)
     args = ap.parse_args()
@@ -757,6 +796,8 @@ def main():
         run_op_attention(args)
     elif args.op == "gemv-fp8":
         run_op_gemv_fp8(args)
+    elif args.op == "lm-loss":
+        run_op_lm_loss(args)
     else:
         run_ours(args)
 

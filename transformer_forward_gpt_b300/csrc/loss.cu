@@ -3,7 +3,7 @@
 // finished from the LM head's per-block softmax partials. The LM-head GEMM's
 // epilogue reduces each 256-column block of a row to (m, s) = (max z, sum
 // exp(z - m)) and keeps the target's logit, so the logits themselves are never
-// stored. Here one thread per row merges its blocks in order,
+// stored. Here one warp per row merges its blocks,
 //   M = max m_nb,  S = sum s_nb exp(m_nb - M),  loss = log S + M - z_target,
 // and one block sums the rows' losses in a fixed order for the mean.
 #include <math.h>
@@ -14,20 +14,24 @@
 namespace nc {
 namespace {
 
+// One warp per row: lane j merges blocks j, j + 32, ... in order, then the
+// lanes' pairs are merged by a butterfly (max first, then the rescaled sums).
 __global__ void ce_rows_kernel(const float2* __restrict__ part, int nblk, int64_t M,
                                const float* __restrict__ zt, const int32_t* __restrict__ targets,
                                int V, float* __restrict__ loss, uint32_t* status) {
-  const int64_t r = (int64_t)blockIdx.x * blockDim.x + threadIdx.x;
-  if (r >= M) return;
+  const int64_t r = ((int64_t)blockIdx.x * blockDim.x + threadIdx.x) / 32;
+  const int lane = threadIdx.x % 32;
+  if (r >= M) return;   // uniform across the warp
   const int t = targets[r];
   if (t < 0 || t >= V) {
-    loss[r] = 0.f;
-    if (t >= V && status) atomicOr(status, ST_BAD_TOKEN);
+    if (lane == 0) {
+      loss[r] = 0.f;
+      if (t >= V && status) atomicOr(status, ST_BAD_TOKEN);
+    }
     return;
   }
   float mx = -INFINITY, S = 0.f;
-#pragma unroll 8
-  for (int nb = 0; nb < nblk; ++nb) {
+  for (int nb = lane; nb < nblk; nb += 32) {
     const float2 q = part[(int64_t)nb * M + r];
     if (q.x > mx) {
       S = S * expf(mx - q.x) + q.y;   // S is 0 while mx is -inf
@@ -36,7 +40,13 @@ __global__ void ce_rows_kernel(const float2* __restrict__ part, int nblk, int64_
       S += q.y * expf(q.x - mx);
     }
   }
-  loss[r] = logf(S) + mx - zt[r];
+  float gm = mx;
+#pragma unroll
+  for (int o = 16; o > 0; o >>= 1) gm = fmaxf(gm, __shfl_xor_sync(0xffffffffu, gm, o));
+  S = mx > -INFINITY ? S * expf(mx - gm) : 0.f;
+#pragma unroll
+  for (int o = 16; o > 0; o >>= 1) S += __shfl_xor_sync(0xffffffffu, S, o);
+  if (lane == 0) loss[r] = logf(S) + gm - zt[r];
 }
 
 constexpr int kMeanThreads = 1024;
@@ -76,8 +86,8 @@ void launch_ce_finish(const float2* part, int nblk, const float* zt, const int32
                       int V, int64_t M, float* loss, float* mean, uint32_t* status,
                       cudaStream_t s) {
   if (M > 0)
-    ce_rows_kernel<<<(unsigned)((M + 255) / 256), 256, 0, s>>>(part, nblk, M, zt, targets, V, loss,
-                                                               status);
+    ce_rows_kernel<<<(unsigned)((M + 7) / 8), 256, 0, s>>>(part, nblk, M, zt, targets, V, loss,
+                                                           status);
   ce_mean_kernel<<<1, kMeanThreads, 0, s>>>(loss, targets, V, M, mean);
   count_launches(M > 0 ? 2 : 1);
 }
