@@ -89,3 +89,33 @@ def test_sample_and_continue_reject_bad_arguments_on_the_host(lib):
     with pytest.raises(binding.NcError) as e:
         binding.nc_prefill_continue(None, fake, 1, 4, fake, None, stream=0)
     assert e.value.code == binding.NC_ERR_INVALID_ARG
+
+
+def test_cross_entropy_scratch_and_host_checks(lib):
+    """Scratch of nc_op_cross_entropy: the per-block pairs (8 bytes per row and
+    256-column block) and two per-row arrays, each rounded up to 256 bytes; the
+    argument checks of the loss entry points return before any device call."""
+    def r256(x):
+        return (x + 255) // 256 * 256
+    for M, N in [(1, 1), (300, 1000), (8192, 65536), (37, 257)]:
+        want = r256(M * ((N + 255) // 256) * 8) + 2 * r256(M * 4)
+        assert binding.nc_op_cross_entropy_scratch_bytes(M, N) == want
+    assert binding.nc_op_cross_entropy_scratch_bytes(4, 0) == 0
+    assert binding.nc_op_cross_entropy_scratch_bytes(-1, 8) == 0
+    fake = 1 << 20   # 16-byte aligned, never dereferenced: the checks return first
+    ok = (fake, fake, fake, 4, 256, 64, binding.NC_BF16, None, fake, fake, 1 << 20)
+    for i, bad in [(2, None), (2, fake + 2), (8, None), (3, -1), (5, 0),
+                   (6, binding.NC_F32), (10, 16)]:
+        args = list(ok)
+        args[i] = bad
+        with pytest.raises(binding.NcError) as e:
+            binding.nc_op_cross_entropy(*args, stream=0)
+        assert e.value.code == binding.NC_ERR_INVALID_ARG, (i, bad)
+    args = list(ok)
+    args[5] = 48                                   # K not a multiple of 64
+    with pytest.raises(binding.NcError) as e:
+        binding.nc_op_cross_entropy(*args, stream=0)
+    assert e.value.code == binding.NC_ERR_UNSUPPORTED
+    with pytest.raises(binding.NcError) as e:
+        binding.nc_prefill_loss(None, fake, fake, 1, 4, None, fake, None, stream=0)
+    assert e.value.code == binding.NC_ERR_INVALID_ARG
