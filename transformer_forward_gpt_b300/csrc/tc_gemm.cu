@@ -21,6 +21,7 @@
 //     finishing kernel reduces (or, unsplit, the logits directly).
 #include <limits.h>
 #include <stdlib.h>
+#include <string.h>
 
 #include <algorithm>
 #include <vector>
@@ -52,6 +53,7 @@ struct GemmArgs {
   const float* tok_scale;  // and of each B row (token); NULL for 16-bit operands
   const int32_t* targets;  // EPI_CE: target column of each row (out_f32: float2 partials)
   float* ce_zt;            // EPI_CE: the target column's value of each row
+  int c_tma;               // EPI_F32: store C through its tensor map (tmC) by TMA
 };
 
 // Work schedule shared by the three roles of a CTA: a sequence of segments
@@ -140,7 +142,10 @@ struct TileCfg {
                                    : (2 * BN <= 256) ? 256 : 512;
   static constexpr int kEpiStride = 36;   // floats per staged row (16-byte aligned, conflict-free)
   static constexpr int kEpiBytes = 4 * 32 * kEpiStride * 4;
-  static constexpr size_t kSmemBytes = (size_t)kStages * kStageBytes + 1024 + 256 + kEpiBytes;
+  static constexpr int kEpiTmaBytes = 4 * 32 * 128;   // per warp 32 rows x 128 B, swizzled
+  // stages | barriers (1 KB) | epilogue staging (1024-aligned) ; + 1 KB of alignment slack
+  static constexpr size_t kSmemBytes = (size_t)kStages * kStageBytes + 1024 + 1024 +
+                                       (kEpiBytes > kEpiTmaBytes ? kEpiBytes : kEpiTmaBytes);
 };
 
 __device__ __forceinline__ const CUtensorMap* pick_map(const CUtensorMap* m0, const CUtensorMap* m1,
@@ -330,6 +335,37 @@ __device__ __forceinline__ void epi_swap(const GemmArgs& p, uint32_t taddr, int 
   }
 }
 
+// fp32 store of the tile through TMA: per 32-column chunk the warp writes its 32
+// rows x 128 bytes into a 1024-aligned staging area in the 128-byte swizzled
+// layout of the tensor map (16-byte chunk j of row r at position j ^ (r % 8)),
+// and one lane issues the bulk tensor store. The staging area is rewritten only
+// after the previous store has read it. Rows past M are clipped by the copy; a
+// slab that starts past M is skipped.
+template <int BN>
+__device__ __forceinline__ void epi_store_tma(const GemmArgs& p, const CUtensorMap* tmC,
+                                              uint32_t taddr, uint8_t* stage, int row0, int nb) {
+  const int lane = threadIdx.x % 32;
+#pragma unroll 1
+  for (int c = 0; c < BN / 32; ++c) {
+    float v[32];
+    tmem_ld32_sync(taddr + c * 32, v);
+    const int n0 = nb * BN + c * 32;
+    if (n0 >= p.N || row0 >= p.M) continue;   // uniform across the warp
+    if (lane == 0) bulk_wait_read_all();
+    __syncwarp();
+#pragma unroll
+    for (int j = 0; j < 8; ++j)
+      *reinterpret_cast<float4*>(stage + lane * 128 + ((j ^ (lane & 7)) << 4)) =
+          make_float4(v[4 * j], v[4 * j + 1], v[4 * j + 2], v[4 * j + 3]);
+    fence_proxy_async_smem();
+    __syncwarp();
+    if (lane == 0) {
+      tma_store_2d(tmC, stage, n0, row0);
+      bulk_commit();
+    }
+  }
+}
+
 // Cross-entropy epilogue: the thread's row of the tile's BN logits becomes the
 // pair (m, s) = (max z, sum exp(z - m)) over the columns below N, stored at
 // part[nb][row] (lanes of a warp write consecutive rows); the value of the
@@ -380,7 +416,7 @@ __global__ void __launch_bounds__(192, 1)
     gemm_tc_kernel(const __grid_constant__ CUtensorMap tmA0, const __grid_constant__ CUtensorMap tmA1,
                    const __grid_constant__ CUtensorMap tmA2, const __grid_constant__ CUtensorMap tmB0,
                    const __grid_constant__ CUtensorMap tmB1, const __grid_constant__ CUtensorMap tmB2,
-                   const GemmArgs p) {
+                   const __grid_constant__ CUtensorMap tmC, const GemmArgs p) {
   using C = TileCfg<BN>;
   constexpr int S = C::kStages;
   extern __shared__ uint8_t smem_raw[];
@@ -392,7 +428,7 @@ __global__ void __launch_bounds__(192, 1)
   uint64_t* tempty = tfull + 2;  // [2] accumulator drained by the epilogue
   uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(tempty + 2);
   volatile int* abort_flag = reinterpret_cast<volatile int*>(tmem_slot + 1);
-  float* epi_stage = reinterpret_cast<float*>(smem + S * C::kStageBytes + 256);
+  float* epi_stage = reinterpret_cast<float*>(smem + S * C::kStageBytes + 1024);
 
   const int warp = threadIdx.x / 32, lane = threadIdx.x % 32;
   if (threadIdx.x == 0) {
@@ -537,6 +573,10 @@ __global__ void __launch_bounds__(192, 1)
         epi_qkv<BN, T16>(p, taddr, row, nb);
       else if constexpr (EPI == EPI_CE)
         epi_ce<BN>(p, taddr, row, nb);
+      else if (EPI == EPI_F32 && p.c_tma)
+        epi_store_tma<BN>(p, &tmC, taddr,
+                          reinterpret_cast<uint8_t*>(epi_stage) + quarter * 32 * 128,
+                          mb * 128 + quarter * 32, nb);
       else
         epi_store_rows<BN, T16>(p, taddr, epi_stage + quarter * 32 * C::kEpiStride,
                                 mb * 128 + quarter * 32, nb, EPI);
@@ -548,6 +588,8 @@ __global__ void __launch_bounds__(192, 1)
         acc_phase ^= 1;
       }
     }
+    // the staging area must outlive the reads of the last bulk stores
+    if (EPI == EPI_F32 && p.c_tma && lane == 0) bulk_wait_all();
   }
   tc_fence_before();
   __syncthreads();
@@ -602,6 +644,22 @@ static bool make_map(CUtensorMap* map, const void* base, uint64_t rows, uint64_t
             CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
 }
 
+// fp32 matrix [rows, cols] with row pitch ld (elements) as the target of the
+// epilogue's TMA stores: boxes of 32 x 32 values, 128-byte swizzle. Needs a 16-byte
+// aligned base and ld % 4 == 0 (the caller falls back to plain stores otherwise).
+static bool make_store_map(CUtensorMap* map, float* base, uint64_t rows, uint64_t cols, uint64_t ld) {
+  EncodeTiledFn fn = encode_fn();
+  if (!fn || (reinterpret_cast<uintptr_t>(base) & 15u) || (ld % 4) || cols == 0 || rows == 0)
+    return false;
+  cuuint64_t dims[2] = {cols, rows};
+  cuuint64_t strides[1] = {ld * 4};
+  cuuint32_t box[2] = {32, 32};
+  cuuint32_t estr[2] = {1, 1};
+  return fn(map, CU_TENSOR_MAP_DATA_TYPE_FLOAT32, 2, base, dims, strides, box, estr,
+            CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B,
+            CU_TENSOR_MAP_L2_PROMOTION_NONE, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
+}
+
 struct LayerMaps {
   CUtensorMap wq, wk, wv, wo, wfc, wproj;
 };
@@ -627,13 +685,19 @@ static int sm_count_now() {
 template <int BN, int EPI, class T16>
 static nc_status launch_gemm(const CUtensorMap& a0, const CUtensorMap& a1, const CUtensorMap& a2,
                              const CUtensorMap& b0, const CUtensorMap& b1, const CUtensorMap& b2,
-                             const GemmArgs& args, int sm_count, cudaStream_t s) {
+                             const GemmArgs& args, int sm_count, cudaStream_t s,
+                             const CUtensorMap* c_map = nullptr) {
   using C = TileCfg<BN>;
   auto kern = gemm_tc_kernel<BN, EPI, T16>;
   if (!ensure_dyn_smem((const void*)kern, C::kSmemBytes)) return NC_ERR_CUDA;
   const int units = args.num_m_blk * args.num_n_blk * args.k_splits;
   const int grid = args.stream_k ? sm_count : std::min(units, sm_count);
-  kern<<<grid, 192, C::kSmemBytes, s>>>(a0, a1, a2, b0, b1, b2, args);
+  CUtensorMap cm;
+  memset(&cm, 0, sizeof(cm));
+  if (c_map) cm = *c_map;
+  GemmArgs a = args;
+  a.c_tma = (EPI == EPI_F32 && c_map) ? 1 : 0;
+  kern<<<grid, 192, C::kSmemBytes, s>>>(a0, a1, a2, b0, b1, b2, cm, a);
   count_launches(1);
   return cudaGetLastError() == cudaSuccess ? NC_OK : NC_ERR_CUDA;
 }
@@ -675,10 +739,10 @@ static int pick_bn(int M, int N, int sm_count) {
 template <int EPI, class T16>
 static nc_status tile_gemm(const CUtensorMap& a, const CUtensorMap& b0, const CUtensorMap& b1,
                            const CUtensorMap& b2, GemmArgs args, int BN, int sm_count,
-                           cudaStream_t s) {
+                           cudaStream_t s, const CUtensorMap* c_map = nullptr) {
   args.num_n_blk = (args.N + BN - 1) / BN;
-  if (BN == 256) return launch_gemm<256, EPI, T16>(a, a, a, b0, b1, b2, args, sm_count, s);
-  return launch_gemm<128, EPI, T16>(a, a, a, b0, b1, b2, args, sm_count, s);
+  if (BN == 256) return launch_gemm<256, EPI, T16>(a, a, a, b0, b1, b2, args, sm_count, s, c_map);
+  return launch_gemm<128, EPI, T16>(a, a, a, b0, b1, b2, args, sm_count, s, c_map);
 }
 
 // swap mode: features (weight rows, A) x tokens (B), split over K
@@ -839,7 +903,10 @@ static nc_status lm_impl(TcModel* t, const void* xn, int64_t M, float* logits, c
   GemmArgs args = base_args((int)M, V, d, 256, t->status);
   args.out_f32 = logits;
   args.ldo = V;
-  return tile_gemm<EPI_F32, T16>(a, t->lm, t->lm, t->lm, args, 256, t->sm_count, s);
+  CUtensorMap cmap;
+  const bool tma = make_store_map(&cmap, logits, (uint64_t)M, V, V);
+  return tile_gemm<EPI_F32, T16>(a, t->lm, t->lm, t->lm, args, 256, t->sm_count, s,
+                                 tma ? &cmap : nullptr);
 }
 
 template <class T16>
@@ -1062,8 +1129,10 @@ nc_status tc_gemm_f32out(const void* A, const void* B, float* C, int M, int N, i
     return NC_ERR_CUDA;
   args.out_f32 = C;
   args.ldo = N;
-  return h ? tile_gemm<EPI_F32, f16>(a, b, b, b, args, BN, sm, s)
-           : tile_gemm<EPI_F32, bf16>(a, b, b, b, args, BN, sm, s);
+  CUtensorMap cmap;
+  const CUtensorMap* cm = make_store_map(&cmap, C, M, N, N) ? &cmap : nullptr;
+  return h ? tile_gemm<EPI_F32, f16>(a, b, b, b, args, BN, sm, s, cm)
+           : tile_gemm<EPI_F32, bf16>(a, b, b, b, args, BN, sm, s, cm);
 }
 
 }  // namespace nc
