@@ -53,7 +53,7 @@ struct GemmArgs {
   const float* tok_scale;  // and of each B row (token); NULL for 16-bit operands
   const int32_t* targets;  // EPI_CE: target column of each row (out_f32: float2 partials)
   float* ce_zt;            // EPI_CE: the target column's value of each row
-  int c_tma;               // EPI_F32: store C through its tensor map (tmC) by TMA
+  int c_tma;               // EPI_F32, EPI_RELU2: store the output through tmC by TMA
 };
 
 // Work schedule shared by the three roles of a CTA: a sequence of segments
@@ -366,6 +366,49 @@ __device__ __forceinline__ void epi_store_tma(const GemmArgs& p, const CUtensorM
   }
 }
 
+// The same for the 16-bit ReLU^2 output: two 32-column chunks become one box of
+// 64 values per row (128 bytes, the same swizzled layout).
+template <int BN, class T16>
+__device__ __forceinline__ void epi_store_tma_relu2(const GemmArgs& p, const CUtensorMap* tmC,
+                                                    uint32_t taddr, uint8_t* stage, int row0,
+                                                    int nb) {
+  static_assert(BN % 64 == 0, "pairs of 32-column chunks");
+  const int lane = threadIdx.x % 32;
+#pragma unroll 1
+  for (int c = 0; c < BN / 64; ++c) {
+    uint32_t w[32];
+    float amax = 0.f;
+#pragma unroll
+    for (int hlf = 0; hlf < 2; ++hlf) {
+      float v[32];
+      tmem_ld32_sync(taddr + c * 64 + hlf * 32, v);
+#pragma unroll
+      for (int j = 0; j < 32; ++j) {
+        const float r = fmaxf(v[j], 0.f);
+        v[j] = r * r;
+        amax = fmaxf(amax, v[j]);
+      }
+#pragma unroll
+      for (int j = 0; j < 16; ++j) w[hlf * 16 + j] = pack2<T16>(v[2 * j], v[2 * j + 1]);
+    }
+    const int n0 = nb * BN + c * 64;
+    if (n0 >= p.N || row0 >= p.M) continue;   // uniform across the warp
+    if (row0 + lane < p.M) note_range<T16>(amax, p.status);
+    if (lane == 0) bulk_wait_read_all();
+    __syncwarp();
+#pragma unroll
+    for (int j = 0; j < 8; ++j)
+      *reinterpret_cast<uint4*>(stage + lane * 128 + ((j ^ (lane & 7)) << 4)) =
+          make_uint4(w[4 * j], w[4 * j + 1], w[4 * j + 2], w[4 * j + 3]);
+    fence_proxy_async_smem();
+    __syncwarp();
+    if (lane == 0) {
+      tma_store_2d(tmC, stage, n0, row0);
+      bulk_commit();
+    }
+  }
+}
+
 // Cross-entropy epilogue: the thread's row of the tile's BN logits becomes the
 // pair (m, s) = (max z, sum exp(z - m)) over the columns below N, stored at
 // part[nb][row] (lanes of a warp write consecutive rows); the value of the
@@ -577,6 +620,15 @@ __global__ void __launch_bounds__(192, 1)
         epi_store_tma<BN>(p, &tmC, taddr,
                           reinterpret_cast<uint8_t*>(epi_stage) + quarter * 32 * 128,
                           mb * 128 + quarter * 32, nb);
+      else if constexpr (EPI == EPI_RELU2 && BN % 64 == 0) {
+        if (p.c_tma)
+          epi_store_tma_relu2<BN, T16>(p, &tmC, taddr,
+                                       reinterpret_cast<uint8_t*>(epi_stage) + quarter * 32 * 128,
+                                       mb * 128 + quarter * 32, nb);
+        else
+          epi_store_rows<BN, T16>(p, taddr, epi_stage + quarter * 32 * C::kEpiStride,
+                                  mb * 128 + quarter * 32, nb, EPI);
+      }
       else
         epi_store_rows<BN, T16>(p, taddr, epi_stage + quarter * 32 * C::kEpiStride,
                                 mb * 128 + quarter * 32, nb, EPI);
@@ -589,7 +641,7 @@ __global__ void __launch_bounds__(192, 1)
       }
     }
     // the staging area must outlive the reads of the last bulk stores
-    if (EPI == EPI_F32 && p.c_tma && lane == 0) bulk_wait_all();
+    if ((EPI == EPI_F32 || EPI == EPI_RELU2) && p.c_tma && lane == 0) bulk_wait_all();
   }
   tc_fence_before();
   __syncthreads();
@@ -660,6 +712,22 @@ static bool make_store_map(CUtensorMap* map, float* base, uint64_t rows, uint64_
             CU_TENSOR_MAP_L2_PROMOTION_NONE, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
 }
 
+// 16-bit matrix [rows, cols] (pitch cols) as the target of the ReLU^2 epilogue's
+// TMA stores: boxes of 64 x 32 values (128-byte rows), 128-byte swizzle.
+template <class T16>
+static bool make_store_map16(CUtensorMap* map, void* base, uint64_t rows, uint64_t cols) {
+  EncodeTiledFn fn = encode_fn();
+  if (!fn || (reinterpret_cast<uintptr_t>(base) & 15u) || (cols % 8) || cols == 0 || rows == 0)
+    return false;
+  cuuint64_t dims[2] = {cols, rows};
+  cuuint64_t strides[1] = {cols * sizeof(T16)};
+  cuuint32_t box[2] = {64, 32};
+  cuuint32_t estr[2] = {1, 1};
+  return fn(map, MapType<T16>::v, 2, base, dims, strides, box, estr, CU_TENSOR_MAP_INTERLEAVE_NONE,
+            CU_TENSOR_MAP_SWIZZLE_128B, CU_TENSOR_MAP_L2_PROMOTION_NONE,
+            CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
+}
+
 struct LayerMaps {
   CUtensorMap wq, wk, wv, wo, wfc, wproj;
 };
@@ -696,7 +764,7 @@ static nc_status launch_gemm(const CUtensorMap& a0, const CUtensorMap& a1, const
   memset(&cm, 0, sizeof(cm));
   if (c_map) cm = *c_map;
   GemmArgs a = args;
-  a.c_tma = (EPI == EPI_F32 && c_map) ? 1 : 0;
+  a.c_tma = ((EPI == EPI_F32 || (EPI == EPI_RELU2 && BN % 64 == 0)) && c_map) ? 1 : 0;
   kern<<<grid, 192, C::kSmemBytes, s>>>(a0, a1, a2, b0, b1, b2, cm, a);
   count_launches(1);
   return cudaGetLastError() == cudaSuccess ? NC_OK : NC_ERR_CUDA;
@@ -855,7 +923,10 @@ static nc_status fc_impl(TcModel* t, int l, int64_t M, float* part, cudaStream_t
   GemmArgs args = base_args((int)M, F, d, BN, t->status);
   args.out_16 = t->h;
   args.ldo = F;
-  return tile_gemm<EPI_RELU2, T16>(a, w.wfc, w.wfc, w.wfc, args, BN, t->sm_count, s);
+  CUtensorMap hmap;
+  const bool tma = make_store_map16<T16>(&hmap, t->h, (uint64_t)M, F);
+  return tile_gemm<EPI_RELU2, T16>(a, w.wfc, w.wfc, w.wfc, args, BN, t->sm_count, s,
+                                   tma ? &hmap : nullptr);
 }
 
 template <class T16>
