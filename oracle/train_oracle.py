@@ -1,5 +1,5 @@
-"""fp64 CPU oracle of the training step's backward pass: the mean next-token loss of a
-batch and its gradient with respect to every parameter.
+"""fp64 CPU oracle of the training step: the mean next-token loss of a batch, its
+gradient with respect to every parameter (the backward pass), and the Adam update.
 
 TEST INFRASTRUCTURE. Only the tests may import this module; the product path never
 calls it and shares no code with it.
@@ -24,7 +24,9 @@ order:
 * residual x + f(x): the gradient passes to both;
 * embedding lookup: each position's dx is added into its token's row of d wte.
 
-Nothing is blocked or fused; numpy matmuls are the only library steps.
+The update (训练过程 item 4) is Adam with bias-corrected moment estimates
+(`adam_update`); `train_step` chains the three. Nothing is blocked or fused; numpy
+matmuls are the only library steps.
 """
 from __future__ import annotations
 
@@ -150,3 +152,45 @@ def loss_and_grads(cfg, wte, layers, lm_head, tokens, targets):
         np.add.at(d_wte, tokens[b], dx)
     loss = loss_sum / count if count else float("nan")
     return loss, {"wte": d_wte, "layers": [tuple(m) for m in d_layers], "lm_head": d_lm}
+
+
+def adam_update(w, g, m, v, t, lr, beta1=0.9, beta2=0.999, eps=1e-8):
+    """One Adam step (Kingma and Ba, "Adam: A Method for Stochastic Optimization",
+    Algorithm 1) for parameter w with gradient g, moment estimates m, v and step
+    count t >= 1 (this step's). The Microgpt summary (训练过程 item 4) says only that
+    Adam keeps the mean of the gradients and the mean of their squares; the
+    constants are the paper's defaults, a reading. Returns (w, m, v), new arrays:
+      m = beta1 m + (1 - beta1) g,  v = beta2 v + (1 - beta2) g^2,
+      w = w - lr (m / (1 - beta1^t)) / (sqrt(v / (1 - beta2^t)) + eps)."""
+    g = np.asarray(g, dtype=F64)
+    m = beta1 * np.asarray(m, dtype=F64) + (1.0 - beta1) * g
+    v = beta2 * np.asarray(v, dtype=F64) + (1.0 - beta2) * g * g
+    m_hat = m / (1.0 - beta1 ** t)
+    v_hat = v / (1.0 - beta2 ** t)
+    return np.asarray(w, dtype=F64) - lr * m_hat / (np.sqrt(v_hat) + eps), m, v
+
+
+def train_step(cfg, params, state, tokens, targets, lr):
+    """One iteration of the summary's training loop (训练过程 items 2-4): forward
+    pass and mean loss, gradients by backpropagation, one Adam step for every
+    parameter. params: {"wte", "layers" (list of 6-tuples), "lm_head"}; state: None
+    for the first step, else what the previous call returned. Returns (loss before
+    the step, new params, new state)."""
+    loss, g = loss_and_grads(cfg, params["wte"], params["layers"], params["lm_head"], tokens,
+                             targets)
+    flat_p = [params["wte"], params["lm_head"]] + [m for mats in params["layers"] for m in mats]
+    flat_g = [g["wte"], g["lm_head"]] + [m for mats in g["layers"] for m in mats]
+    if state is None:
+        state = {"t": 0, "m": [np.zeros_like(p, dtype=F64) for p in flat_p],
+                 "v": [np.zeros_like(p, dtype=F64) for p in flat_p]}
+    t = state["t"] + 1
+    new_p, new_m, new_v = [], [], []
+    for p, gp, m, v in zip(flat_p, flat_g, state["m"], state["v"]):
+        w, m, v = adam_update(p, gp, m, v, t, lr)
+        new_p.append(w)
+        new_m.append(m)
+        new_v.append(v)
+    n_l = len(params["layers"])
+    out = {"wte": new_p[0], "lm_head": new_p[1],
+           "layers": [tuple(new_p[2 + 6 * l: 8 + 6 * l]) for l in range(n_l)]}
+    return loss, out, {"t": t, "m": new_m, "v": new_v}

@@ -90,3 +90,48 @@ def test_zero_lm_head_gradient_in_closed_form():
     dz /= keep.sum()
     assert np.allclose(g["lm_head"], dz.T @ xnf, rtol=0, atol=1e-14)
     assert not np.any(g["wte"]) and not any(np.any(m) for mats in g["layers"] for m in mats)
+
+
+def test_adam_first_step_is_lr_times_sign():
+    """At t = 1 the bias-corrected moments are g and g^2, so the step is
+    lr g / (|g| + eps): lr times the sign of g up to eps."""
+    g = np.array([3.0, -0.5, 1e-3, 0.0])
+    w, m, v = TR.adam_update(np.zeros(4), g, np.zeros(4), np.zeros(4), 1, 0.01)
+    assert np.allclose(w, -0.01 * g / (np.abs(g) + 1e-8), rtol=1e-15, atol=0)
+    assert np.allclose(m, 0.1 * g) and np.allclose(v, 0.001 * g * g)
+    assert w[3] == 0.0
+
+
+def test_adam_constant_gradient_takes_equal_steps():
+    """With the same gradient every step, m_hat = g and v_hat = g^2 at every t."""
+    g = np.array([0.7, -2.0])
+    w, m, v = np.zeros(2), np.zeros(2), np.zeros(2)
+    prev = w
+    for t in range(1, 30):
+        w, m, v = TR.adam_update(w, g, m, v, t, 0.05)
+        assert np.allclose(w - prev, -0.05 * g / (np.abs(g) + 1e-8), rtol=1e-12, atol=0)
+        prev = w
+
+
+def test_adam_minimises_a_quadratic():
+    w, m, v = np.array([0.0]), np.zeros(1), np.zeros(1)
+    for t in range(1, 3001):
+        w, m, v = TR.adam_update(w, w - 3.0, m, v, t, 0.01)   # gradient of (w - 3)^2 / 2
+    assert abs(w[0] - 3.0) < 1e-3
+
+
+def test_training_steps_lower_the_loss():
+    """A few steps of the loop on the tiny model and one batch: the loss falls at
+    each step, and the parameters move only where the gradient is nonzero."""
+    shape = synth.TINY
+    W, toks, tgt = _setup(shape, 2, 8, 6)
+    params = {"wte": W.wte, "layers": W.layers, "lm_head": W.lm_head}
+    state = None
+    losses = []
+    for _ in range(5):
+        loss, new, state = TR.train_step(shape, params, state, toks, tgt, 1e-2)
+        losses.append(loss)
+        unused = np.setdiff1d(np.arange(shape.vocab), np.unique(toks))
+        assert np.array_equal(new["wte"][unused], np.asarray(params["wte"], np.float64)[unused])
+        params = new
+    assert all(b < a for a, b in zip(losses, losses[1:])), losses
